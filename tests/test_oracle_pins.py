@@ -1,0 +1,516 @@
+"""Pins for the fp64 CPU oracle: checks against what the pages and the
+mathematics fix, never against the oracle itself.
+
+Each test names the passage it follows ("vLLM 中 Attention Kernel 如何并行处理
+多个请求" is abbreviated "multi-request page"; "FlashAttention deep dive" is
+the vLLM backend page).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from varlen_flashattention_causal_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def cache_of(b, dtype=torch.bfloat16):
+    """Build CPU caches for batch b with the oracle's own KV write."""
+    if b.kv_dtype == "fp8":
+        dtype = torch.float8_e4m3fn
+    kc = torch.zeros((b.num_blocks, b.bs, b.Hkv, b.D), dtype=dtype)
+    vc = torch.zeros_like(kc)
+    oracle.kv_write(b.k_tok, b.v_tok, kc, vc, b.slot_mapping, b.k_scale, b.v_scale)
+    return kc, vc
+
+
+def run(b, kc=None, vc=None, **kw):
+    if kc is None:
+        kc, vc = cache_of(b)
+    return oracle.attention(b.q, kc, vc, b.cu_seqlens_q, b.seqused_k, b.block_table,
+                            b.softmax_scale, causal=b.causal, k_scale=b.k_scale,
+                            v_scale=b.v_scale, **kw)
+
+
+def key_rows(b, r):
+    """Token-major K/V rows of request r (the order they were written)."""
+    start = sum(b.kv_lens[:r])
+    n = b.kv_lens[r]
+    return b.k_tok[start:start + n], b.v_tok[start:start + n]
+
+
+def read_golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# --------------------------------------------------------------- worked examples
+
+def test_packed_6_4_mask_is_the_pages_matrix():
+    """multi-request page, sec. 1: the block-diagonal lower-triangular mask."""
+    rows = read_golden("packed_6_4_mask.txt")
+    want = np.array([[int(x) for x in r[1:]] for r in rows], dtype=bool)
+    q = np.zeros((10, 1, 4))
+    k = np.zeros((10, 1, 4))
+    _, _, mask = oracle.dense_masked_attention(q, k, k, [0, 6, 10], [0, 6, 10], 1.0)
+    assert (mask == want).all()
+
+
+def test_packed_6_4_oracle_equals_brute_force_and_isolation():
+    """multi-request page, sec. 1 and 5: packing A (6) and B (4) together
+    gives the same result as running each alone; changing B's inputs leaves
+    A's outputs bit-identical and vice versa."""
+    b = W.make_batch([6, 4], [6, 4], Hq=4, Hkv=2, D=16, bs=16, seed=1)
+    out, lse = run(b)
+    ref, ref_lse, _ = oracle.dense_masked_attention(
+        b.q.double(), b.k_tok.double(), b.v_tok.double(), [0, 6, 10], [0, 6, 10], b.softmax_scale)
+    np.testing.assert_allclose(out.numpy(), ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse.numpy(), ref_lse, rtol=0, atol=1e-12)
+
+    # perturb request B only (its queries and its cached K/V)
+    b2 = W.make_batch([6, 4], [6, 4], Hq=4, Hkv=2, D=16, bs=16, seed=1)
+    b2.q[6:] = W.randn((4, 4, 16), torch.Generator().manual_seed(7))
+    b2.k_tok[6:] = -b2.k_tok[6:]
+    b2.v_tok[6:] = 3 * b2.v_tok[6:]
+    out2, lse2 = run(b2)
+    assert torch.equal(out2[:6], out[:6]) and torch.equal(lse2[:6], lse[:6])
+    assert not torch.equal(out2[6:], out[6:])
+    # and the other way round
+    b3 = W.make_batch([6, 4], [6, 4], Hq=4, Hkv=2, D=16, bs=16, seed=1)
+    b3.k_tok[:6] = 2 * b3.k_tok[:6]
+    out3, lse3 = run(b3)
+    assert torch.equal(out3[6:], out[6:]) and torch.equal(lse3[6:], lse[6:])
+
+    # each request alone
+    for r, (lo, hi) in enumerate([(0, 6), (6, 10)]):
+        single = W.make_batch([hi - lo], [hi - lo], Hq=4, Hkv=2, D=16, bs=16, seed=1)
+        single.q = b.q[lo:hi].clone()
+        single.k_tok, single.v_tok = key_rows(b, r)
+        o1, l1 = run(single)
+        assert torch.equal(o1, out[lo:hi]) and torch.equal(l1, lse[lo:hi])
+
+
+def test_multi_token_verify_equals_six_decodes():
+    """multi-request page, sec. 10: 6 new positions over 20,000 cached
+    tokens.  Each query row equals an independent decode at its position,
+    and sees exactly the number of keys the page's picture gives."""
+    g = read_golden("verify_6_over_20000.txt")
+    ctx, q_len = int(g[0][1]), int(g[1][1])
+    nvis = {int(a): int(c) for a, c in g[2:]}
+    b = W.make_batch([q_len], [ctx + q_len], Hq=2, Hkv=1, D=16, bs=64, seed=2)
+    kc, vc = cache_of(b)
+    out, lse = run(b, kc, vc)
+    for i in range(q_len):
+        dec = W.make_batch([1], [nvis[i]], Hq=2, Hkv=1, D=16, bs=64, seed=2)
+        dec.q = b.q[i:i + 1].clone()
+        dec.block_table = b.block_table
+        dec.num_blocks = b.num_blocks
+        o, l = run(dec, kc, vc)
+        np.testing.assert_allclose(o.numpy(), out[i:i + 1].numpy(), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l.numpy(), lse[i:i + 1].numpy(), rtol=0, atol=1e-12)
+    # the visible-count column: with q = 0 every visible key scores 0, so
+    # lse = ln(number of visible keys)
+    b.q.zero_()
+    _, lse0 = run(b, kc, vc)
+    for i in range(q_len):
+        assert abs(float(lse0[i, 0]) - math.log(nvis[i])) < 1e-12
+
+
+def test_paged_lookup_example():
+    """multi-request page, sec. 11: position 1024 -> physical block 37 for
+    request A and 912 for request B; the KV write puts the token there and
+    the attention read finds it there."""
+    g = read_golden("paged_lookup.txt")
+    pos, blkA, blkB = int(g[0][1]), int(g[1][1]), int(g[2][1])
+    bs, Hkv, D = 16, 1, 16
+    nb = 1024
+    logical = pos // bs
+    bt = torch.full((2, logical + 1), -1, dtype=torch.int32)
+    rng = torch.Generator().manual_seed(3)
+    others = [x for x in torch.randperm(nb, generator=rng).tolist() if x not in (blkA, blkB)]
+    bt[0, :logical] = torch.tensor(others[:logical], dtype=torch.int32)
+    bt[1, :logical] = torch.tensor(others[logical:2 * logical], dtype=torch.int32)
+    bt[0, logical], bt[1, logical] = blkA, blkB
+    slot = torch.tensor([blkA * bs + pos % bs, blkB * bs + pos % bs], dtype=torch.int64)
+    k = W.randn((2, Hkv, D), rng)
+    v = W.randn((2, Hkv, D), rng)
+    kc = torch.zeros((nb, bs, Hkv, D), dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    oracle.kv_write(k, v, kc, vc, slot)
+    assert torch.equal(kc[blkA, pos % bs], k[0]) and torch.equal(kc[blkB, pos % bs], k[1])
+    assert torch.equal(vc[blkA, pos % bs], v[0]) and torch.equal(vc[blkB, pos % bs], v[1])
+    assert int(torch.count_nonzero(kc.float())) == int(torch.count_nonzero(k.float()))
+    # read back through the block table: with q = 0 all pos + 1 visible keys
+    # score equally and every other cached row is zero
+    q = torch.zeros((2, 1, D), dtype=torch.bfloat16)
+    cu = torch.tensor([0, 1, 2], dtype=torch.int32)
+    su = torch.tensor([pos + 1, pos + 1], dtype=torch.int32)
+    out, _ = oracle.attention(q, kc, vc, cu, su, bt, 1.0, causal=True)
+    np.testing.assert_allclose(out[:, 0].numpy(), (v[:, 0].double() / (pos + 1)).numpy(),
+                               rtol=0, atol=1e-15)
+
+
+# -------------------------------------------------------------- closed forms
+
+def test_single_key_returns_v0_exactly():
+    """Row 0 of a causal request with no cached context sees only key 0:
+    out = V_0 exactly and lse = scale * q . K_0."""
+    b = W.make_batch([5, 3], [5, 3], Hq=4, Hkv=2, D=32, bs=16, seed=4)
+    out, lse = run(b)
+    for r, t in enumerate([0, 5]):
+        k, v = key_rows(b, r)
+        for h in range(4):
+            g = h // 2
+            assert torch.equal(out[t, h], v[0, g].double())
+            s = b.softmax_scale * float((b.q[t, h].double() * k[0, g].double()).sum())
+            assert abs(float(lse[t, h]) - s) < 1e-12
+
+
+def test_two_keys_closed_form():
+    """Two visible keys: out = sigmoid(s0 - s1) V_0 + sigmoid(s1 - s0) V_1."""
+    b = W.make_batch([2], [2], Hq=1, Hkv=1, D=8, bs=16, seed=5)
+    out, lse = run(b)
+    k, v = key_rows(b, 0)
+    qd, kd, vd = b.q[1, 0].double(), k[:, 0].double(), v[:, 0].double()
+    s0 = b.softmax_scale * float(qd @ kd[0])
+    s1 = b.softmax_scale * float(qd @ kd[1])
+    w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    want = w0 * vd[0] + (1.0 - w0) * vd[1]
+    np.testing.assert_allclose(out[1, 0].numpy(), want.numpy(), rtol=0, atol=1e-14)
+    assert abs(float(lse[1, 0]) - (s0 + math.log1p(math.exp(s1 - s0)))) < 1e-13
+
+
+@pytest.mark.parametrize("ctx", [0, 13])
+def test_equal_scores_give_mean_of_visible_values(ctx):
+    """q = 0 makes every visible score 0: out = mean of the visible V rows
+    and lse = ln(#visible).  With cached context ctx, query i sees ctx+i+1
+    keys (bottom-right alignment, multi-request page sec. 10)."""
+    q_len = 7
+    b = W.make_batch([q_len], [ctx + q_len], Hq=2, Hkv=2, D=16, bs=16, seed=6)
+    b.q.zero_()
+    out, lse = run(b)
+    _, v = key_rows(b, 0)
+    for i in range(q_len):
+        n = ctx + i + 1
+        for h in range(2):
+            np.testing.assert_allclose(out[i, h].numpy(), v[:n, h].double().mean(0).numpy(),
+                                       rtol=0, atol=1e-14)
+            assert abs(float(lse[i, h]) - math.log(n)) < 1e-13
+
+
+def test_gqa_head_mapping():
+    """Query head h reads KV head h // (Hq / Hkv).  Each KV head holds a
+    different constant value row, so with q = 0 the output of head h is
+    exactly that constant."""
+    Hq, Hkv = 8, 2
+    b = W.make_batch([3], [3], Hq=Hq, Hkv=Hkv, D=16, bs=16, seed=7)
+    b.q.zero_()
+    for g in range(Hkv):
+        b.v_tok[:, g, :] = float(g + 1)
+    out, _ = run(b)
+    for h in range(Hq):
+        assert torch.equal(out[:, h], torch.full((3, 16), float(h // (Hq // Hkv) + 1), dtype=torch.float64))
+
+
+def test_non_causal_sees_every_key():
+    """causal=False (the cascade prefix stage): every query sees all keys."""
+    b = W.make_batch([4], [9], Hq=2, Hkv=1, D=16, bs=16, seed=8, causal=False)
+    b.q.zero_()
+    out, lse = run(b)
+    _, v = key_rows(b, 0)
+    for i in range(4):
+        np.testing.assert_allclose(out[i, 0].numpy(), v[:, 0].double().mean(0).numpy(), atol=1e-14)
+        assert abs(float(lse[i, 0]) - math.log(9)) < 1e-13
+
+
+def test_empty_kv_gives_zero_and_minus_inf():
+    """No visible key: out 0, lse -inf (reading adopted for kv_len = 0)."""
+    b = W.make_batch([1, 1], [0, 4], Hq=2, Hkv=1, D=16, bs=16, seed=9)
+    out, lse = run(b)
+    assert torch.equal(out[0], torch.zeros((2, 16), dtype=torch.float64))
+    assert lse[0].tolist() == [-math.inf, -math.inf]
+    assert torch.isfinite(lse[1]).all()
+
+
+# ------------------------------------------------------------ brute force
+
+@pytest.mark.parametrize("seed,causal", [(10, True), (11, True), (12, False)])
+def test_oracle_equals_dense_brute_force(seed, causal):
+    """Random varlen batch with cached context and GQA: the per-row paged
+    oracle equals the dense whole-matrix formulation."""
+    rng = np.random.default_rng(seed)
+    B = 4
+    q_lens = rng.integers(1, 9, B).tolist()
+    ctx = rng.integers(0, 20, B).tolist()
+    kv = [c + q for c, q in zip(ctx, q_lens)]
+    b = W.make_batch(q_lens, kv, Hq=6, Hkv=2, D=32, bs=16, seed=seed, causal=causal)
+    out, lse = run(b)
+    # the cached rows of request r are its kv_len tokens in position order
+    cuk = [0] + np.cumsum(kv).tolist()
+    ref, ref_lse, _ = oracle.dense_masked_attention(
+        b.q.double(), b.k_tok.double(), b.v_tok.double(),
+        b.cu_seqlens_q.tolist(), cuk, b.softmax_scale, causal=causal)
+    np.testing.assert_allclose(out.numpy(), ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse.numpy(), ref_lse, rtol=0, atol=1e-12)
+
+
+def test_online_softmax_recurrence_matches():
+    """multi-request page, sec. 7: the online recurrence over K/V tiles
+    (m_new = max(m, rowmax S), alpha = e^(m - m_new), l = alpha l + sum p,
+    O = alpha O + p V, out = O / l) equals the oracle's two-pass softmax for
+    any tiling."""
+    b = W.make_batch([5], [40], Hq=1, Hkv=1, D=16, bs=16, seed=13)
+    out, lse = run(b)
+    k, v = key_rows(b, 0)
+    kd, vd = k[:, 0].double().numpy(), v[:, 0].double().numpy()
+    for tile in (1, 3, 16, 40):
+        for i in range(5):
+            qi = b.q[i, 0].double().numpy()
+            n = 35 + i + 1
+            m, l, o = -np.inf, 0.0, np.zeros(16)
+            for j0 in range(0, n, tile):
+                s = b.softmax_scale * (kd[j0:min(n, j0 + tile)] @ qi)
+                m_new = max(m, s.max())
+                alpha = math.exp(m - m_new) if m > -np.inf else 0.0
+                p = np.exp(s - m_new)
+                l = alpha * l + p.sum()
+                o = alpha * o + p @ vd[j0:min(n, j0 + tile)]
+                m = m_new
+            np.testing.assert_allclose(o / l, out[i, 0].numpy(), rtol=0, atol=1e-13)
+            assert abs(m + math.log(l) - float(lse[i, 0])) < 1e-12
+
+
+# ------------------------------------------------------------- invariances
+
+def test_paged_equals_contiguous_and_any_block_size():
+    """vAttention notes (virtually contiguous KV) and multi-request page
+    sec. 11: the block-table walk is pure addressing, so a randomly permuted
+    paged layout at any block size gives bit-identical fp64 results to a
+    contiguous layout (one block per request)."""
+    q_lens, kv = [3, 1, 6], [50, 17, 70]
+    ref = W.make_batch(q_lens, kv, Hq=4, Hkv=2, D=16, bs=16, seed=14)
+    out_ref, lse_ref = run(ref)
+    for bs in (32, 64, 256, 80):
+        b = W.make_batch(q_lens, kv, Hq=4, Hkv=2, D=16, bs=bs, seed=14)
+        b.q, b.k_tok, b.v_tok = ref.q, ref.k_tok, ref.v_tok
+        o, l = run(b)
+        assert torch.equal(o, out_ref) and torch.equal(l, lse_ref)
+    # contiguous: request r is physical block r, block size >= every kv_len
+    bsz = 80
+    c = W.make_batch(q_lens, kv, Hq=4, Hkv=2, D=16, bs=bsz, seed=14)
+    c.q, c.k_tok, c.v_tok = ref.q, ref.k_tok, ref.v_tok
+    c.num_blocks = 3
+    c.block_table = torch.arange(3, dtype=torch.int32).view(3, 1)
+    c.slot_mapping = torch.cat([torch.arange(L) + r * bsz for r, L in enumerate(kv)]).to(torch.int64)
+    o, l = run(c)
+    assert torch.equal(o, out_ref) and torch.equal(l, lse_ref)
+
+
+def _decode_split(b, kc, vc, split_blocks):
+    """Attention of the decode query over keys [0, a) and [a, kv) separately,
+    using a column-offset view of the block table for the second part
+    (the cascade suffix trick, FlashAttention deep dive, cascade stage 2)."""
+    a = split_blocks * b.bs
+    lo = oracle.attention(b.q, kc, vc, b.cu_seqlens_q, torch.tensor([a], dtype=torch.int32),
+                          b.block_table, b.softmax_scale, causal=False)
+    hi_bt = b.block_table[:, split_blocks:].contiguous()
+    hi = oracle.attention(b.q, kc, vc, b.cu_seqlens_q, b.seqused_k - a, hi_bt,
+                          b.softmax_scale, causal=False)
+    return lo, hi
+
+
+def test_split_kv_merge_equals_unsplit():
+    """multi-request page sec. 12 and the merge formula of the vLLM backend
+    page: splitting the keys into segments and merging by log-sum-exp gives
+    the unsplit result."""
+    b = W.make_batch([1], [300], Hq=4, Hkv=2, D=32, bs=16, seed=15)
+    kc, vc = cache_of(b)
+    full, full_lse = run(b, kc, vc)
+    for split_blocks in (1, 7, 18):
+        (o1, l1), (o2, l2) = _decode_split(b, kc, vc, split_blocks)
+        o, l = oracle.merge_states(o1.view(-1, 32), l1.view(-1), o2.view(-1, 32), l2.view(-1))
+        np.testing.assert_allclose(o.numpy(), full.view(-1, 32).numpy(), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l.numpy(), full_lse.view(-1).numpy(), rtol=0, atol=1e-12)
+    # three segments, merged pairwise in either order
+    a, c = 5 * 16, 12 * 16
+    segs = []
+    for lo_b, hi_tok in ((0, a), (5, c - a), (12, 300 - c)):
+        bt = b.block_table[:, lo_b:].contiguous()
+        segs.append(oracle.attention(b.q, kc, vc, b.cu_seqlens_q,
+                                     torch.tensor([hi_tok], dtype=torch.int32), bt,
+                                     b.softmax_scale, causal=False))
+    (o1, l1), (o2, l2), (o3, l3) = [(o.view(-1, 32), l.view(-1)) for o, l in segs]
+    o12, l12 = oracle.merge_states(o1, l1, o2, l2)
+    oa, la = oracle.merge_states(o12, l12, o3, l3)
+    o23, l23 = oracle.merge_states(o2, l2, o3, l3)
+    ob, lb = oracle.merge_states(o1, l1, o23, l23)
+    for o, l in ((oa, la), (ob, lb)):
+        np.testing.assert_allclose(o.numpy(), full.view(-1, 32).numpy(), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l.numpy(), full_lse.view(-1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_cascade_prefix_suffix_merge_equals_full():
+    """vLLM backend page, cascade attention: stage 1 (all queries vs the
+    shared prefix, non-causal, block_table[:1]), stage 2 (each request's
+    suffix, causal, block_table[:, num_common_kv_blocks:]), stage 3 (merge)
+    equals attention over prefix + suffix."""
+    b = W.cascade_decode(B=6, prefix=128, lo=20, hi=70)
+    b.bs = 64
+    kc, vc = cache_of(b)
+    full, full_lse = run(b, kc, vc)
+    T, Hq, D = b.q.shape
+    pre = oracle.attention(b.q, kc, vc, torch.tensor([0, T], dtype=torch.int32),
+                           torch.tensor([128], dtype=torch.int32), b.block_table[:1],
+                           b.softmax_scale, causal=False)
+    nblk = 128 // b.bs
+    suf = oracle.attention(b.q, kc, vc, b.cu_seqlens_q, b.seqused_k - 128,
+                           b.block_table[:, nblk:].contiguous(), b.softmax_scale, causal=True)
+    o, l = oracle.merge_states(pre[0].view(-1, D), pre[1].view(-1), suf[0].view(-1, D), suf[1].view(-1))
+    np.testing.assert_allclose(o.numpy(), full.view(-1, D).numpy(), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l.numpy(), full_lse.view(-1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_decode_equals_last_prefill_row():
+    """multi-request page sec. 9: the decode query is the last row of the
+    causal matrix, whose mask is all ones."""
+    b = W.make_batch([9], [9], Hq=4, Hkv=1, D=16, bs=16, seed=16)
+    kc, vc = cache_of(b)
+    out, lse = run(b, kc, vc)
+    d = W.make_batch([1], [9], Hq=4, Hkv=1, D=16, bs=16, seed=16)
+    d.q = b.q[8:9].clone()
+    d.block_table, d.num_blocks = b.block_table, b.num_blocks
+    o, l = run(d, kc, vc)
+    assert torch.equal(o[0], out[8]) and torch.equal(l[0], lse[8])
+
+
+def test_row_subset_matches_full():
+    b = W.make_batch([4, 6], [10, 6], Hq=2, Hkv=1, D=16, bs=16, seed=17)
+    out, lse = run(b)
+    rows = [9, 0, 4]
+    o, l = run(b, rows=rows)
+    assert torch.equal(o, out[rows]) and torch.equal(l, lse[rows])
+
+
+# ------------------------------------------------------------------- merge
+
+def test_merge_special_cases():
+    rng = np.random.default_rng(18)
+    o1, o2 = rng.normal(size=(3, 8)), rng.normal(size=(3, 8))
+    l1 = np.array([-np.inf, 0.5, -np.inf])
+    l2 = np.array([1.25, -np.inf, -np.inf])
+    o, l = oracle.merge_states(torch.tensor(o1), torch.tensor(l1), torch.tensor(o2), torch.tensor(l2))
+    assert np.array_equal(o[0].numpy(), o2[0]) and l[0] == 1.25
+    assert np.array_equal(o[1].numpy(), o1[1]) and l[1] == 0.5
+    assert np.array_equal(o[2].numpy(), np.zeros(8)) and l[2] == -np.inf
+    # equal lse: plain average, lse + ln 2
+    le = np.array([0.3, 0.3, 0.3])
+    o, l = oracle.merge_states(torch.tensor(o1), torch.tensor(le), torch.tensor(o2), torch.tensor(le))
+    np.testing.assert_allclose(o.numpy(), 0.5 * (o1 + o2), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(l.numpy(), 0.3 + math.log(2.0), rtol=0, atol=1e-15)
+    # large lse values do not overflow
+    lb = np.array([900.0, 1000.0, -1000.0])
+    o, l = oracle.merge_states(torch.tensor(o1), torch.tensor(lb), torch.tensor(o2), torch.tensor(lb - 1.0))
+    w = 1.0 / (1.0 + math.exp(-1.0))
+    np.testing.assert_allclose(o.numpy(), w * o1 + (1 - w) * o2, rtol=0, atol=1e-12)
+
+
+# -------------------------------------------------------------------- fp8
+
+def _e4m3_brute(x: float) -> int:
+    """Nearest e4m3 code by exhaustive search over the finite positive codes,
+    ties to the even code (= even mantissa, codes are monotone in value),
+    |x| >= 448 saturating."""
+    a = abs(x)
+    sign = 0x80 if math.copysign(1.0, x) < 0 else 0
+    vals = [(c, _e4m3_value_by_definition(c)) for c in range(0x7F)]
+    if a >= 448.0:
+        return sign | 0x7E
+    best = min(vals, key=lambda cv: (abs(a - cv[1]), cv[0] & 1))
+    return sign | best[0]
+
+
+def _e4m3_value_by_definition(c):
+    e, m = (c >> 3) & 15, c & 7
+    v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+    return -v if c & 0x80 else v
+
+
+def test_e4m3_decode_known_values():
+    """FlashAttention deep dive, FP8 support: float8_e4m3fn (bias 7, no inf)."""
+    assert oracle.e4m3_to_double(0x7E) == 448.0
+    assert oracle.e4m3_to_double(0xFE) == -448.0
+    assert oracle.e4m3_to_double(0x38) == 1.0
+    assert oracle.e4m3_to_double(0x08) == 2.0 ** -6
+    assert oracle.e4m3_to_double(0x01) == 2.0 ** -9
+    assert oracle.e4m3_to_double(0x00) == 0.0
+    assert math.isnan(oracle.e4m3_to_double(0x7F))
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        assert oracle.e4m3_to_double(c) == _e4m3_value_by_definition(c)
+    # torch's independent table
+    codes = torch.tensor([c for c in range(256) if c & 0x7F != 0x7F], dtype=torch.uint8)
+    tv = codes.view(torch.float8_e4m3fn).double()
+    assert [oracle.e4m3_to_double(int(c)) for c in codes] == tv.tolist()
+
+
+def test_e4m3_encode_matches_brute_force_and_torch():
+    rng = np.random.default_rng(19)
+    xs = list(rng.normal(scale=50.0, size=600)) + list(rng.normal(scale=0.01, size=300))
+    # exact midpoints between neighbouring codes (ties) and the subnormal range
+    for c in range(0x7D):
+        lo, hi = _e4m3_value_by_definition(c), _e4m3_value_by_definition(c + 1)
+        xs += [0.5 * (lo + hi), -0.5 * (lo + hi), lo, hi * 0.999]
+    xs += [0.0, -0.0, 447.9, 448.0, 449.0, 463.9, 464.0, 1e6, -1e6, 2.0 ** -10, 2.0 ** -11]
+    xs = [float(np.float32(x)) for x in xs]
+    for x in xs:
+        assert oracle.e4m3_from_float(x) == _e4m3_brute(x), x
+    inrange = torch.tensor([x for x in xs if abs(x) <= 448.0], dtype=torch.float32)
+    want = inrange.to(torch.float8_e4m3fn).view(torch.uint8).tolist()
+    got = [oracle.e4m3_from_float(float(x)) for x in inrange]
+    assert got == want
+
+
+def test_fp8_kv_write_quantizes_x_over_scale():
+    """FlashAttention deep dive, KV cache update: reshape_and_cache_flash
+    with k_scale / v_scale.  Reading adopted: store e4m3(x / scale) with the
+    division in fp32."""
+    b = W.make_batch([2], [20], Hq=2, Hkv=2, D=16, bs=16, seed=20, kv_dtype="fp8")
+    kc, vc = cache_of(b)
+    kb = kc.view(torch.uint8)
+    for t in (0, 7, 19):
+        slot = int(b.slot_mapping[t])
+        for h in range(2):
+            for d in (0, 5, 15):
+                x = np.float32(b.k_tok[t, h, d].float().item()) / np.float32(b.k_scale)
+                assert int(kb[slot // 16, slot % 16, h, d]) == _e4m3_brute(float(x))
+    # dequantised attention with an fp8 cache is the bf16 formula applied to
+    # the widened values times the scale
+    out, _ = run(b, kc, vc)
+    deq_k = kc.double() * b.k_scale
+    deq_v = vc.double() * b.v_scale
+    q, s = b.q.double(), b.softmax_scale
+    bt = b.block_table[0]
+    rows_k = torch.stack([deq_k[bt[j // 16], j % 16] for j in range(20)])
+    rows_v = torch.stack([deq_v[bt[j // 16], j % 16] for j in range(20)])
+    for i in range(2):
+        for h in range(2):
+            n = 18 + i + 1
+            sc = s * (rows_k[:n, h] @ q[i, h])
+            p = torch.softmax(sc, 0)
+            np.testing.assert_allclose(out[i, h].numpy(), (p @ rows_v[:n, h]).numpy(), atol=1e-12)
+
+
+def test_kv_write_skips_negative_slots_and_rejects_out_of_range():
+    k = W.randn((3, 1, 16), torch.Generator().manual_seed(21))
+    kc = torch.zeros((2, 16, 1, 16), dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    oracle.kv_write(k, k, kc, vc, torch.tensor([5, -1, 17]))
+    assert torch.equal(kc[0, 5, 0], k[0, 0]) and torch.equal(kc[1, 1, 0], k[2, 0])
+    assert int(torch.count_nonzero(kc.float())) == 32
+    with pytest.raises(ValueError):
+        oracle.kv_write(k, k, kc, vc, torch.tensor([0, 1, 32]))
