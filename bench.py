@@ -1,0 +1,402 @@
+"""Benchmark of the attention hot path on one GB300 (or N independent ranks).
+
+A step is one paged-decode step of the Llama-3-8B-shaped workload (64
+requests, one new token each, 32 query / 8 KV heads, head size 128, bf16,
+contexts U[512, 4096], block size 16, 40960-block pool): write the 64 new
+tokens' K/V through slot_mapping, then attention over the paged cache
+(split-KV kernel + combine).  `value` is algorithmic HBM bytes per step over
+the device time per step (GB/s).  The chunked varlen prefill (16 requests,
+new U[1k, 8k] on cached U[0, 4k], bs 64) is timed in the same run and
+reported as TFLOP/s under "prefill".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the same decode workload
+(host cores; every step is a bounded sample of the decode batch), the
+deliberately slow reference arm.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from varlen_flashattention_causal_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged-decode KV GB/s + varlen-prefill TFLOP/s, % of 1×GB300 roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def decode_bytes(b, elem=2):
+    """Algorithmic bytes of one decode attention call: every cached K and V
+    row once per KV head, q and out once, the block-table entries and
+    lengths read."""
+    kv = sum(b.kv_lens) * b.Hkv * b.D * 2 * elem
+    qo = 2 * b.T * b.Hq * b.D * 2
+    tables = sum((L + b.bs - 1) // b.bs for L in b.kv_lens) * 4 + b.B * 4
+    return kv + qo + tables
+
+
+def kv_write_bytes(T, Hkv, D, elem=2):
+    return T * Hkv * D * 2 * (2 + elem) + T * 8
+
+
+def prefill_flops(b):
+    """4 * D * Hq * (unmasked query-key pairs): QK^T and PV, 2 flops per MAC."""
+    pairs = 0
+    for q, kv in zip(b.q_lens, b.kv_lens):
+        ctx = kv - q
+        pairs += q * ctx + q * (q + 1) // 2
+    return 4 * b.D * b.Hq * pairs
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        lo, hi = getattr(self, "start", 0.0), getattr(self, "stop", float("inf"))
+        for ts, r in self.rows:
+            if not (lo - 0.1 <= ts <= hi + 0.3):
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for n, v in zip(names, r[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+            except Exception:
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args):
+    import varlen_flashattention_causal_gb300 as va
+    from varlen_flashattention_causal_gb300 import build
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    hbm, tc, tc_sus, peak_kind = peaks()
+
+    # ---------------- decode workload: history resident in the paged cache
+    b = W.decode_llama8b(device="cpu")
+    # the step's own new tokens are the last position of each request
+    last = torch.tensor([sum(b.kv_lens[:r + 1]) - 1 for r in range(b.B)])
+    g = torch.Generator(device=dev)
+    g.manual_seed(W.SEED0 + 1)
+    kc = torch.randn((b.num_blocks, b.bs, b.Hkv, b.D), generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn((b.num_blocks, b.bs, b.Hkv, b.D), generator=g, device=dev).to(torch.bfloat16)
+    q = b.q.to(dev)
+    k_new = b.k_tok[last].to(dev)
+    v_new = b.v_tok[last].to(dev)
+    slots = b.slot_mapping[last].to(dev)
+    seq_lens = b.seqused_k.to(dev)
+    bt = b.block_table.to(dev)
+    out = torch.empty_like(q)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ns = va.attn_num_splits(b.B, 1, b.max_seqlen_k, b.Hq, b.Hkv, sms)
+    wsp = torch.empty(max(1, va.attn_workspace_size(b.B, b.Hq, b.D, ns)), dtype=torch.uint8, device=dev)
+
+    def step(stream=None):
+        va.kv_cache_write(k_new, v_new, kc, vc, slots)
+        va.attn_paged_decode(q, kc, vc, out, seq_lens, bt, b.max_seqlen_k, b.softmax_scale,
+                             num_splits=ns, workspace=wsp)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(dev.index) as clk:
+        t_w = time.time()
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        while time.time() - t_w < 1.0:        # the sampler is up before timing starts
+            step()
+            torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clk.mark("start")
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(K):
+            va.kv_cache_write(k_new, v_new, kc, vc, slots)
+            ev[i][0].record()
+            va.attn_paged_decode(q, kc, vc, out, seq_lens, bt, b.max_seqlen_k, b.softmax_scale,
+                                 num_splits=ns, workspace=wsp)
+            ev[i][1].record()
+        t1.record()
+        torch.cuda.synchronize()
+        clk.mark("stop")
+    if ws > 1:
+        dist.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt)
+    attn_ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
+    dbytes = decode_bytes(b)
+    step_bytes = dbytes + kv_write_bytes(b.B, b.Hkv, b.D)
+    ms_per_step = elapsed_ms / K
+    value = step_bytes * ws / (ms_per_step * 1e-3) / 1e9
+    achieved = dbytes / (attn_ms * 1e-3) / 1e9
+
+    # ---------------- e2e: host inputs -> device -> result back, per step
+    h_q = q.cpu().pin_memory()
+    h_k, h_v = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    h_slots, h_lens, h_bt = slots.cpu().pin_memory(), seq_lens.cpu().pin_memory(), bt.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    d_slots, d_lens, d_bt = torch.empty_like(slots), torch.empty_like(seq_lens), torch.empty_like(bt)
+    bi = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_lens, h_bt))
+    bo = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_lens, h_lens), (d_bt, h_bt)):
+            d.copy_(h, non_blocking=True)
+        va.kv_cache_write(d_k, d_v, kc, vc, d_slots)
+        va.attn_paged_decode(d_q, kc, vc, out, d_lens, d_bt, b.max_seqlen_k, b.softmax_scale,
+                             num_splits=ns, workspace=wsp)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = max(10, K // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
+
+    # ---------------- chunked varlen prefill (TFLOP/s)
+    pf = prefill_stats(va, dev, args, tc)
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "paged decode, Llama-3-8B shaped: B=64, Hq=32, Hkv=8, D=128, bf16, "
+                               "ctx U[512,4096], block_size 16, 40960-block pool",
+                   "step": "kv_cache_write of 64 new tokens + attn_paged_decode (split-KV + combine)",
+                   "num_splits": ns, "bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2: %.0f MB of K/V read per step vs %d MB L2"
+                         % (sum(b.kv_lens) * b.Hkv * b.D * 4 / 1e6, L2_BYTES >> 20),
+                   "parallelism": "replicas x%d (independent batches, no collective)" % ws},
+        "roofline": {"kernel": "attn_paged_decode (fwd_mma_kernel + combine_kernel)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(attn_ms, 5)},
+        "prefill": pf,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(res))
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def prefill_stats(va, dev, args, tc_peak):
+    b = W.chunked_prefill(device="cpu", gen_kv=False)
+    g = torch.Generator(device=dev)
+    g.manual_seed(W.SEED0 + 3)
+    kc = torch.randn((b.num_blocks, b.bs, b.Hkv, b.D), generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn((b.num_blocks, b.bs, b.Hkv, b.D), generator=g, device=dev).to(torch.bfloat16)
+    q = b.q.to(dev)
+    out = torch.empty_like(q)
+    cu, su, bt = b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev)
+
+    def call():
+        va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt, b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale,
+                               causal=True, num_splits=1)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    n = max(3, min(20, args.steps // 10))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, c in evs:
+        a.record()
+        call()
+        c.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(c) for a, c in evs)
+    fl = prefill_flops(b)
+    tf = fl / (ms * 1e-3) / 1e12
+    return {"workload": "chunked varlen causal prefill: B=16, new U[1k,8k] on cached U[0,4k], Hq=32, "
+                        "Hkv=8, D=128, bf16, block_size 64",
+            "tflops": round(tf, 1), "ms": round(ms, 4), "flops": fl, "peak": tc_peak,
+            "frac": round(tf / tc_peak, 4), "bound": "tensor", "kernel": "fwd_mma_kernel (mma.sync)"}
+
+
+def _oracle_decode_setup():
+    import oracle
+    b = W.decode_llama8b(device="cpu", pool=16384)
+    kc = torch.zeros((b.num_blocks, b.bs, b.Hkv, b.D), dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    oracle.kv_write(b.k_tok, b.v_tok, kc, vc, b.slot_mapping)
+    return b, kc, vc
+
+
+def _oracle_decode(b, kc, vc, rows, cores):
+    import oracle
+    oracle.attention(b.q, kc, vc, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                     causal=True, rows=rows, nthreads=cores)
+
+
+def _sample_bytes(b, rows):
+    kv = sum(b.kv_lens[r] for r in rows) * b.Hkv * b.D * 2 * 2
+    return kv + 2 * len(rows) * b.Hq * b.D * 2 + sum((b.kv_lens[r] + b.bs - 1) // b.bs for r in rows) * 4
+
+
+def cpu_baseline(args, budget_s=10.0):
+    """The fp64 oracle on the full decode batch, on this host's cores,
+    repeated until about budget_s seconds of CPU work."""
+    b, kc, vc = _oracle_decode_setup()
+    cores = os.cpu_count() or 1
+    rows = list(range(b.B))
+    n, t0 = 0, time.perf_counter()
+    while n < 30 and (n == 0 or time.perf_counter() - t0 < budget_s):
+        _oracle_decode(b, kc, vc, rows, cores)
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(decode_bytes(b) / dt / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "full decode batch (64 requests x 32 heads, %d cached keys), fp64, %d pass(es), %.2f s/pass"
+                      % (sum(b.kv_lens), n, dt)}
+
+
+def run_reference(args, budget_s=150.0):
+    """Reference arm: the fp64 CPU oracle timed on the host cores.  Every
+    step is a bounded sample of the decode batch (the first n requests, all
+    heads), n chosen so that warm-up plus timed steps take about budget_s."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    b, kc, vc = _oracle_decode_setup()
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    _oracle_decode(b, kc, vc, list(range(b.B)), cores)          # calibration pass
+    full = time.perf_counter() - t0
+    per_step = budget_s / max(1, args.steps + args.warmup)
+    n = max(1, min(b.B, int(b.B * per_step / max(full, 1e-6))))
+    rows = list(range(n))
+    for _ in range(args.warmup):
+        _oracle_decode(b, kc, vc, rows, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_decode(b, kc, vc, rows, cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = _sample_bytes(b, rows) / dt / 1e9
+    sample = "first %d of 64 decode requests (all 32 heads) per step, fp64 oracle" % n
+    res = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": "paged decode, Llama-3-8B shaped: B=64, Hq=32, Hkv=8, D=128, bf16, "
+                                  "ctx U[512,4096], block_size 16, 40960-block pool"},
+           "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from oracle.build import build_oracle
+    if args.impl == "reference":
+        build_oracle()
+        run_reference(args)
+    else:
+        if not args.no_cpu_baseline:
+            build_oracle()
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

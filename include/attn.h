@@ -1,0 +1,214 @@
+/*
+ * attn.h -- C ABI of libattn.so: varlen causal attention over a paged KV
+ * cache on one GB300 (sm_103a).
+ *
+ * The operations follow two pages:
+ *  [vLLM-FA]  "FlashAttention deep dive" (vLLM V1 FlashAttention backend):
+ *             flash_attn_varlen_func and its argument table, the KV cache
+ *             shape (2, num_blocks, block_size, num_kv_heads, head_size),
+ *             reshape_and_cache_flash, cascade attention and
+ *             merge_attn_states, the FP8 KV cache.
+ *  [MR]       "vLLM 中 Attention Kernel 如何并行处理多个请求": packed requests
+ *             (sec. 1, 5), tile classification (sec. 3-4), online softmax
+ *             (sec. 7), decode (sec. 9), bottom-right causal alignment
+ *             (sec. 10), paged lookup (sec. 11), split-KV segments merged by a
+ *             second reduction kernel (sec. 12).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the
+ *    library never allocates, frees or retains device memory.  Scratch space
+ *    comes from the caller through (workspace, ws_bytes).
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *    does no host synchronisation, so a call can be captured in a CUDA graph
+ *    when its pointers and host scalars stay fixed.
+ *  - Arguments are validated on the host before anything is launched.  On a
+ *    non-zero status nothing was launched and no memory was touched.
+ *  - Block ids and slots are also checked inside the kernels: an id outside
+ *    [0, num_blocks) or a slot outside [0, num_blocks * block_size) is never
+ *    dereferenced (attention: the rows of that block read as zero K and V;
+ *    KV write: the token is skipped) and the device error word read by
+ *    attn_device_error_flag() is raised.
+ *  - Layouts are row-major with the last dimension contiguous:
+ *      q, out      [T, Hq, D]        token stride given in elements
+ *      lse         [T, Hq] fp32      natural-log log-sum-exp per query head
+ *      k/v cache   [num_blocks, block_size, Hkv, D] each; the two halves of
+ *                  the [vLLM-FA] cache tensor (kv_cache.unbind(0)) are passed
+ *                  as separate pointers
+ *      block_table [B, >= ceil(kv_len / block_size)] int32, row stride given
+ *                  in elements; a pointer offset into a row (cascade suffix
+ *                  view block_table[:, n:]) is allowed
+ *  - Head size D is 64 or 128, Hq % Hkv == 0 (GQA: query head h reads KV
+ *    head h / (Hq / Hkv)), block_size is a positive multiple of 16.
+ *  - Pointers must be 16-byte aligned and token strides multiples of 8
+ *    elements (16 bytes for 16-bit types).
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *attn_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = 1,        /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = 2,       /* inconsistent sizes, strides or counts */
+    ATTN_ERR_DTYPE = 3,       /* unsupported dtype or dtype combination */
+    ATTN_ERR_ALIGN = 4,       /* pointer / stride not 16-byte aligned */
+    ATTN_ERR_BLOCK_SIZE = 5,  /* block_size not a positive multiple of 16 */
+    ATTN_ERR_HEAD_SIZE = 6,   /* head size not 64 or 128 */
+    ATTN_ERR_WORKSPACE = 7,   /* workspace NULL or smaller than required */
+    ATTN_ERR_CUDA = 8,        /* a CUDA runtime call failed (no device, launch error) */
+    ATTN_ERR_DEVICE = 9       /* the current device is not an sm_103 GPU */
+} attn_status;
+
+typedef enum {
+    ATTN_BF16 = 0,
+    ATTN_FP16 = 1,
+    ATTN_FP8_E4M3 = 2,        /* float8 e4m3 "fn": bias 7, no inf, max 448 */
+    ATTN_FP32 = 3
+} attn_dtype;
+
+/*
+ * attn_varlen_prefill -- [vLLM-FA] flash_attn_varlen_func over a paged cache
+ * (argument table: q, k = key_cache, v = value_cache, out, cu_seqlens_q,
+ * max_seqlen_q, seqused_k, max_seqlen_k, softmax_scale, causal,
+ * block_table, k/v descale, num_splits, return of the softmax lse).
+ *
+ * For request r in [0, B): its query tokens are rows
+ * [cu_seqlens_q[r], cu_seqlens_q[r+1]) of q; it has kv_len = seqused_k[r]
+ * cached keys (the new tokens' keys included, written beforehand with
+ * kv_cache_write).  Query i of the request sits at absolute position
+ * ctx + i, ctx = kv_len - q_len ([MR] sec. 10), and with causal != 0 sees
+ * keys j <= ctx + i; otherwise all kv_len keys.  Key j is read from block
+ * block_table[r * bt_row_stride + j / block_size], row j % block_size
+ * ([MR] sec. 11).
+ *
+ *   out[t, h, :] = softmax_j(softmax_scale * k_descale * q[t,h,:] . K_j)
+ *                  @ (v_descale * V_j)
+ *   lse_out[t, h] = log sum_j exp(softmax_scale * k_descale * q . K_j)
+ *
+ * A query with no visible key gets out = 0 and lse = -inf.
+ *
+ * q_dtype: ATTN_BF16 or ATTN_FP16 (out has the same type).
+ * kv_dtype: q_dtype, or ATTN_FP8_E4M3 (k/v_descale multiply the stored
+ *   values; pass 1.0 for 16-bit caches).
+ * max_seqlen_q / max_seqlen_k: upper bounds of q_len / kv_len over the batch
+ *   (host scalars used to size the launch; values larger than the truth are
+ *   safe, smaller ones are an error the kernels cannot detect).
+ * total_q: number of rows of q (= cu_seqlens_q[B]).
+ * num_splits: number of KV segments per (request, KV head) for split-KV
+ *   ([MR] sec. 12): 0 = choose automatically, 1 = no split.  Partial
+ *   results go to the workspace and a second kernel merges them.
+ * lse_out may be NULL.
+ * workspace: device scratch of at least
+ *   attn_workspace_size(total_q, Hq, D, splits) bytes for the split count the
+ *   call ends up using; with num_splits = 0 the automatic choice is capped
+ *   to what fits in ws_bytes (ws_bytes = 0 and workspace = NULL disable
+ *   splitting).
+ */
+attn_status attn_varlen_prefill(
+    const void *q, int64_t q_stride_tok,
+    const void *k_cache, const void *v_cache,
+    void *out, int64_t out_stride_tok, float *lse_out,
+    const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+    const int32_t *block_table, int64_t bt_row_stride,
+    int B, int total_q, int max_seqlen_q, int max_seqlen_k,
+    int Hq, int Hkv, int D, int block_size, int num_blocks,
+    attn_dtype q_dtype, attn_dtype kv_dtype,
+    float softmax_scale, int causal, float k_descale, float v_descale,
+    int num_splits, void *workspace, size_t ws_bytes, attn_stream_t stream);
+
+/*
+ * attn_paged_decode -- one query token per request ([MR] sec. 9: the decode
+ * row is the last row of the causal matrix, so all kv_len = seq_lens[r]
+ * keys are visible).  q and out are [B, Hq, D] contiguous, lse_out [B, Hq].
+ * Same as attn_varlen_prefill with cu_seqlens_q = [0, 1, ..., B] and
+ * seqused_k = seq_lens; split-KV is on by default (num_splits 0).
+ */
+attn_status attn_paged_decode(
+    const void *q, const void *k_cache, const void *v_cache,
+    void *out, float *lse_out,
+    const int32_t *seq_lens, const int32_t *block_table, int64_t bt_row_stride,
+    int B, int max_seq_len, int Hq, int Hkv, int D, int block_size, int num_blocks,
+    attn_dtype q_dtype, attn_dtype kv_dtype,
+    float softmax_scale, float k_descale, float v_descale,
+    int num_splits, void *workspace, size_t ws_bytes, attn_stream_t stream);
+
+/*
+ * attn_merge_states -- [vLLM-FA] merge_attn_states: combine two attention
+ * results over disjoint key sets (cascade prefix and suffix):
+ *   lse = log(exp(lse1) + exp(lse2)),
+ *   out = exp(lse1 - lse) * o1 + exp(lse2 - lse) * o2.
+ * o1, o2, out: [T, Hq, D] contiguous, all of `dtype` (bf16, fp16 or fp32);
+ * lse1, lse2: [T, Hq] fp32; lse_out may be NULL.  A side with lse = -inf
+ * has weight 0; both -inf gives out = 0, lse = -inf.  out may alias o1 or o2.
+ */
+attn_status attn_merge_states(
+    void *out, float *lse_out,
+    const void *o1, const float *lse1, const void *o2, const float *lse2,
+    int T, int Hq, int D, attn_dtype dtype, attn_stream_t stream);
+
+/*
+ * kv_cache_write -- [vLLM-FA] reshape_and_cache_flash: token t of
+ * key/value [T, Hkv, D] (token strides in elements) is stored at block
+ * slot_mapping[t] / block_size, row slot_mapping[t] % block_size of both
+ * caches.  slot_mapping[t] < 0 skips the token (padding).
+ * src_dtype: ATTN_BF16 or ATTN_FP16.  kv_dtype: src_dtype (bit copy) or
+ * ATTN_FP8_E4M3: each value x is stored as e4m3(x / scale) with the
+ * division in fp32, round to nearest even, saturating at +-448
+ * (k_scale for keys, v_scale for values).
+ */
+attn_status kv_cache_write(
+    const void *key, int64_t key_stride_tok, const void *value, int64_t value_stride_tok,
+    void *k_cache, void *v_cache, const int64_t *slot_mapping,
+    int T, int Hkv, int D, int block_size, int num_blocks,
+    attn_dtype src_dtype, attn_dtype kv_dtype, float k_scale, float v_scale,
+    attn_stream_t stream);
+
+/*
+ * attn_workspace_size -- bytes of scratch attn_varlen_prefill /
+ * attn_paged_decode need for `num_splits` KV segments: fp32 partial outputs
+ * and log-sum-exps for every (token, query head, segment).  0 when
+ * num_splits <= 1.
+ */
+size_t attn_workspace_size(int total_q, int Hq, int D, int num_splits);
+
+/*
+ * attn_num_splits -- the split count attn_varlen_prefill(num_splits = 0)
+ * would choose for these host scalars on the current device (the decode
+ * rule: enough segments to fill every SM a few times over, each segment at
+ * least a few K/V tiles long).  Exposed for planning and tests.
+ */
+int attn_num_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int num_sms);
+
+/*
+ * attn_tile_kind -- [MR] sec. 4 tile classification for a query tile holding
+ * local positions [q_lo, q_hi) of a request with cached context ctx against
+ * keys [k_lo, k_hi): 0 = skip (every key in the future of every query),
+ * 1 = full (every key visible to every query), 2 = diagonal (needs the
+ * element mask).  Host mirror of the rule the kernels apply.
+ */
+int attn_tile_kind(int q_lo, int q_hi, int k_lo, int k_hi, int ctx);
+
+/* Human-readable name of a status code. */
+const char *attn_status_string(attn_status s);
+
+/*
+ * attn_device_error_flag -- read (and with reset != 0, clear) the device
+ * error word of the current device: bit 0 = a block id outside
+ * [0, num_blocks) was met, bit 1 = a slot outside the cache was met.
+ * Returns -1 if the CUDA call failed.  Synchronises the device.
+ */
+int attn_device_error_flag(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

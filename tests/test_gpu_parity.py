@@ -1,0 +1,406 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs.
+
+Tolerances: max-abs 1e-2 on out and lse for bf16/fp16 inputs (fp32
+accumulation, N(0, 1) data); 4e-2 for the e4m3 KV path, where the oracle is
+fed the same dequantised e4m3 values.  KV writes (slot_mapping scatter,
+e4m3 quantisation) must be bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_flashattention_causal_gb300 as va
+from varlen_flashattention_causal_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+TOL_FP8 = 4e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from varlen_flashattention_causal_gb300 import build
+    build.build()
+    va.attn_device_error_flag(reset=True)
+    yield
+    torch.cuda.synchronize()
+
+
+def cache_dtype(b):
+    return torch.float8_e4m3fn if b.kv_dtype == "fp8" else b.k_tok.dtype
+
+
+def gpu_cache(b):
+    kc = torch.zeros((b.num_blocks, b.bs, b.Hkv, b.D), dtype=cache_dtype(b), device="cuda")
+    vc = torch.zeros_like(kc)
+    va.kv_cache_write(b.k_tok.cuda(), b.v_tok.cuda(), kc, vc, b.slot_mapping.cuda(), b.k_scale, b.v_scale)
+    return kc, vc
+
+
+def cpu_cache(b):
+    kc = torch.zeros((b.num_blocks, b.bs, b.Hkv, b.D), dtype=cache_dtype(b))
+    vc = torch.zeros_like(kc)
+    oracle.kv_write(b.k_tok, b.v_tok, kc, vc, b.slot_mapping, b.k_scale, b.v_scale)
+    return kc, vc
+
+
+def gpu_attn(b, kc, vc, num_splits=0, causal=None, q=None, block_table=None, seqused_k=None,
+             cu=None, max_q=None, max_k=None):
+    q = (b.q if q is None else q).cuda()
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    bt = (b.block_table if block_table is None else block_table).cuda()
+    su = (b.seqused_k if seqused_k is None else seqused_k).cuda()
+    cu = (b.cu_seqlens_q if cu is None else cu).cuda()
+    va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt,
+                           b.max_seqlen_q if max_q is None else max_q,
+                           b.max_seqlen_k if max_k is None else max_k,
+                           b.softmax_scale, causal=b.causal if causal is None else causal, lse_out=lse,
+                           k_descale=b.k_scale if b.kv_dtype == "fp8" else 1.0,
+                           v_descale=b.v_scale if b.kv_dtype == "fp8" else 1.0,
+                           num_splits=num_splits)
+    return out, lse
+
+
+def ref_attn(b, kc, vc, rows=None, causal=None):
+    return oracle.attention(b.q, kc, vc, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                            causal=b.causal if causal is None else causal,
+                            k_scale=b.k_scale if b.kv_dtype == "fp8" else 1.0,
+                            v_scale=b.v_scale if b.kv_dtype == "fp8" else 1.0, rows=rows)
+
+
+def max_err(gpu, ref):
+    g = gpu.detach().double().cpu()
+    r = ref.double()
+    both_inf = torch.isinf(g) & torch.isinf(r) & (torch.sign(g) == torch.sign(r))
+    d = (g - r).abs()
+    d[both_inf] = 0.0
+    return float(d.max()) if d.numel() else 0.0
+
+
+def check(out, lse, ref_out, ref_lse, tol, rows=None):
+    if rows is not None:
+        out, lse = out[rows], lse[rows]
+    eo, el = max_err(out, ref_out), max_err(lse, ref_lse)
+    assert eo <= tol and el <= tol, "max-abs error out %.3g lse %.3g (tol %.3g)" % (eo, el, tol)
+    assert torch.isfinite(out.float()).all()
+    return eo, el
+
+
+def assert_no_device_error():
+    assert va.attn_device_error_flag(reset=True) == 0
+
+
+# ------------------------------------------------------------------ KV write
+
+@pytest.mark.parametrize("kv_dtype,src", [("bf16", torch.bfloat16), ("fp16", torch.float16), ("fp8", torch.bfloat16)])
+def test_kv_write_bit_exact(kv_dtype, src):
+    b = W.make_batch([3, 1, 9], [70, 33, 200], Hq=8, Hkv=4, D=128, bs=32, seed=1, kv_dtype=kv_dtype, q_dtype=src)
+    # padding tokens (slot -1) must be skipped
+    b.slot_mapping = b.slot_mapping.clone()
+    b.slot_mapping[::17] = -1
+    g = gpu_cache(b)
+    c = cpu_cache(b)
+    assert torch.equal(g[0].view(torch.uint8).cpu(), c[0].view(torch.uint8))
+    assert torch.equal(g[1].view(torch.uint8).cpu(), c[1].view(torch.uint8))
+    assert_no_device_error()
+
+
+def test_kv_write_strided_source_and_bad_slot():
+    b = W.make_batch([2], [40], Hq=4, Hkv=2, D=64, bs=16, seed=2)
+    # key/value as views into a wider per-token buffer (token stride > Hkv*D)
+    wide = torch.zeros((40, 3, 2, 64), dtype=torch.bfloat16)
+    wide[:, 0], wide[:, 2] = b.k_tok, b.v_tok
+    wide = wide.cuda()
+    kc = torch.zeros((b.num_blocks, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = b.slot_mapping.clone()
+    slots[5] = b.num_blocks * 16 + 3          # outside the cache: must not be written
+    va.kv_cache_write(wide[:, 0], wide[:, 2], kc, vc, slots.cuda())
+    assert va.attn_device_error_flag(reset=True) & va.ERR_SLOT
+    c = cpu_cache(b)
+    ok = torch.ones(40, dtype=torch.bool)
+    ok[5] = False
+    good = b.slot_mapping[ok]
+    kc_flat, ck_flat = kc.view(-1, 2, 64).cpu(), c[0].view(-1, 2, 64)
+    assert torch.equal(kc_flat[good], ck_flat[good])
+    s5 = int(b.slot_mapping[5])
+    assert int(torch.count_nonzero(kc_flat[s5].float())) == 0
+
+
+# --------------------------------------------------------------- workload 0
+
+def test_tiny_packed_prefill_then_decode():
+    pre, dec = W.tiny()
+    kc, vc = gpu_cache(pre)
+    ck, cv = cpu_cache(pre)
+    out, lse = gpu_attn(pre, kc, vc)
+    ro, rl = ref_attn(pre, ck, cv)
+    check(out, lse, ro, rl, TOL)
+    # one decode step: write each request's new token, attend over len + 1
+    va.kv_cache_write(dec.k_tok.cuda(), dec.v_tok.cuda(), kc, vc, dec.slot_mapping.cuda())
+    oracle.kv_write(dec.k_tok, dec.v_tok, ck, cv, dec.slot_mapping)
+    assert torch.equal(kc.cpu(), ck) and torch.equal(vc.cpu(), cv)
+    ro, rl = ref_attn(dec, ck, cv)
+    out, lse = gpu_attn(dec, kc, vc)
+    check(out, lse, ro, rl, TOL)
+    q = dec.q.cuda()
+    o2 = torch.empty_like(q)
+    l2 = torch.empty((4, 8), dtype=torch.float32, device="cuda")
+    va.attn_paged_decode(q, kc, vc, o2, dec.seqused_k.cuda(), dec.block_table.cuda(), dec.max_seqlen_k,
+                         dec.softmax_scale, lse_out=l2)
+    check(o2, l2, ro, rl, TOL)
+    assert_no_device_error()
+
+
+# --------------------------------------------------------- randomised cases
+
+CASES = [
+    # q_lens, kv_lens, Hq, Hkv, D, bs, causal
+    ([6, 4], [6, 4], 4, 4, 64, 16, True),                       # the pages' 6 + 4 example, MHA
+    ([1, 1, 1, 1, 1], [1, 17, 64, 65, 300], 8, 2, 128, 16, True),  # decode incl. kv_len 1
+    ([5, 1, 70, 3], [5, 90, 200, 3], 8, 2, 64, 48, True),        # chunked prefill, odd block size
+    ([16, 2, 33], [100, 2, 33], 16, 2, 128, 64, True),           # G = 8
+    ([129, 64, 1], [129, 500, 257], 4, 1, 128, 256, True),       # several row blocks, ragged tails
+    ([7, 9], [20, 9], 6, 3, 64, 32, False),                      # non-causal (cascade prefix stage)
+    ([2, 3], [2, 3], 1, 1, 128, 16, True),                       # one head
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("num_splits", [1, 2, 7, 0])
+def test_random_batches_against_oracle(case, num_splits):
+    q_lens, kv_lens, Hq, Hkv, D, bs, causal = CASES[case]
+    b = W.make_batch(q_lens, kv_lens, Hq, Hkv, D, bs, seed=100 + case, causal=causal)
+    kc, vc = gpu_cache(b)
+    ro, rl = ref_attn(b, *cpu_cache(b))
+    out, lse = gpu_attn(b, kc, vc, num_splits=num_splits)
+    check(out, lse, ro, rl, TOL)
+    assert_no_device_error()
+
+
+def test_fp16_path():
+    b = W.make_batch([5, 1, 40], [50, 70, 40], 8, 2, 128, 32, seed=7, q_dtype=torch.float16)
+    kc, vc = gpu_cache(b)
+    ro, rl = ref_attn(b, *cpu_cache(b))
+    for ns in (1, 3):
+        out, lse = gpu_attn(b, kc, vc, num_splits=ns)
+        assert out.dtype == torch.float16
+        check(out, lse, ro, rl, TOL)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_fp8_kv_small(D):
+    b = W.make_batch([1, 1, 12, 3], [200, 33, 64, 3], 8, 2, D, 32, seed=8, kv_dtype="fp8")
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    assert torch.equal(kc.view(torch.uint8).cpu(), ck.view(torch.uint8))
+    ro, rl = ref_attn(b, ck, cv)
+    for ns in (1, 4):
+        out, lse = gpu_attn(b, kc, vc, num_splits=ns)
+        check(out, lse, ro, rl, TOL_FP8)
+
+
+# ------------------------------------------------------------- edge cases
+
+def test_empty_and_degenerate_requests():
+    # request 1 has kv_len 0, request 2 has no query tokens, request 3 has
+    # more queries than keys (negative context: its first rows see nothing)
+    q_lens, kv_lens = [3, 1, 0, 5, 2], [10, 0, 7, 3, 2]
+    b = W.make_batch(q_lens, kv_lens, 4, 2, 64, 16, seed=9)
+    kc, vc = gpu_cache(b)
+    ro, rl = ref_attn(b, *cpu_cache(b))
+    for ns in (1, 3):
+        out, lse = gpu_attn(b, kc, vc, num_splits=ns)
+        check(out, lse, ro, rl, TOL)
+        assert torch.equal(out[3].float().cpu(), torch.zeros(4, 64))
+        assert torch.isinf(lse[3]).all() and (lse[3] < 0).all()
+        assert torch.isinf(lse[4:6]).all()          # queries 0, 1 of request 3 see nothing
+    assert_no_device_error()
+
+
+def test_paged_layout_invariance_is_bitwise():
+    """Same K/V in two different random block permutations (same block
+    size and launch plan) gives bit-identical results."""
+    b1 = W.make_batch([1, 4, 9], [300, 77, 160], 8, 2, 128, 16, seed=10)
+    b2 = W.make_batch([1, 4, 9], [300, 77, 160], 8, 2, 128, 16, seed=11)
+    b2.q, b2.k_tok, b2.v_tok = b1.q, b1.k_tok, b1.v_tok
+    assert not torch.equal(b1.block_table, b2.block_table)
+    o1, l1 = gpu_attn(b1, *gpu_cache(b1), num_splits=3)
+    o2, l2 = gpu_attn(b2, *gpu_cache(b2), num_splits=3)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # a different block size changes only the rounding, within tolerance
+    b3 = W.make_batch([1, 4, 9], [300, 77, 160], 8, 2, 128, 256, seed=12)
+    b3.q, b3.k_tok, b3.v_tok = b1.q, b1.k_tok, b1.v_tok
+    o3, l3 = gpu_attn(b3, *gpu_cache(b3), num_splits=3)
+    assert max_err(o3, o1.double().cpu()) <= TOL and max_err(l3, l1.double().cpu()) <= TOL
+
+
+def test_decode_equals_last_row_of_prefill():
+    b = W.make_batch([64], [64], 8, 2, 128, 16, seed=12)
+    kc, vc = gpu_cache(b)
+    out, lse = gpu_attn(b, kc, vc, num_splits=1)
+    d_out = torch.empty((1, 8, 128), dtype=torch.bfloat16, device="cuda")
+    d_lse = torch.empty((1, 8), dtype=torch.float32, device="cuda")
+    va.attn_paged_decode(b.q[63:64].cuda(), kc, vc, d_out, b.seqused_k.cuda(), b.block_table.cuda(), 64,
+                         b.softmax_scale, lse_out=d_lse, num_splits=1)
+    assert max_err(d_out[0], out[63].double().cpu()) <= 4e-3
+    assert max_err(d_lse[0], lse[63].double().cpu()) <= 1e-4
+
+
+def test_out_of_range_block_id_reads_zeros_and_is_flagged():
+    """A block id outside [0, num_blocks) is never dereferenced: its rows
+    read as zero K and V, and the device error word records it."""
+    b = W.make_batch([1, 1], [64, 64], 4, 1, 64, 16, seed=13)
+    kc, vc = gpu_cache(b)
+    bad = b.block_table.clone()
+    bad[1, 2] = b.num_blocks + 5         # keys 32..47 of request 1 point outside the pool
+    out, lse = gpu_attn(b, kc, vc, block_table=bad, num_splits=1)
+    assert va.attn_device_error_flag(reset=True) & va.ERR_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    ck, cv = cpu_cache(b)
+    ro, rl = ref_attn(b, ck, cv)
+    check(out[:1], lse[:1], ro[:1], rl[:1], TOL)          # request 0 untouched
+    # request 1 equals the oracle on a cache whose block 2 of that row is zero
+    blk = int(b.block_table[1, 2])
+    ck[blk] = 0
+    cv[blk] = 0
+    ro, rl = ref_attn(b, ck, cv)
+    check(out[1:], lse[1:], ro[1:], rl[1:], TOL)
+
+
+# ------------------------------------------------------------------- merge
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+def test_merge_states_against_oracle(dtype):
+    g = torch.Generator().manual_seed(14)
+    T, Hq, D = 37, 8, 128
+    o1 = torch.randn((T, Hq, D), generator=g).to(dtype)
+    o2 = torch.randn((T, Hq, D), generator=g).to(dtype)
+    l1 = torch.randn((T, Hq), generator=g) * 5
+    l2 = torch.randn((T, Hq), generator=g) * 5
+    l1[0, :3] = -math.inf
+    l2[0, 1:5] = -math.inf
+    out = torch.empty((T, Hq, D), dtype=dtype, device="cuda")
+    lo = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+    va.attn_merge_states(out, lo, o1.cuda(), l1.cuda(), o2.cuda(), l2.cuda())
+    ro, rl = oracle.merge_states(o1.view(-1, D), l1.view(-1), o2.view(-1, D), l2.view(-1))
+    tol = 1e-2 if dtype != torch.float32 else 1e-5
+    assert max_err(out.view(-1, D), ro) <= tol
+    assert max_err(lo.view(-1), rl) <= 1e-5
+    # in place: out aliases o1
+    a = o1.cuda()
+    va.attn_merge_states(a, None, a, l1.cuda(), o2.cuda(), l2.cuda())
+    assert torch.equal(a, out)
+
+
+# ------------------------------------------------------ full-size workloads
+
+def _rows_sample(b, n, seed):
+    """Seeded sample of packed rows: every request's first and last query
+    plus uniformly drawn rows."""
+    cu = b.cu_seqlens_q.tolist()
+    rows = set()
+    for r in range(b.B):
+        if cu[r + 1] > cu[r]:
+            rows.update([cu[r], cu[r + 1] - 1])
+    g = torch.Generator().manual_seed(seed)
+    rows.update(torch.randint(0, b.T, (n,), generator=g).tolist())
+    return sorted(rows)
+
+
+def test_workload1_llama8b_decode_full():
+    b = W.decode_llama8b()
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    assert torch.equal(kc.cpu(), ck) and torch.equal(vc.cpu(), cv)
+    ro, rl = ref_attn(b, ck, cv)
+    out = torch.empty((b.B, b.Hq, b.D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((b.B, b.Hq), dtype=torch.float32, device="cuda")
+    va.attn_paged_decode(b.q.cuda(), kc, vc, out, b.seqused_k.cuda(), b.block_table.cuda(), b.max_seqlen_k,
+                         b.softmax_scale, lse_out=lse)
+    check(out, lse, ro, rl, TOL)
+    assert_no_device_error()
+
+
+@pytest.fixture(scope="module")
+def longctx_ref():
+    b = W.decode_longctx(bs=16)
+    ck, cv = cpu_cache(b)
+    ro, rl = ref_attn(b, ck, cv)
+    return b, ro, rl
+
+
+@pytest.mark.parametrize("bs", [16, 64, 256])
+def test_workload2_longctx_decode_full(longctx_ref, bs):
+    # the oracle is layout-invariant (pinned), so the bs = 16 reference
+    # serves every block size
+    b16, ro, rl = longctx_ref
+    b = W.decode_longctx(bs=bs, gen_kv=False)
+    b.q = b16.q
+    positions = [range(L) for L in b.kv_lens]
+    b.slot_mapping = torch.cat([W.slots(b.block_table, r, p, bs) for r, p in enumerate(positions)])
+    b.k_tok, b.v_tok = b16.k_tok, b16.v_tok
+    kc, vc = gpu_cache(b)
+    out = torch.empty((b.B, b.Hq, b.D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((b.B, b.Hq), dtype=torch.float32, device="cuda")
+    va.attn_paged_decode(b.q.cuda(), kc, vc, out, b.seqused_k.cuda(), b.block_table.cuda(), b.max_seqlen_k,
+                         b.softmax_scale, lse_out=lse)
+    check(out, lse, ro, rl, TOL)
+    assert_no_device_error()
+
+
+def test_workload3_chunked_prefill_full_sampled():
+    b = W.chunked_prefill()
+    kc, vc = gpu_cache(b)
+    out, lse = gpu_attn(b, kc, vc)
+    rows = _rows_sample(b, 48, seed=3)
+    ro, rl = ref_attn(b, *cpu_cache(b), rows=rows)
+    check(out, lse, ro, rl, TOL, rows=rows)
+    assert_no_device_error()
+
+
+def test_workload3_cascade_decode_full():
+    b = W.cascade_decode()
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    ro, rl = ref_attn(b, ck, cv)            # plain attention over prefix + suffix
+    P = b.extra["prefix"]
+    nblk = P // b.bs
+    T, Hq, D = b.q.shape
+    q = b.q.cuda()
+    # stage 1: every query against the shared prefix, non-causal, first row of the block table
+    pre_o = torch.empty_like(q)
+    pre_l = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+    va.attn_varlen_prefill(q, kc, vc, pre_o, torch.tensor([0, T], dtype=torch.int32, device="cuda"),
+                           torch.tensor([P], dtype=torch.int32, device="cuda"), b.block_table[:1].cuda(),
+                           T, P, b.softmax_scale, causal=False, lse_out=pre_l)
+    # stage 2: each request's own suffix, causal, column-offset block table view
+    suf_o = torch.empty_like(q)
+    suf_l = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+    bt = b.block_table.cuda()
+    va.attn_varlen_prefill(q, kc, vc, suf_o, b.cu_seqlens_q.cuda(), (b.seqused_k - P).cuda(), bt[:, nblk:],
+                           1, b.max_seqlen_k - P, b.softmax_scale, causal=True, lse_out=suf_l)
+    out = torch.empty_like(q)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+    va.attn_merge_states(out, lse, pre_o, pre_l, suf_o, suf_l)
+    check(out, lse, ro, rl, TOL)
+    assert_no_device_error()
+
+
+def test_workload4_fp8_mixed_full_sampled():
+    b = W.fp8_mixed()
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    assert torch.equal(kc.view(torch.uint8).cpu(), ck.view(torch.uint8))
+    assert torch.equal(vc.view(torch.uint8).cpu(), cv.view(torch.uint8))
+    out, lse = gpu_attn(b, kc, vc)
+    rows = sorted(set(range(128)) | set(_rows_sample(b, 40, seed=4)))
+    ro, rl = ref_attn(b, ck, cv, rows=rows)
+    check(out, lse, ro, rl, TOL_FP8, rows=rows)
+    assert_no_device_error()

@@ -1,0 +1,169 @@
+"""Host-side checks of libattn.so that need no GPU: the library builds and
+loads, exports every entry point include/attn.h declares, rejects bad
+arguments with the documented status before launching anything, and its
+host mirrors of the planning rules follow the pages' examples."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import varlen_flashattention_causal_gb300 as va
+from varlen_flashattention_causal_gb300 import build as vb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_BS, ERR_HD, ERR_WS, ERR_CUDA, ERR_DEV = range(10)
+BF16, FP16, E4M3, FP32 = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    vb.build()
+    return va._load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_ ]*?\*?\s*\b([a-z_][a-z0-9_]*)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"attn_varlen_prefill", "attn_paged_decode", "attn_merge_states", "kv_cache_write",
+            "attn_workspace_size", "attn_status_string"} <= set(names)
+    raw = ctypes.CDLL(vb.LIB)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(lib):
+    for s in range(10):
+        assert va.attn_status_string(s)
+    assert va.attn_status_string(ERR_HD).startswith("head size")
+
+
+FAKE = ctypes.c_void_p(4096)    # 16-byte aligned, never dereferenced on the validation path
+
+
+def prefill(lib, **kw):
+    a = dict(q=FAKE, qs=8 * 128, k=FAKE, v=FAKE, out=FAKE, os=8 * 128, lse=None, cu=FAKE, su=FAKE,
+             bt=FAKE, bts=4, B=2, T=10, mq=6, mk=6, Hq=8, Hkv=2, D=128, bs=16, nb=4, qd=BF16,
+             kd=BF16, scale=0.125, causal=1, kds=1.0, vds=1.0, ns=1, ws=None, wsb=0)
+    a.update(kw)
+    return lib.attn_varlen_prefill(a["q"], a["qs"], a["k"], a["v"], a["out"], a["os"], a["lse"], a["cu"],
+                                   a["su"], a["bt"], a["bts"], a["B"], a["T"], a["mq"], a["mk"], a["Hq"],
+                                   a["Hkv"], a["D"], a["bs"], a["nb"], a["qd"], a["kd"], a["scale"],
+                                   a["causal"], a["kds"], a["vds"], a["ns"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), ERR_NULL),
+    (dict(k=None), ERR_NULL),
+    (dict(bt=None), ERR_NULL),
+    (dict(cu=None), ERR_NULL),
+    (dict(D=96), ERR_HD),
+    (dict(D=256), ERR_HD),
+    (dict(bs=24), ERR_BS),
+    (dict(bs=0), ERR_BS),
+    (dict(Hq=6, Hkv=4), ERR_SHAPE),
+    (dict(qs=8 * 128 - 8), ERR_SHAPE),
+    (dict(B=-1), ERR_SHAPE),
+    (dict(qd=E4M3, kd=E4M3), ERR_DTYPE),
+    (dict(qd=BF16, kd=FP16), ERR_DTYPE),
+    (dict(qd=FP32, kd=FP32), ERR_DTYPE),
+    (dict(q=ctypes.c_void_p(4104)), ERR_ALIGN),
+    (dict(qs=8 * 128 + 4), ERR_ALIGN),
+    (dict(ns=4, ws=None, wsb=0), None),     # no device here: reaches CUDA or fails on workspace
+])
+def test_prefill_validation(lib, kw, status):
+    st = prefill(lib, **kw)
+    if status is None:
+        assert st in (ERR_WS, ERR_CUDA, ERR_DEV)
+    else:
+        assert st == status
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert prefill(lib, B=0, T=0) == OK
+
+
+def test_decode_validation(lib):
+    st = lib.attn_paged_decode(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 4, 2, 100, 8, 2, 80, 16, 4,
+                               BF16, BF16, 0.1, 1.0, 1.0, 0, None, 0, None)
+    assert st == ERR_HD
+    st = lib.attn_paged_decode(FAKE, FAKE, None, FAKE, None, FAKE, FAKE, 4, 2, 100, 8, 2, 64, 16, 4,
+                               BF16, BF16, 0.1, 1.0, 1.0, 0, None, 0, None)
+    assert st == ERR_NULL
+
+
+def test_kv_write_validation(lib):
+    # key, ks, value, vs, k_cache, v_cache, slots, T, Hkv, D, bs, nb, src, kv, k_scale, v_scale, stream
+    args = [FAKE, 256, FAKE, 256, FAKE, FAKE, FAKE, 3, 2, 128, 16, 4, BF16, BF16, 1.0, 1.0, None]
+
+    def call(**edit):
+        a = list(args)
+        for i, v in edit.items():
+            a[int(i[1:])] = v
+        return lib.kv_cache_write(*a)
+
+    assert call(a10=33) == ERR_BS
+    assert call(a9=100) == ERR_HD
+    assert call(a13=FP16) == ERR_DTYPE
+    assert call(a12=E4M3, a13=E4M3) == ERR_DTYPE
+    assert call(a13=E4M3, a14=0.0) == ERR_SHAPE
+    assert call(a6=None) == ERR_NULL
+    assert call(a1=100) == ERR_SHAPE
+    assert call(a1=264, a4=ctypes.c_void_p(4100)) == ERR_ALIGN
+    assert call(a7=0) == OK
+
+
+def test_merge_validation(lib):
+    assert lib.attn_merge_states(FAKE, None, FAKE, FAKE, FAKE, FAKE, 4, 8, 128, E4M3, None) == ERR_DTYPE
+    assert lib.attn_merge_states(FAKE, None, None, FAKE, FAKE, FAKE, 4, 8, 128, BF16, None) == ERR_NULL
+    assert lib.attn_merge_states(FAKE, None, FAKE, FAKE, FAKE, FAKE, 4, 8, 72, BF16, None) == ERR_HD
+    assert lib.attn_merge_states(FAKE, None, FAKE, FAKE, FAKE, FAKE, 0, 8, 128, BF16, None) == OK
+
+
+def test_tile_kind_follows_the_pages_walkthrough(lib):
+    """"vLLM 中 Attention Kernel 如何并行处理多个请求", sec. 3-4: BLOCK_M =
+    BLOCK_N = 4 over request A (6 tokens): (q0-3, k0-3) diagonal, (q0-3,
+    k4-5) skipped, (q4-5, k0-3) full, (q4-5, k4-5) diagonal."""
+    kinds = {"skip": 0, "full": 1, "diagonal": 2}
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "tile_walk_4x4.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 4
+    for q_lo, q_hi, k_lo, k_hi, kind in rows:
+        assert va.attn_tile_kind(int(q_lo), int(q_hi), int(k_lo), int(k_hi), 0) == kinds[kind]
+
+
+def test_tile_kind_with_context_and_brute_force(lib):
+    # with cached context the diagonal moves right by ctx (sec. 10); check
+    # every small tile against the element mask by enumeration
+    for ctx in (0, 3, 20):
+        for q_lo in range(0, 8, 2):
+            for q_hi in range(q_lo + 1, 10, 3):
+                for k_lo in range(0, 30, 5):
+                    for k_hi in range(k_lo + 1, 32, 7):
+                        vis = [[k <= ctx + i for k in range(k_lo, k_hi)] for i in range(q_lo, q_hi)]
+                        flat = [v for row in vis for v in row]
+                        want = 1 if all(flat) else (0 if not any(flat) else 2)
+                        assert va.attn_tile_kind(q_lo, q_hi, k_lo, k_hi, ctx) == want
+
+
+def test_workspace_and_split_rules(lib):
+    assert va.attn_workspace_size(64, 32, 128, 1) == 0
+    n = va.attn_workspace_size(64, 32, 128, 5)
+    assert n >= 64 * 32 * 5 * (128 + 1) * 4 and n % 256 == 0
+    # decode with few (request, KV head) pairs and long contexts splits;
+    # big prefill batches do not
+    assert va.attn_num_splits(4, 1, 131072, 64, 8, 152) > 8
+    assert va.attn_num_splits(16, 8192, 12288, 32, 8, 152) == 1
+    assert va.attn_num_splits(1, 1, 100, 32, 8, 152) == 1     # too short to split
+    for B, L in ((64, 4096), (4, 32768), (128, 16384), (1, 2048)):
+        s = va.attn_num_splits(B, 1, L, 32, 8, 152)
+        assert 1 <= s <= 256 and (L // 64) >= s or s == 1

@@ -1,0 +1,225 @@
+"""Varlen causal FlashAttention over a paged KV cache on GB300 (sm_103a).
+
+Thin ctypes binding over ``libattn.so``: each function has the name of the
+C entry point it wraps (declared in ``include/attn.h``) and only marshals
+arguments -- every step of the computation runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors; the call is enqueued on the
+current torch stream unless ``stream`` is given.  There is no CPU fallback:
+if the library is missing or the device is not sm_103, calls raise.
+
+Build the library with ``varlen_flashattention_causal_gb300.build.build()``
+(``__graft_entry__.build()`` does it too).
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "AttnError", "attn_varlen_prefill", "attn_paged_decode", "attn_merge_states",
+    "kv_cache_write", "attn_workspace_size", "attn_num_splits", "attn_tile_kind",
+    "attn_status_string", "attn_device_error_flag", "library_path",
+]
+
+ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3, ATTN_FP32 = 0, 1, 2, 3
+ERR_BLOCK_ID, ERR_SLOT = 1, 2
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (fn, attn_status_string(status), status))
+
+
+def library_path():
+    return _build.LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError("libattn.so is not built (run varlen_flashattention_causal_gb300.build.build())")
+    lib = ctypes.CDLL(_build.LIB)
+    c = ctypes
+    vp, i64, i32, f32, sz = c.c_void_p, c.c_int64, c.c_int, c.c_float, c.c_size_t
+    lib.attn_varlen_prefill.restype = i32
+    lib.attn_varlen_prefill.argtypes = [
+        vp, i64, vp, vp, vp, i64, vp, vp, vp, vp, i64,
+        i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+        f32, i32, f32, f32, i32, vp, sz, vp]
+    lib.attn_paged_decode.restype = i32
+    lib.attn_paged_decode.argtypes = [
+        vp, vp, vp, vp, vp, vp, vp, i64,
+        i32, i32, i32, i32, i32, i32, i32, i32, i32,
+        f32, f32, f32, i32, vp, sz, vp]
+    lib.attn_merge_states.restype = i32
+    lib.attn_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    lib.kv_cache_write.restype = i32
+    lib.kv_cache_write.argtypes = [vp, i64, vp, i64, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, f32, vp]
+    lib.attn_workspace_size.restype = sz
+    lib.attn_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.attn_num_splits.restype = i32
+    lib.attn_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.attn_tile_kind.restype = i32
+    lib.attn_tile_kind.argtypes = [i32, i32, i32, i32, i32]
+    lib.attn_status_string.restype = c.c_char_p
+    lib.attn_status_string.argtypes = [i32]
+    lib.attn_device_error_flag.restype = i32
+    lib.attn_device_error_flag.argtypes = [i32]
+    _lib = lib
+    return lib
+
+
+def _dt(t):
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float16:
+        return ATTN_FP16
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return ATTN_FP8_E4M3
+    if t.dtype == torch.float32:
+        return ATTN_FP32
+    raise TypeError("unsupported dtype %s" % t.dtype)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn, st):
+    if st != 0:
+        raise AttnError(fn, st)
+
+
+def _i32(t, name):
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous int32 tensor" % name)
+    return t
+
+
+def _workspace(T, Hq, D, ns, device, workspace):
+    if workspace is not None:
+        return workspace, workspace.numel() * workspace.element_size()
+    if ns == 1:
+        return None, 0
+    n = attn_workspace_size(T, Hq, D, ns)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device), n
+
+
+def _sms(device):
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
+def attn_varlen_prefill(q, k_cache, v_cache, out, cu_seqlens_q, seqused_k, block_table,
+                        max_seqlen_q, max_seqlen_k, softmax_scale, causal=True, lse_out=None,
+                        k_descale=1.0, v_descale=1.0, num_splits=0, workspace=None, stream=None):
+    """flash_attn_varlen_func over a paged cache (see include/attn.h).
+
+    q, out: [T, Hq, D] (token stride may exceed Hq * D); k_cache, v_cache:
+    [num_blocks, block_size, Hkv, D]; cu_seqlens_q [B+1], seqused_k [B],
+    block_table [B, >=max_blocks] int32 (row stride taken from the tensor);
+    lse_out: optional [T, Hq] fp32.  num_splits 0 = automatic; the
+    workspace is allocated here when not given.
+    """
+    lib = _load()
+    T, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    B = seqused_k.numel()
+    _i32(cu_seqlens_q, "cu_seqlens_q")
+    _i32(seqused_k, "seqused_k")
+    if block_table.dtype != torch.int32 or block_table.stride(-1) != 1:
+        raise TypeError("block_table must be int32 with unit column stride")
+    ns = num_splits
+    if ns == 0 and workspace is None:
+        ns = attn_num_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, _sms(q.device))
+    ws, ws_bytes = _workspace(T, Hq, D, ns, q.device, workspace)
+    st = lib.attn_varlen_prefill(
+        _p(q), q.stride(0), _p(k_cache), _p(v_cache), _p(out), out.stride(0), _p(lse_out),
+        _p(cu_seqlens_q), _p(seqused_k), _p(block_table), block_table.stride(0),
+        B, T, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, bs, nb,
+        _dt(q), _dt(k_cache), float(softmax_scale), int(bool(causal)),
+        float(k_descale), float(v_descale), int(ns), _p(ws), ws_bytes, _stream(stream))
+    _check("attn_varlen_prefill", st)
+    return out
+
+
+def attn_paged_decode(q, k_cache, v_cache, out, seq_lens, block_table, max_seq_len,
+                      softmax_scale, lse_out=None, k_descale=1.0, v_descale=1.0,
+                      num_splits=0, workspace=None, stream=None):
+    """One query token per request: q, out [B, Hq, D] contiguous."""
+    lib = _load()
+    B, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    _i32(seq_lens, "seq_lens")
+    if block_table.dtype != torch.int32 or block_table.stride(-1) != 1:
+        raise TypeError("block_table must be int32 with unit column stride")
+    ns = num_splits
+    if ns == 0 and workspace is None:
+        ns = attn_num_splits(B, 1, max_seq_len, Hq, Hkv, _sms(q.device))
+    ws, ws_bytes = _workspace(B, Hq, D, ns, q.device, workspace)
+    st = lib.attn_paged_decode(
+        _p(q), _p(k_cache), _p(v_cache), _p(out), _p(lse_out), _p(seq_lens), _p(block_table),
+        block_table.stride(0), B, int(max_seq_len), Hq, Hkv, D, bs, nb, _dt(q), _dt(k_cache),
+        float(softmax_scale), float(k_descale), float(v_descale), int(ns), _p(ws), ws_bytes,
+        _stream(stream))
+    _check("attn_paged_decode", st)
+    return out
+
+
+def attn_merge_states(out, lse_out, o1, lse1, o2, lse2, stream=None):
+    """merge_attn_states: o* [T, Hq, D] (bf16/fp16/fp32), lse* [T, Hq] fp32."""
+    lib = _load()
+    T, Hq, D = o1.shape
+    st = lib.attn_merge_states(_p(out), _p(lse_out), _p(o1), _p(lse1), _p(o2), _p(lse2),
+                               T, Hq, D, _dt(o1), _stream(stream))
+    _check("attn_merge_states", st)
+    return out
+
+
+def kv_cache_write(key, value, k_cache, v_cache, slot_mapping, k_scale=1.0, v_scale=1.0, stream=None):
+    """reshape_and_cache_flash: key/value [T, Hkv, D] -> caches via slot_mapping (int64)."""
+    lib = _load()
+    T, Hkv, D = key.shape
+    nb, bs, _, _ = k_cache.shape
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous():
+        raise TypeError("slot_mapping must be a contiguous int64 tensor")
+    st = lib.kv_cache_write(_p(key), key.stride(0), _p(value), value.stride(0), _p(k_cache), _p(v_cache),
+                            _p(slot_mapping), T, Hkv, D, bs, nb, _dt(key), _dt(k_cache),
+                            float(k_scale), float(v_scale), _stream(stream))
+    _check("kv_cache_write", st)
+
+
+def attn_workspace_size(total_q, Hq, D, num_splits):
+    return int(_load().attn_workspace_size(int(total_q), int(Hq), int(D), int(num_splits)))
+
+
+def attn_num_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, num_sms):
+    return int(_load().attn_num_splits(int(B), int(max_seqlen_q), int(max_seqlen_k), int(Hq), int(Hkv),
+                                       int(num_sms)))
+
+
+def attn_tile_kind(q_lo, q_hi, k_lo, k_hi, ctx):
+    return int(_load().attn_tile_kind(q_lo, q_hi, k_lo, k_hi, ctx))
+
+
+def attn_status_string(status):
+    return _load().attn_status_string(int(status)).decode()
+
+
+def attn_device_error_flag(reset=False):
+    v = int(_load().attn_device_error_flag(int(bool(reset))))
+    if v < 0:
+        raise RuntimeError("attn_device_error_flag: CUDA call failed")
+    return v

@@ -1,0 +1,371 @@
+// attn_api.cu -- the C ABI of libattn (declared in include/attn.h): host-side
+// argument validation, split planning and kernel launches.  No entry point
+// allocates device memory or synchronises the host.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <algorithm>
+
+#include "../../include/attn.h"
+#include "internal.h"
+
+using namespace attn;
+
+// device error word (bit flags from internal.h); kernels get its address
+__device__ unsigned g_attn_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 256;
+constexpr int kTileN = 64;          // keys per K/V tile of the mma kernel
+
+struct DevInfo {
+    int ready = 0;
+    int sms = 0;
+    int major = 0, minor = 0;
+    unsigned *err = nullptr;
+};
+DevInfo g_dev[kMaxDevices];
+
+attn_status device_info(DevInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    DevInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_attn_error_word) != cudaSuccess) return ATTN_ERR_CUDA;
+        d.err = static_cast<unsigned *>(p);
+        d.ready = 1;
+    }
+    if (d.major != 10 || d.minor != 3) return ATTN_ERR_DEVICE;
+    *out = &d;
+    return ATTN_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool is16(attn_dtype t) { return t == ATTN_BF16 || t == ATTN_FP16; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t part_o_bytes(int T, int Hq, int D, int ns) { return align256((size_t)T * Hq * ns * D * sizeof(float)); }
+
+// the automatic split rule: without splitting, B * Hkv * row_blocks CTAs
+// run; when that is too few to fill the GPU several times over, cut each
+// request's keys into segments of at least two K/V tiles
+int auto_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int sms) {
+    if (B <= 0 || Hkv <= 0 || Hq <= 0 || max_seqlen_k <= 0) return 1;
+    const int G = Hq / Hkv;
+    const int rows = std::max(1, max_seqlen_q) * G;
+    const int rpc = mma_rows_per_cta(rows);
+    const long long row_blocks = (rows + rpc - 1) / rpc;
+    const long long base = (long long)B * Hkv * row_blocks;
+    const long long target = 4LL * sms;            // two resident CTAs per SM, two waves
+    if (base >= target) return 1;
+    const int tiles = (max_seqlen_k + kTileN - 1) / kTileN;
+    long long s = (2 * target + base - 1) / base;
+    s = std::min<long long>(s, tiles / 2);
+    s = std::min<long long>(s, kMaxSplits);
+    return (int)std::max<long long>(s, 1);
+}
+
+attn_status check_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+struct FwdArgs {
+    const void *q;
+    int64_t q_stride;
+    const void *k_cache, *v_cache;
+    void *out;
+    int64_t out_stride;
+    float *lse;
+    const int32_t *cu_seqlens_q, *seqused_k, *block_table;
+    int64_t bt_stride;
+    int B, T, max_q, max_k, Hq, Hkv, D, bs, num_blocks;
+    attn_dtype q_dtype, kv_dtype;
+    float scale;
+    int causal;
+    float k_descale, v_descale;
+    int num_splits;
+    void *ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+attn_status validate_fwd(const FwdArgs &a) {
+    if (!a.q || !a.k_cache || !a.v_cache || !a.out || !a.seqused_k || !a.block_table) return ATTN_ERR_NULL;
+    if (a.B > 0 && a.cu_seqlens_q == nullptr && a.max_q != 1) return ATTN_ERR_NULL;
+    if (a.D != 64 && a.D != 128) return ATTN_ERR_HEAD_SIZE;
+    if (a.bs <= 0 || a.bs % 16 != 0) return ATTN_ERR_BLOCK_SIZE;
+    if (!is16(a.q_dtype)) return ATTN_ERR_DTYPE;
+    if (!(a.kv_dtype == a.q_dtype || a.kv_dtype == ATTN_FP8_E4M3)) return ATTN_ERR_DTYPE;
+    if (a.B < 0 || a.B > 65535 || a.T < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0 || a.Hkv > 65535 ||
+        a.num_blocks < 0 || a.max_q < 0 || a.max_k < 0 || a.bt_stride < 0 || a.num_splits < 0)
+        return ATTN_ERR_SHAPE;
+    if (a.q_stride < (int64_t)a.Hq * a.D || a.out_stride < (int64_t)a.Hq * a.D) return ATTN_ERR_SHAPE;
+    if ((long long)a.max_q * (a.Hq / a.Hkv) > (1LL << 30)) return ATTN_ERR_SHAPE;
+    if (!aligned16(a.q) || !aligned16(a.k_cache) || !aligned16(a.v_cache) || !aligned16(a.out) ||
+        (a.q_stride % 8) != 0 || (a.out_stride % 8) != 0)
+        return ATTN_ERR_ALIGN;
+    if (!(a.scale == a.scale) || !(a.k_descale == a.k_descale) || !(a.v_descale == a.v_descale))
+        return ATTN_ERR_SHAPE;
+    return ATTN_OK;
+}
+
+attn_status run_fwd(const FwdArgs &a) {
+    attn_status st = validate_fwd(a);
+    if (st != ATTN_OK) return st;
+    if (a.B == 0 || a.T == 0) return ATTN_OK;
+    DevInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+
+    const int G = a.Hq / a.Hkv;
+    int ns = a.num_splits;
+    const size_t per_split = (size_t)a.T * a.Hq * (a.D + 1) * sizeof(float) + 512;
+    if (ns == 0) {
+        ns = auto_splits(a.B, a.max_q, a.max_k, a.Hq, a.Hkv, dev->sms);
+        if (ns > 1) {
+            const size_t fit = a.ws ? a.ws_bytes / per_split : 0;
+            ns = (int)std::min<size_t>((size_t)ns, fit);
+            if (ns < 2) ns = 1;
+        }
+    }
+    ns = std::min(ns, kMaxSplits);
+    if (ns > 1) {
+        if (!a.ws) return ATTN_ERR_WORKSPACE;
+        if (a.ws_bytes < attn_workspace_size(a.T, a.Hq, a.D, ns)) return ATTN_ERR_WORKSPACE;
+        if (!aligned16(a.ws)) return ATTN_ERR_ALIGN;
+    }
+
+    FwdParams p{};
+    p.q = a.q;
+    p.q_stride = a.q_stride;
+    p.k_cache = a.k_cache;
+    p.v_cache = a.v_cache;
+    p.out = a.out;
+    p.out_stride = a.out_stride;
+    p.lse = a.lse;
+    p.cu_seqlens_q = a.cu_seqlens_q;
+    p.seqused_k = a.seqused_k;
+    p.block_table = a.block_table;
+    p.bt_stride = a.bt_stride;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = G;
+    p.bs = a.bs;
+    p.num_blocks = a.num_blocks;
+    p.causal = a.causal ? 1 : 0;
+    p.scale_log2 = a.scale * a.k_descale * 1.4426950408889634f;
+    p.v_descale = a.v_descale;
+    p.err = dev->err;
+    p.nsplit = ns;
+    if (ns > 1) {
+        // every segment spans a whole number of K/V tiles
+        const int per = (a.max_k + ns - 1) / ns;
+        p.split_chunk = ((per + kTileN - 1) / kTileN) * kTileN;
+        p.part_o = static_cast<float *>(a.ws);
+        p.part_lse = reinterpret_cast<float *>(static_cast<char *>(a.ws) + part_o_bytes(a.T, a.Hq, a.D, ns));
+    } else {
+        p.split_chunk = 1 << 30;
+    }
+
+    const int max_rows = std::max(1, a.max_q) * G;
+    const int rpc = mma_rows_per_cta(max_rows);
+    p.rows_lo = 0;
+    p.rows_hi = INT32_MAX;
+    p.n_row_blocks = (max_rows + rpc - 1) / rpc;
+    if ((long long)p.n_row_blocks * ns > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+    st = check_cuda(launch_fwd_mma(p, a.D, a.q_dtype, a.kv_dtype, rpc, a.stream));
+    if (st != ATTN_OK) return st;
+
+    if (ns > 1) {
+        CombineParams c{};
+        c.part_o = p.part_o;
+        c.part_lse = p.part_lse;
+        c.out = a.out;
+        c.out_stride = a.out_stride;
+        c.lse = a.lse;
+        c.T = a.T;
+        c.Hq = a.Hq;
+        c.D = a.D;
+        c.nsplit = ns;
+        st = check_cuda(launch_combine(c, a.q_dtype, a.stream));
+    }
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_workspace_size(int total_q, int Hq, int D, int num_splits) {
+    if (num_splits <= 1 || total_q <= 0 || Hq <= 0 || D <= 0) return 0;
+    return part_o_bytes(total_q, Hq, D, num_splits) + align256((size_t)total_q * Hq * num_splits * sizeof(float));
+}
+
+int attn_num_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int num_sms) {
+    if (Hkv <= 0 || Hq % Hkv != 0) return 1;
+    return auto_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, num_sms);
+}
+
+int attn_tile_kind(int q_lo, int q_hi, int k_lo, int k_hi, int ctx) { return tile_kind(q_lo, q_hi, k_lo, k_hi, ctx); }
+
+const char *attn_status_string(attn_status s) {
+    switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "inconsistent sizes or strides";
+    case ATTN_ERR_DTYPE: return "unsupported dtype combination";
+    case ATTN_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case ATTN_ERR_BLOCK_SIZE: return "block_size must be a positive multiple of 16";
+    case ATTN_ERR_HEAD_SIZE: return "head size must be 64 or 128";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA runtime error";
+    case ATTN_ERR_DEVICE: return "current device is not sm_103";
+    }
+    return "unknown status";
+}
+
+int attn_device_error_flag(int reset) {
+    unsigned v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(&v, g_attn_error_word, sizeof v) != cudaSuccess) return -1;
+    if (reset) {
+        const unsigned z = 0;
+        if (cudaMemcpyToSymbol(g_attn_error_word, &z, sizeof z) != cudaSuccess) return -1;
+    }
+    return (int)v;
+}
+
+attn_status attn_varlen_prefill(const void *q, int64_t q_stride_tok, const void *k_cache, const void *v_cache,
+                                void *out, int64_t out_stride_tok, float *lse_out, const int32_t *cu_seqlens_q,
+                                const int32_t *seqused_k, const int32_t *block_table, int64_t bt_row_stride, int B,
+                                int total_q, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                                int block_size, int num_blocks, attn_dtype q_dtype, attn_dtype kv_dtype,
+                                float softmax_scale, int causal, float k_descale, float v_descale, int num_splits,
+                                void *workspace, size_t ws_bytes, attn_stream_t stream) {
+    FwdArgs a{};
+    a.q = q;
+    a.q_stride = q_stride_tok;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.out = out;
+    a.out_stride = out_stride_tok;
+    a.lse = lse_out;
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.seqused_k = seqused_k;
+    a.block_table = block_table;
+    a.bt_stride = bt_row_stride;
+    a.B = B;
+    a.T = total_q;
+    a.max_q = max_seqlen_q;
+    a.max_k = max_seqlen_k;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.bs = block_size;
+    a.num_blocks = num_blocks;
+    a.q_dtype = q_dtype;
+    a.kv_dtype = kv_dtype;
+    a.scale = softmax_scale;
+    a.causal = causal;
+    a.k_descale = k_descale;
+    a.v_descale = v_descale;
+    a.num_splits = num_splits;
+    a.ws = workspace;
+    a.ws_bytes = ws_bytes;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    if (B > 0 && !cu_seqlens_q) return ATTN_ERR_NULL;
+    return run_fwd(a);
+}
+
+attn_status attn_paged_decode(const void *q, const void *k_cache, const void *v_cache, void *out, float *lse_out,
+                              const int32_t *seq_lens, const int32_t *block_table, int64_t bt_row_stride, int B,
+                              int max_seq_len, int Hq, int Hkv, int D, int block_size, int num_blocks,
+                              attn_dtype q_dtype, attn_dtype kv_dtype, float softmax_scale, float k_descale,
+                              float v_descale, int num_splits, void *workspace, size_t ws_bytes,
+                              attn_stream_t stream) {
+    FwdArgs a{};
+    a.q = q;
+    a.q_stride = (int64_t)Hq * D;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.out = out;
+    a.out_stride = (int64_t)Hq * D;
+    a.lse = lse_out;
+    a.cu_seqlens_q = nullptr;   // request r owns query row r
+    a.seqused_k = seq_lens;
+    a.block_table = block_table;
+    a.bt_stride = bt_row_stride;
+    a.B = B;
+    a.T = B;
+    a.max_q = 1;
+    a.max_k = max_seq_len;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.bs = block_size;
+    a.num_blocks = num_blocks;
+    a.q_dtype = q_dtype;
+    a.kv_dtype = kv_dtype;
+    a.scale = softmax_scale;
+    a.causal = 1;
+    a.k_descale = k_descale;
+    a.v_descale = v_descale;
+    a.num_splits = num_splits;
+    a.ws = workspace;
+    a.ws_bytes = ws_bytes;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run_fwd(a);
+}
+
+attn_status attn_merge_states(void *out, float *lse_out, const void *o1, const float *lse1, const void *o2,
+                              const float *lse2, int T, int Hq, int D, attn_dtype dtype, attn_stream_t stream) {
+    if (!out || !o1 || !lse1 || !o2 || !lse2) return ATTN_ERR_NULL;
+    if (T < 0 || Hq <= 0) return ATTN_ERR_SHAPE;
+    if (D != 64 && D != 128) return ATTN_ERR_HEAD_SIZE;
+    if (!(dtype == ATTN_BF16 || dtype == ATTN_FP16 || dtype == ATTN_FP32)) return ATTN_ERR_DTYPE;
+    if (!aligned16(out) || !aligned16(o1) || !aligned16(o2)) return ATTN_ERR_ALIGN;
+    if (T == 0) return ATTN_OK;
+    DevInfo *dev = nullptr;
+    attn_status st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    return check_cuda(launch_merge(out, lse_out, o1, lse1, o2, lse2, T, Hq, D, dtype,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+attn_status kv_cache_write(const void *key, int64_t key_stride_tok, const void *value, int64_t value_stride_tok,
+                           void *k_cache, void *v_cache, const int64_t *slot_mapping, int T, int Hkv, int D,
+                           int block_size, int num_blocks, attn_dtype src_dtype, attn_dtype kv_dtype, float k_scale,
+                           float v_scale, attn_stream_t stream) {
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return ATTN_ERR_NULL;
+    if (D != 64 && D != 128) return ATTN_ERR_HEAD_SIZE;
+    if (block_size <= 0 || block_size % 16 != 0) return ATTN_ERR_BLOCK_SIZE;
+    if (!is16(src_dtype)) return ATTN_ERR_DTYPE;
+    if (!(kv_dtype == src_dtype || kv_dtype == ATTN_FP8_E4M3)) return ATTN_ERR_DTYPE;
+    if (T < 0 || Hkv <= 0 || num_blocks < 0 || key_stride_tok < (int64_t)Hkv * D ||
+        value_stride_tok < (int64_t)Hkv * D)
+        return ATTN_ERR_SHAPE;
+    if (kv_dtype == ATTN_FP8_E4M3 && !(k_scale > 0.f && v_scale > 0.f)) return ATTN_ERR_SHAPE;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        key_stride_tok % 8 != 0 || value_stride_tok % 8 != 0)
+        return ATTN_ERR_ALIGN;
+    if (T == 0) return ATTN_OK;
+    DevInfo *dev = nullptr;
+    attn_status st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    return check_cuda(launch_kv_write(key, key_stride_tok, value, value_stride_tok, k_cache, v_cache, slot_mapping, T,
+                                      Hkv, D, block_size, num_blocks, src_dtype, kv_dtype, k_scale, v_scale, dev->err,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

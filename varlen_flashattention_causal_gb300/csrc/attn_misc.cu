@@ -1,0 +1,251 @@
+// attn_misc.cu -- the memory-bound side kernels of the attention path:
+//   * kv_write_kernel   reshape_and_cache_flash ("FlashAttention deep dive",
+//                       KV cache update): scatter new K/V rows to their slots,
+//                       optionally quantising to e4m3
+//   * combine_kernel    split-KV reduction ("vLLM 中 Attention Kernel 如何并行
+//                       处理多个请求", sec. 12): merge the per-segment states
+//   * merge_kernel      merge_attn_states (cascade attention, stage 3)
+#include <climits>
+
+#include "common.cuh"
+
+namespace attn {
+
+// ----------------------------------------------------------------- KV write
+
+// One thread moves 8 consecutive elements (16 source bytes) of one
+// (token, KV head) row.  slot < 0 skips the token; a slot past the cache is
+// never written and raises ERR_SLOT.
+template <int ST, int CT>
+__global__ void __launch_bounds__(256) kv_write_kernel(const uint8_t *__restrict__ key, int64_t ks,
+                                                        const uint8_t *__restrict__ value, int64_t vs,
+                                                        uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+                                                        const int64_t *__restrict__ slot_mapping, int T, int Hkv,
+                                                        int D, int bs, int num_blocks, float k_scale, float v_scale,
+                                                        unsigned *err) {
+    const int chunks = D / 8;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t total = (int64_t)T * Hkv * chunks;
+    if (idx >= total) return;
+    const int c = (int)(idx % chunks);
+    const int h = (int)((idx / chunks) % Hkv);
+    const int64_t t = idx / ((int64_t)chunks * Hkv);
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;
+    if (slot >= (int64_t)num_blocks * bs) {
+        raise_error(err, ERR_SLOT);
+        return;
+    }
+    const int64_t src_k = (t * ks + (int64_t)h * D + c * 8) * 2;
+    const int64_t src_v = (t * vs + (int64_t)h * D + c * 8) * 2;
+    const int64_t dst = (slot * Hkv + h) * D + c * 8;   // elements; slot = block * bs + row
+    const int4 kx = ldg_nc16(key + src_k);
+    const int4 vx = ldg_nc16(value + src_v);
+    if constexpr (CT == ST) {
+        *reinterpret_cast<int4 *>(k_cache + dst * 2) = kx;
+        *reinterpret_cast<int4 *>(v_cache + dst * 2) = vx;
+    } else {
+        // e4m3(x / scale): fp32 division (IEEE, round to nearest), then one
+        // rounding to e4m3, nearest-even, saturating to +-448
+        using T = typename Elem<ST>::T;
+        const T *ke = reinterpret_cast<const T *>(&kx);
+        const T *ve = reinterpret_cast<const T *>(&vx);
+        uint32_t kq[2], vq[2];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            uint32_t kw = 0, vw = 0;
+#pragma unroll
+            for (int j = 0; j < 4; j += 2) {
+                const float2 kf = make_float2(__fdiv_rn(to_float(ke[w * 4 + j]), k_scale),
+                                              __fdiv_rn(to_float(ke[w * 4 + j + 1]), k_scale));
+                const float2 vf = make_float2(__fdiv_rn(to_float(ve[w * 4 + j]), v_scale),
+                                              __fdiv_rn(to_float(ve[w * 4 + j + 1]), v_scale));
+                const uint32_t k2 = __nv_cvt_float2_to_fp8x2(kf, __NV_SATFINITE, __NV_E4M3);
+                const uint32_t v2 = __nv_cvt_float2_to_fp8x2(vf, __NV_SATFINITE, __NV_E4M3);
+                kw |= (k2 & 0xffffu) << (j * 8);
+                vw |= (v2 & 0xffffu) << (j * 8);
+            }
+            kq[w] = kw;
+            vq[w] = vw;
+        }
+        *reinterpret_cast<uint2 *>(k_cache + dst) = make_uint2(kq[0], kq[1]);
+        *reinterpret_cast<uint2 *>(v_cache + dst) = make_uint2(vq[0], vq[1]);
+    }
+}
+
+cudaError_t launch_kv_write(const void *key, int64_t ks, const void *value, int64_t vs, void *k_cache,
+                            void *v_cache, const int64_t *slot, int T, int Hkv, int D, int bs, int num_blocks,
+                            int src_dtype, int kv_dtype, float k_scale, float v_scale, unsigned *err,
+                            cudaStream_t stream) {
+    const int64_t total = (int64_t)T * Hkv * (D / 8);
+    if (total == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((total + 255) / 256);
+    auto *k = reinterpret_cast<const uint8_t *>(key);
+    auto *v = reinterpret_cast<const uint8_t *>(value);
+    auto *kc = reinterpret_cast<uint8_t *>(k_cache);
+    auto *vc = reinterpret_cast<uint8_t *>(v_cache);
+#define KVW(ST, CT)                                                                                          \
+    kv_write_kernel<ST, CT><<<blocks, 256, 0, stream>>>(k, ks, v, vs, kc, vc, slot, T, Hkv, D, bs, num_blocks, \
+                                                         k_scale, v_scale, err)
+    if (src_dtype == DT_BF16 && kv_dtype == DT_BF16) KVW(DT_BF16, DT_BF16);
+    else if (src_dtype == DT_FP16 && kv_dtype == DT_FP16) KVW(DT_FP16, DT_FP16);
+    else if (src_dtype == DT_BF16 && kv_dtype == DT_E4M3) KVW(DT_BF16, DT_E4M3);
+    else if (src_dtype == DT_FP16 && kv_dtype == DT_E4M3) KVW(DT_FP16, DT_E4M3);
+    else return cudaErrorInvalidValue;
+#undef KVW
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ state merges
+
+template <class T>
+__device__ __forceinline__ float4 load4(const T *p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+template <>
+__device__ __forceinline__ float4 load4<__half>(const __half *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <class T>
+__device__ __forceinline__ void store4(T *p, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float *p, float4 v) {
+    *reinterpret_cast<float4 *>(p) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v) {
+    *reinterpret_cast<uint2 *>(p) = make_uint2(pack2<true>(v.x, v.y), pack2<true>(v.z, v.w));
+}
+template <>
+__device__ __forceinline__ void store4<__half>(__half *p, float4 v) {
+    *reinterpret_cast<uint2 *>(p) = make_uint2(pack2<false>(v.x, v.y), pack2<false>(v.z, v.w));
+}
+
+// One warp per (token, query head).  Segment s contributes with weight
+// exp(lse_s - lse), lse = log sum_s exp(lse_s); segments with lse_s = -inf
+// (no visible key) contribute nothing.
+template <class OT>
+__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+    const int warp_global = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp_global >= p.T * p.Hq) return;
+    const int64_t t = warp_global / p.Hq;
+    const int h = warp_global % p.Hq;
+    const int64_t base = (t * p.Hq + h) * (int64_t)p.nsplit;
+    const float *ls = p.part_lse + base;
+    float mx = -INFINITY;
+    for (int s = lane; s < p.nsplit; s += 32) mx = fmaxf(mx, ls[s]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const int D = p.D;
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+        for (int s = 0; s < p.nsplit; ++s) {
+            const float l = ls[s];
+            if (l == -INFINITY) continue;
+            const float w = expf(l - mx);
+            wsum += w;
+            const float *po = p.part_o + (base + s) * D;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int d = (lane + 32 * k) * 4;
+                if (d < D) {
+                    const float4 v = *reinterpret_cast<const float4 *>(po + d);
+                    acc[k].x += w * v.x;
+                    acc[k].y += w * v.y;
+                    acc[k].z += w * v.z;
+                    acc[k].w += w * v.w;
+                }
+            }
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    OT *out = reinterpret_cast<OT *>(p.out) + t * p.out_stride + (int64_t)h * D;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int d = (lane + 32 * k) * 4;
+        if (d < D) {
+            float4 v = acc[k];
+            v.x *= inv;
+            v.y *= inv;
+            v.z *= inv;
+            v.w *= inv;
+            store4<OT>(out + d, v);
+        }
+    }
+    if (lane == 0 && p.lse) p.lse[t * p.Hq + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
+cudaError_t launch_combine(const CombineParams &p, int out_dtype, cudaStream_t stream) {
+    const int64_t threads = (int64_t)p.T * p.Hq * 32;
+    if (threads == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((threads + 127) / 128);
+    if (out_dtype == DT_BF16) combine_kernel<__nv_bfloat16><<<blocks, 128, 0, stream>>>(p);
+    else if (out_dtype == DT_FP16) combine_kernel<__half><<<blocks, 128, 0, stream>>>(p);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+// merge_attn_states: two states per (token, head), one warp each
+template <class T>
+__global__ void __launch_bounds__(128) merge_kernel(T *out, float *lse_out, const T *o1, const float *lse1,
+                                                    const T *o2, const float *lse2, int T_, int Hq, int D) {
+    const int warp_global = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp_global >= T_ * Hq) return;
+    const int64_t row = warp_global;
+    const float a = lse1[row], b = lse2[row];
+    const float mx = fmaxf(a, b);
+    float w1 = 0.f, w2 = 0.f, l = -INFINITY;
+    if (mx != -INFINITY) {
+        const float e1 = expf(a - mx), e2 = expf(b - mx);
+        const float s = e1 + e2;
+        w1 = e1 / s;
+        w2 = e2 / s;
+        l = mx + logf(s);
+    }
+    for (int d = lane * 4; d < D; d += 128) {
+        const float4 x = load4<T>(o1 + row * D + d);
+        const float4 y = load4<T>(o2 + row * D + d);
+        float4 z;
+        z.x = w1 * x.x + w2 * y.x;
+        z.y = w1 * x.y + w2 * y.y;
+        z.z = w1 * x.z + w2 * y.z;
+        z.w = w1 * x.w + w2 * y.w;
+        store4<T>(out + row * D + d, z);   // same lane read these elements: out may alias o1/o2
+    }
+    if (lane == 0 && lse_out) lse_out[row] = l;
+}
+
+cudaError_t launch_merge(void *out, float *lse_out, const void *o1, const float *lse1, const void *o2,
+                         const float *lse2, int T, int Hq, int D, int dtype, cudaStream_t stream) {
+    const int64_t threads = (int64_t)T * Hq * 32;
+    if (threads == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((threads + 127) / 128);
+#define MRG(TYPE)                                                                                              \
+    merge_kernel<TYPE><<<blocks, 128, 0, stream>>>(reinterpret_cast<TYPE *>(out), lse_out,                     \
+                                                   reinterpret_cast<const TYPE *>(o1), lse1,                   \
+                                                   reinterpret_cast<const TYPE *>(o2), lse2, T, Hq, D)
+    if (dtype == DT_BF16) MRG(__nv_bfloat16);
+    else if (dtype == DT_FP16) MRG(__half);
+    else if (dtype == DT_FP32) MRG(float);
+    else return cudaErrorInvalidValue;
+#undef MRG
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,466 @@
+// attn_mma.cu -- FlashAttention-style forward over a paged KV cache with
+// warp-level mma.sync (m16n8k16) tensor-core tiles.
+//
+// This kernel serves the rows-light side of the hot path: decode (one query
+// token per request), multi-token verification and short queries.  Its
+// tiles are 16 query rows per warp, the smallest tensor-core tile, so the
+// G query heads that share a KV head (GQA) are packed into the rows and
+// every K/V tile fetched from HBM serves all of them.  The kernel is
+// HBM-bound: one K/V row per (token, KV head) is read exactly once.
+//
+// Work of one CTA ("vLLM 中 Attention Kernel 如何并行处理多个请求", sec. 3 and 12):
+// one request x one KV head x one block of packed query rows x one KV
+// segment.  Rows are (query token, head-in-group) pairs.  The K/V tiles of
+// BN keys are gathered through the block table (sec. 11) with 16-byte
+// cp.async copies into a multi-stage shared-memory ring: each warp computes
+// the addresses of its rows once (one lane per row) and shares them by
+// shuffle, instead of every thread re-deriving 64-bit row pointers
+// ("Making FlashAttention-4 faster for inference", transposed address
+// generation).  Scores are masked in registers from local positions with
+// the bottom-right alignment of sec. 10 (q_abs = ctx + i), only on tiles
+// that need it (sec. 4), and the softmax is the online recurrence of sec. 7.
+// With WN > 1 the warps split each K/V tile's keys (flash-decoding inside
+// the CTA) and merge their states through shared memory at the end; with
+// nsplit > 1 each CTA writes a normalised partial state that the combine
+// kernel merges by log-sum-exp (sec. 12).
+#include "common.cuh"
+
+namespace attn {
+
+template <int D_, int WM_, int WN_, int BN_, int STAGES_, int QT_, int KVT_>
+struct MmaCfg {
+    static constexpr int D = D_, WM = WM_, WN = WN_, BN = BN_, STAGES = STAGES_, QT = QT_, KVT = KVT_;
+    static constexpr int ROWS = 16 * WM;
+    static constexpr bool MMA_BF16 = (KVT == DT_BF16);   // fp16 and e4m3 caches run f16 MMAs
+    static constexpr int KV_BYTES = Elem<KVT>::bytes;
+    static constexpr int KV_ROW = D * KV_BYTES;          // bytes of one cached row (one KV head)
+    static constexpr int TILE_RAW = BN * KV_ROW;         // one K (or V) tile as stored
+    static constexpr int ROW16 = D * 2;                  // one row in 16-bit MMA form
+    static constexpr int TILE16 = BN * ROW16;
+    static constexpr int Q_BYTES = ROWS * ROW16;
+    static constexpr int STAGE_BYTES = 2 * TILE_RAW;
+    static constexpr int CONV_BYTES = (KVT == DT_E4M3) ? 2 * TILE16 : 0;
+    static constexpr int OSTRIDE = D + 4;                // fp32 epilogue row stride (bank spread)
+    static constexpr int EPI_BYTES = WN * ROWS * OSTRIDE * 4 + 2 * WN * ROWS * 4;
+    static constexpr int MAIN_BYTES = STAGES * STAGE_BYTES + CONV_BYTES;
+    static constexpr int SMEM = Q_BYTES + (MAIN_BYTES > EPI_BYTES ? MAIN_BYTES : EPI_BYTES);
+    static constexpr int NW = BN / WN;                   // keys per warp per tile
+    static constexpr int NT = NW / 8;                    // n8 tiles of S per warp
+    static constexpr int KT = D / 16;                    // k16 steps of Q K^T
+    static constexpr int RPW = BN / 4;                   // K/V rows each warp fetches
+    static constexpr int CH = KV_ROW / 16;               // 16-byte chunks per cached row
+    static_assert(WM * WN == 4, "4 warps");
+    static_assert(NT % 2 == 0, "n-tile pairs");
+    static_assert((RPW * CH) % 32 == 0, "whole warp copy rounds");
+};
+
+// two e4m3 values (low byte first) -> two fp16 values in one register; the
+// conversion is exact (every e4m3 value is an fp16 value)
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+template <class C>
+__global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
+    constexpr int D = C::D, ROWS = C::ROWS, BN = C::BN, STAGES = C::STAGES;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *sQ = smem;
+    uint8_t *sMain = smem + C::Q_BYTES;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wm = warp % C::WM, wn = warp / C::WM;
+    const int r = blockIdx.z, kvh = blockIdx.y;
+    const int s_idx = blockIdx.x % p.nsplit;
+    const int rb = p.n_row_blocks - 1 - (int)(blockIdx.x / p.nsplit);   // longest rows first
+
+    int q_start, q_len;
+    if (p.cu_seqlens_q) {
+        q_start = p.cu_seqlens_q[r];
+        q_len = p.cu_seqlens_q[r + 1] - q_start;
+    } else {
+        q_start = r;
+        q_len = 1;
+    }
+    const int kv_len = p.seqused_k[r];
+    const int G = p.G;
+    const int rows = q_len * G;
+    if (rows < p.rows_lo || rows > p.rows_hi) return;
+    const int row0 = rb * ROWS;
+    if (row0 >= rows) return;
+    const int row_end = min(row0 + ROWS, rows);
+    const int ctx = kv_len - q_len;                  // cached context before the queries
+    const int i_min = row0 / G, i_max = (row_end - 1) / G;
+    int kv_end = kv_len;
+    if (p.causal) kv_end = min(kv_len, ctx + i_max + 1);
+    const int kv_lo = s_idx * p.split_chunk;
+    const int kv_hi = min(kv_end, kv_lo + p.split_chunk);
+
+    if (kv_lo >= kv_hi) {
+        // no key in this segment for any row of the block: empty state
+        for (int pr = row0 + tid; pr < row_end; pr += blockDim.x) {
+            const int64_t tok = q_start + pr / G;
+            const int h = kvh * G + pr % G;
+            if (p.nsplit > 1) {
+                p.part_lse[(tok * p.Hq + h) * p.nsplit + s_idx] = -INFINITY;
+            } else {
+                if (p.lse) p.lse[tok * p.Hq + h] = -INFINITY;
+                using OT = typename Elem<C::QT>::T;
+                OT *o = reinterpret_cast<OT *>(p.out) + tok * p.out_stride + (int64_t)h * D;
+                for (int d = 0; d < D; ++d) o[d] = OT(0.f);
+            }
+        }
+        return;
+    }
+
+    // ---- Q rows of this block -> shared memory (16-bit MMA form, swizzled)
+    for (int c = tid; c < ROWS * (D / 8); c += blockDim.x) {
+        const int lr = c / (D / 8), ch = c % (D / 8);
+        const int pr = row0 + lr;
+        int4 v = make_int4(0, 0, 0, 0);
+        if (pr < row_end) {
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(p.q) +
+                                 ((int64_t)(q_start + pr / G) * p.q_stride + (int64_t)(kvh * G + pr % G) * D) * 2 +
+                                 ch * 16;
+            v = ldg_nc16(src);
+            if constexpr (C::QT == DT_BF16 && !C::MMA_BF16) {
+                const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&v);
+                int4 w;
+                uint32_t *wu = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = __bfloat1622float2(b[k]);
+                    wu[k] = pack2<false>(f.x, f.y);
+                }
+                v = w;
+            }
+        }
+        *reinterpret_cast<int4 *>(sQ + swz(lr, ch, C::ROW16)) = v;
+    }
+
+    // ---- K/V tile gather through the block table
+    const int64_t bt_base = (int64_t)r * p.bt_stride;
+    const uint8_t *kbase = reinterpret_cast<const uint8_t *>(p.k_cache);
+    const uint8_t *vbase = reinterpret_cast<const uint8_t *>(p.v_cache);
+    auto load_tile = [&](int t, int stage) {
+        const int n0 = kv_lo + t * BN;
+        int64_t off = 0;
+        int ok = 0;
+        if (lane < C::RPW) {
+            const int tok = n0 + warp * C::RPW + lane;
+            if (tok < kv_hi) {
+                const int blk = p.block_table[bt_base + tok / p.bs];
+                if ((unsigned)blk < (unsigned)p.num_blocks) {
+                    ok = 1;
+                    off = (((int64_t)blk * p.bs + tok % p.bs) * p.Hkv + kvh) * (int64_t)C::KV_ROW;
+                } else {
+                    raise_error(p.err, ERR_BLOCK_ID);
+                }
+            }
+        }
+        uint8_t *sK = sMain + stage * C::STAGE_BYTES;
+        uint8_t *sV = sK + C::TILE_RAW;
+#pragma unroll
+        for (int it = 0; it < C::RPW * C::CH / 32; ++it) {
+            const int idx = it * 32 + lane;
+            const int lr = idx / C::CH, ch = idx % C::CH;
+            const int64_t o = __shfl_sync(0xffffffffu, off, lr);
+            const int v = __shfl_sync(0xffffffffu, ok, lr);
+            const int row = warp * C::RPW + lr;
+            const uint32_t dst = (C::KVT == DT_E4M3) ? (uint32_t)(row * C::KV_ROW + ch * 16)
+                                                     : swz(row, ch, C::KV_ROW);
+            const int64_t so = v ? o + ch * 16 : 0;
+            cp_async16(smem_u32(sK + dst), kbase + so, v ? 16 : 0);
+            cp_async16(smem_u32(sV + dst), vbase + so, v ? 16 : 0);
+        }
+    };
+
+    // e4m3 tiles are widened to fp16 (exact) into a swizzled tile for ldmatrix
+    uint8_t *cK = sMain + STAGES * C::STAGE_BYTES;
+    uint8_t *cV = cK + C::TILE16;
+    auto convert_tile = [&](int stage) {
+        const uint8_t *sK = sMain + stage * C::STAGE_BYTES;
+        const uint8_t *sV = sK + C::TILE_RAW;
+        for (int c = tid; c < BN * D / 16; c += blockDim.x) {
+            const int row = c / (D / 16), ch = c % (D / 16);
+            const int4 rk = *reinterpret_cast<const int4 *>(sK + row * D + ch * 16);
+            const int4 rv = *reinterpret_cast<const int4 *>(sV + row * D + ch * 16);
+            const uint16_t *bk = reinterpret_cast<const uint16_t *>(&rk);
+            const uint16_t *bv = reinterpret_cast<const uint16_t *>(&rv);
+            int4 k0, k1, v0, v1;
+            uint32_t *uk0 = reinterpret_cast<uint32_t *>(&k0), *uk1 = reinterpret_cast<uint32_t *>(&k1);
+            uint32_t *uv0 = reinterpret_cast<uint32_t *>(&v0), *uv1 = reinterpret_cast<uint32_t *>(&v1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uk0[k] = e4m3x2_to_h2(bk[k]);
+                uk1[k] = e4m3x2_to_h2(bk[k + 4]);
+                uv0[k] = e4m3x2_to_h2(bv[k]);
+                uv1[k] = e4m3x2_to_h2(bv[k + 4]);
+            }
+            *reinterpret_cast<int4 *>(cK + swz(row, 2 * ch, C::ROW16)) = k0;
+            *reinterpret_cast<int4 *>(cK + swz(row, 2 * ch + 1, C::ROW16)) = k1;
+            *reinterpret_cast<int4 *>(cV + swz(row, 2 * ch, C::ROW16)) = v0;
+            *reinterpret_cast<int4 *>(cV + swz(row, 2 * ch + 1, C::ROW16)) = v1;
+        }
+    };
+
+    const int n_tiles = (kv_hi - kv_lo + BN - 1) / BN;
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < n_tiles) load_tile(s, s);
+        cp_async_commit();
+    }
+    __syncthreads();   // Q visible to every warp
+
+    uint32_t qf[C::KT][4];
+#pragma unroll
+    for (int kk = 0; kk < C::KT; ++kk) {
+        const int row = wm * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int ch = kk * 2 + (lane >> 4);
+        ldmatrix_x4(qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], smem_u32(sQ + swz(row, ch, C::ROW16)));
+    }
+
+    // query token (local index) of the two rows this thread owns in C frags
+    const int ir0 = (row0 + wm * 16 + (lane >> 2)) / G;
+    const int ir1 = (row0 + wm * 16 + (lane >> 2) + 8) / G;
+    const int lim0 = p.causal ? ctx + ir0 : INT_MAX;   // last visible key of row 0
+    const int lim1 = p.causal ? ctx + ir1 : INT_MAX;
+
+    float o[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY};
+    float l[2] = {0.f, 0.f};
+
+    for (int t = 0; t < n_tiles; ++t) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        {
+            const int tn = t + STAGES - 1;
+            if (tn < n_tiles) load_tile(tn, tn % STAGES);
+            cp_async_commit();
+        }
+        const uint8_t *tK, *tV;
+        if constexpr (C::KVT == DT_E4M3) {
+            convert_tile(t % STAGES);
+            __syncthreads();
+            tK = cK;
+            tV = cV;
+        } else {
+            tK = sMain + (t % STAGES) * C::STAGE_BYTES;
+            tV = tK + C::TILE_RAW;
+        }
+        const int n0 = kv_lo + t * BN;
+
+        // S = Q K^T for this warp's NW keys
+        float s[C::NT][4];
+#pragma unroll
+        for (int i = 0; i < C::NT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < C::KT; ++kk) {
+#pragma unroll
+            for (int j = 0; j < C::NT / 2; ++j) {
+                const int key = wn * C::NW + j * 16 + (lane & 7) + (lane >> 4) * 8;
+                const int ch = kk * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(b0, b1, b2, b3, smem_u32(tK + swz(key, ch, C::ROW16)));
+                mma16816<C::MMA_BF16>(s[2 * j], qf[kk], b0, b1);
+                mma16816<C::MMA_BF16>(s[2 * j + 1], qf[kk], b2, b3);
+            }
+        }
+
+        // scale to log2 units; mask only tiles crossing the sequence end or
+        // the causal diagonal ("full" tiles skip this, sec. 4)
+        const bool need_mask =
+            (n0 + BN > kv_hi) || (p.causal && tile_kind(i_min, i_max + 1, n0, n0 + BN, ctx) != 1);
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float v = s[nt][e] * p.scale_log2;
+                if (need_mask) {
+                    const int key = n0 + wn * C::NW + nt * 8 + 2 * (lane & 3) + (e & 1);
+                    const int lim = (e >> 1) ? lim1 : lim0;
+                    if (key >= kv_hi || key > lim) v = -INFINITY;
+                }
+                s[nt][e] = v;
+            }
+        }
+
+        // online softmax (two rows per thread, four lanes per row)
+        float mx[2] = {m[0], m[1]};
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+            mx[0] = fmaxf(mx[0], fmaxf(s[nt][0], s[nt][1]));
+            mx[1] = fmaxf(mx[1], fmaxf(s[nt][2], s[nt][3]));
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+        }
+        float base[2], alpha[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            base[h] = (mx[h] == -INFINITY) ? 0.f : mx[h];   // fully masked row so far
+            alpha[h] = ex2(m[h] - base[h]);
+            m[h] = mx[h];
+        }
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+            s[nt][0] = ex2(s[nt][0] - base[0]);
+            s[nt][1] = ex2(s[nt][1] - base[0]);
+            s[nt][2] = ex2(s[nt][2] - base[1]);
+            s[nt][3] = ex2(s[nt][3] - base[1]);
+            rs[0] += s[nt][0] + s[nt][1];
+            rs[1] += s[nt][2] + s[nt][3];
+        }
+        l[0] = l[0] * alpha[0] + rs[0];
+        l[1] = l[1] * alpha[1] + rs[1];
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+            o[i][0] *= alpha[0];
+            o[i][1] *= alpha[0];
+            o[i][2] *= alpha[1];
+            o[i][3] *= alpha[1];
+        }
+
+        // O += P V (P re-used from the S accumulators as A fragments)
+#pragma unroll
+        for (int kk = 0; kk < C::NW / 16; ++kk) {
+            uint32_t a[4];
+            a[0] = pack2<C::MMA_BF16>(s[2 * kk][0], s[2 * kk][1]);
+            a[1] = pack2<C::MMA_BF16>(s[2 * kk][2], s[2 * kk][3]);
+            a[2] = pack2<C::MMA_BF16>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+            a[3] = pack2<C::MMA_BF16>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                const int key = wn * C::NW + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int ch = 2 * j + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(b0, b1, b2, b3, smem_u32(tV + swz(key, ch, C::ROW16)));
+                mma16816<C::MMA_BF16>(o[2 * j], a, b0, b1);
+                mma16816<C::MMA_BF16>(o[2 * j + 1], a, b2, b3);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();   // all shared-memory tiles consumed; reuse for the epilogue
+
+    // ---- epilogue: merge the WN warp states of each row, normalise, store
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+    }
+    float *sO = reinterpret_cast<float *>(sMain);
+    float *sM = sO + C::WN * ROWS * C::OSTRIDE;
+    float *sL = sM + C::WN * ROWS;
+    {
+        const int lr = wm * 16 + (lane >> 2);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+            const int col = i * 8 + 2 * (lane & 3);
+            *reinterpret_cast<float2 *>(&sO[(wn * ROWS + lr) * C::OSTRIDE + col]) = make_float2(o[i][0], o[i][1]);
+            *reinterpret_cast<float2 *>(&sO[(wn * ROWS + lr + 8) * C::OSTRIDE + col]) = make_float2(o[i][2], o[i][3]);
+        }
+        if ((lane & 3) == 0) {
+            sM[wn * ROWS + lr] = m[0];
+            sM[wn * ROWS + lr + 8] = m[1];
+            sL[wn * ROWS + lr] = l[0];
+            sL[wn * ROWS + lr + 8] = l[1];
+        }
+    }
+    __syncthreads();
+
+    constexpr int DV = D / 4;
+    for (int idx = tid; idx < ROWS * DV; idx += blockDim.x) {
+        const int lr = idx / DV, c4 = idx % DV;
+        const int pr = row0 + lr;
+        if (pr >= row_end) continue;
+        float mf = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::WN; ++w) mf = fmaxf(mf, sM[w * ROWS + lr]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lf = 0.f;
+        if (mf != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < C::WN; ++w) {
+                const float sc = ex2(sM[w * ROWS + lr] - mf);
+                lf += sL[w * ROWS + lr] * sc;
+                const float4 v = *reinterpret_cast<const float4 *>(&sO[(w * ROWS + lr) * C::OSTRIDE + c4 * 4]);
+                acc.x += sc * v.x;
+                acc.y += sc * v.y;
+                acc.z += sc * v.z;
+                acc.w += sc * v.w;
+            }
+        }
+        const float inv = lf > 0.f ? p.v_descale / lf : 0.f;
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
+        const float lse_v = lf > 0.f ? (mf + __log2f(lf)) * 0.6931471805599453f : -INFINITY;
+        const int64_t tok = q_start + pr / G;
+        const int h = kvh * G + pr % G;
+        if (p.nsplit == 1) {
+            using OT = typename Elem<C::QT>::T;
+            OT *dst = reinterpret_cast<OT *>(p.out) + tok * p.out_stride + (int64_t)h * D + c4 * 4;
+            uint2 pk;
+            if constexpr (C::QT == DT_BF16) {
+                pk.x = pack2<true>(acc.x, acc.y);
+                pk.y = pack2<true>(acc.z, acc.w);
+            } else {
+                pk.x = pack2<false>(acc.x, acc.y);
+                pk.y = pack2<false>(acc.z, acc.w);
+            }
+            *reinterpret_cast<uint2 *>(dst) = pk;
+            if (c4 == 0 && p.lse) p.lse[tok * p.Hq + h] = lse_v;
+        } else {
+            const int64_t slot = (tok * p.Hq + h) * p.nsplit + s_idx;
+            *reinterpret_cast<float4 *>(p.part_o + slot * D + c4 * 4) = acc;
+            if (c4 == 0) p.part_lse[slot] = lse_v;
+        }
+    }
+}
+
+template <class C>
+static cudaError_t launch_cfg(const FwdParams &p, cudaStream_t stream) {
+    auto kern = fwd_mma_kernel<C>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(p.n_row_blocks * p.nsplit), (unsigned)p.Hkv, (unsigned)p.B);
+    kern<<<grid, 128, C::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, int QT, int KVT>
+static cudaError_t launch_rows(const FwdParams &p, int rows_per_cta, cudaStream_t stream) {
+    constexpr int STAGES = (KVT == DT_E4M3) ? 4 : (D == 128 ? 3 : 4);
+    switch (rows_per_cta) {
+    case 16: return launch_cfg<MmaCfg<D, 1, 4, 64, STAGES, QT, KVT>>(p, stream);
+    case 32: return launch_cfg<MmaCfg<D, 2, 2, 64, STAGES, QT, KVT>>(p, stream);
+    default: return launch_cfg<MmaCfg<D, 4, 1, 64, STAGES, QT, KVT>>(p, stream);
+    }
+}
+
+template <int D>
+static cudaError_t launch_d(const FwdParams &p, int q_dtype, int kv_dtype, int rows_per_cta, cudaStream_t s) {
+    if (q_dtype == DT_BF16 && kv_dtype == DT_BF16) return launch_rows<D, DT_BF16, DT_BF16>(p, rows_per_cta, s);
+    if (q_dtype == DT_FP16 && kv_dtype == DT_FP16) return launch_rows<D, DT_FP16, DT_FP16>(p, rows_per_cta, s);
+    if (q_dtype == DT_BF16 && kv_dtype == DT_E4M3) return launch_rows<D, DT_BF16, DT_E4M3>(p, rows_per_cta, s);
+    if (q_dtype == DT_FP16 && kv_dtype == DT_E4M3) return launch_rows<D, DT_FP16, DT_E4M3>(p, rows_per_cta, s);
+    return cudaErrorInvalidValue;
+}
+
+int mma_rows_per_cta(int max_rows) { return max_rows <= 16 ? 16 : (max_rows <= 32 ? 32 : 64); }
+
+cudaError_t launch_fwd_mma(const FwdParams &p, int D, int q_dtype, int kv_dtype, int rows_per_cta,
+                           cudaStream_t stream) {
+    if (D == 64) return launch_d<64>(p, q_dtype, kv_dtype, rows_per_cta, stream);
+    if (D == 128) return launch_d<128>(p, q_dtype, kv_dtype, rows_per_cta, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -1,0 +1,80 @@
+// internal.h -- parameter blocks and launcher declarations shared by the
+// translation units of libattn (not part of the public C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+// storage type codes (same numbering as attn_dtype in include/attn.h)
+enum : int { DT_BF16 = 0, DT_FP16 = 1, DT_E4M3 = 2, DT_FP32 = 3 };
+
+// error bits of the device error word
+enum : unsigned { ERR_BLOCK_ID = 1u, ERR_SLOT = 2u };
+
+// One attention launch over the requests whose packed row count
+// rows = q_len * G lies in [rows_lo, rows_hi].  Packed row p of a request
+// is query token p / G, query head kvh * G + p % G (all heads of one KV
+// group side by side, so each K/V tile serves G heads).
+struct FwdParams {
+    const void *q;
+    int64_t q_stride;            // elements between consecutive tokens
+    const void *k_cache;
+    const void *v_cache;
+    void *out;
+    int64_t out_stride;
+    float *lse;                  // [T, Hq] or nullptr
+    const int32_t *cu_seqlens_q; // nullptr: request r owns token r (decode)
+    const int32_t *seqused_k;
+    const int32_t *block_table;
+    int64_t bt_stride;
+    int B, Hq, Hkv, G, bs, num_blocks;
+    int causal;
+    float scale_log2;            // softmax_scale * k_descale * log2(e)
+    float v_descale;
+    int nsplit;                  // KV segments per (request, KV head, row block)
+    int split_chunk;             // keys per segment (multiple of the KV tile)
+    float *part_o;               // [T, Hq, nsplit, D] fp32 (nsplit > 1)
+    float *part_lse;             // [T, Hq, nsplit]
+    int rows_lo, rows_hi;
+    int n_row_blocks;            // grid.x = n_row_blocks * nsplit
+    unsigned *err;
+};
+
+struct CombineParams {
+    const float *part_o;
+    const float *part_lse;
+    void *out;
+    int64_t out_stride;
+    float *lse;
+    int T, Hq, D, nsplit;
+    float v_scale_unused;
+};
+
+// launchers (return the launch error)
+cudaError_t launch_fwd_mma(const FwdParams &p, int D, int q_dtype, int kv_dtype, int rows_per_cta,
+                           cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams &p, int out_dtype, cudaStream_t stream);
+cudaError_t launch_merge(void *out, float *lse_out, const void *o1, const float *lse1, const void *o2,
+                         const float *lse2, int T, int Hq, int D, int dtype, cudaStream_t stream);
+cudaError_t launch_kv_write(const void *key, int64_t ks, const void *value, int64_t vs, void *k_cache,
+                            void *v_cache, const int64_t *slot, int T, int Hkv, int D, int bs, int num_blocks,
+                            int src_dtype, int kv_dtype, float k_scale, float v_scale, unsigned *err,
+                            cudaStream_t stream);
+
+// Tile classification ("vLLM 中 Attention Kernel 如何并行处理多个请求", sec. 4)
+// for query positions [q_lo, q_hi) of a request with cached context ctx
+// (query i sees keys j <= ctx + i) against keys [k_lo, k_hi):
+// 0 = skip (all in the future), 1 = full (no mask), 2 = diagonal (mask).
+__host__ __device__ inline int tile_kind(int q_lo, int q_hi, int k_lo, int k_hi, int ctx) {
+    if (q_hi <= q_lo || k_hi <= k_lo) return 0;
+    if ((long long)k_lo > (long long)ctx + q_hi - 1) return 0;
+    if ((long long)k_hi - 1 <= (long long)ctx + q_lo) return 1;
+    return 2;
+}
+
+// rows per CTA of the mma kernel for a given largest packed row count
+int mma_rows_per_cta(int max_rows);
+
+}  // namespace attn
