@@ -141,6 +141,48 @@ attn_status attn_paged_decode(
     int num_splits, void *workspace, size_t ws_bytes, attn_stream_t stream);
 
 /*
+ * attn_paged_decode_noalloc -- attn_paged_decode for callers that cannot
+ * allocate device memory.  (The source pages have no counterpart: this is a
+ * deployment convenience, not part of the method.)
+ *
+ * Who needs it: code that may not call cudaMalloc or an allocating library
+ * routine -- for instance a plugin inside a host framework that owns every
+ * device allocation, or a latency-critical serving loop where cudaMalloc /
+ * cudaFree can synchronise the device and stall other work.  The caller
+ * still passes q, the caches, out, lse_out and the tables; only the split-KV
+ * scratch (per-segment partial outputs) is taken from a fixed array of
+ * ATTN_NOALLOC_SCRATCH_BYTES that the library keeps in device memory.
+ *
+ * Arguments and results are those of attn_paged_decode without the
+ * workspace.  num_splits = 0 picks the split count automatically and caps it
+ * to what fits in the array; an explicit num_splits > 1 whose partials need
+ * more than ATTN_NOALLOC_SCRATCH_BYTES (attn_workspace_size(B, Hq, D,
+ * num_splits)) returns ATTN_ERR_WORKSPACE and launches nothing.
+ *
+ * Notes for callers:
+ *  - Every GPU that loads the library holds the array until the process
+ *    exits, whether or not this entry point is used.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress) and caches it; make that
+ *    first call before any stream capture.
+ *  - All calls on a device share the one array and it keeps whatever the
+ *    last call left in it.  Nothing in it needs to start at zero (every slot
+ *    read is written earlier in the same call), but calls whose execution
+ *    overlaps on the GPU (different streams, or different host threads)
+ *    race on it: serialise them.
+ *  - Allocates nothing and calls no allocating routine.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+attn_status attn_paged_decode_noalloc(
+    const void *q, const void *k_cache, const void *v_cache,
+    void *out, float *lse_out,
+    const int32_t *seq_lens, const int32_t *block_table, int64_t bt_row_stride,
+    int B, int max_seq_len, int Hq, int Hkv, int D, int block_size, int num_blocks,
+    attn_dtype q_dtype, attn_dtype kv_dtype,
+    float softmax_scale, float k_descale, float v_descale,
+    int num_splits, attn_stream_t stream);
+
+/*
  * attn_merge_states -- [vLLM-FA] merge_attn_states: combine two attention
  * results over disjoint key sets (cascade prefix and suffix):
  *   lse = log(exp(lse1) + exp(lse2)),

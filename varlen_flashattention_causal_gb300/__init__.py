@@ -223,3 +223,39 @@ def attn_device_error_flag(reset=False):
     if v < 0:
         raise RuntimeError("attn_device_error_flag: CUDA call failed")
     return v
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20   # ATTN_NOALLOC_SCRATCH_BYTES in include/attn.h
+
+
+def attn_paged_decode_noalloc(q, k_cache, v_cache, out, seq_lens, block_table, max_seq_len,
+                              softmax_scale, lse_out=None, k_descale=1.0, v_descale=1.0,
+                              num_splits=0, stream=None):
+    """attn_paged_decode for callers that cannot allocate device memory.
+
+    Some callers may not allocate: a plugin inside a framework that owns all
+    device memory, or a serving loop that cannot afford the device
+    synchronisation cudaMalloc/cudaFree may cause.  This wrapper allocates
+    nothing (no workspace tensor either): the split-KV scratch is a fixed
+    8 MiB array inside libattn.so.  Calls on one device share that array,
+    so calls that overlap on the GPU race; serialise them.  An explicit
+    num_splits too large for the array raises AttnError (ATTN_ERR_WORKSPACE).
+    """
+    lib = _load()
+    fn = lib.attn_paged_decode_noalloc
+    if fn.argtypes is None:
+        c = ctypes
+        fn.restype = c.c_int
+        fn.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,
+                       c.c_int64, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
+                       c.c_int, c.c_float, c.c_float, c.c_float, c.c_int, c.c_void_p]
+    B, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    _i32(seq_lens, "seq_lens")
+    if block_table.dtype != torch.int32 or block_table.stride(-1) != 1:
+        raise TypeError("block_table must be int32 with unit column stride")
+    st = fn(_p(q), _p(k_cache), _p(v_cache), _p(out), _p(lse_out), _p(seq_lens), _p(block_table),
+            block_table.stride(0), B, int(max_seq_len), Hq, Hkv, D, bs, nb, _dt(q), _dt(k_cache),
+            float(softmax_scale), float(k_descale), float(v_descale), int(num_splits), _stream(stream))
+    _check("attn_paged_decode_noalloc", st)
+    return out
