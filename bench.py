@@ -304,7 +304,7 @@ def prefill_stats(va, dev, args, tc_peak):
     return {"workload": "chunked varlen causal prefill: B=16, new U[1k,8k] on cached U[0,4k], Hq=32, "
                         "Hkv=8, D=128, bf16, block_size 64",
             "tflops": round(tf, 1), "ms": round(ms, 4), "flops": fl, "peak": tc_peak,
-            "frac": round(tf / tc_peak, 4), "bound": "tensor", "kernel": "fwd_mma_kernel (mma.sync)"}
+            "frac": round(tf / tc_peak, 4), "bound": "tensor", "kernel": "fwd_tc_kernel (tcgen05)"}
 
 
 def _oracle_decode_setup():

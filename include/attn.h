@@ -25,9 +25,11 @@
  *    non-zero status nothing was launched and no memory was touched.
  *  - Block ids and slots are also checked inside the kernels: an id outside
  *    [0, num_blocks) or a slot outside [0, num_blocks * block_size) is never
- *    dereferenced (attention: the rows of that block read as zero K and V;
- *    KV write: the token is skipped) and the device error word read by
- *    attn_device_error_flag() is raised.
+ *    dereferenced and the device error word read by attn_device_error_flag()
+ *    is raised.  KV write: the token is skipped.  Attention: the result of
+ *    the affected request is unspecified (the rows-light kernel reads zero K
+ *    and V for that block, the tensor-core kernel reads block 0 instead);
+ *    every other request is unaffected.
  *  - Layouts are row-major with the last dimension contiguous:
  *      q, out      [T, Hq, D]        token stride given in elements
  *      lse         [T, Hq] fp32      natural-log log-sum-exp per query head
@@ -244,7 +246,9 @@ const char *attn_status_string(attn_status s);
 /*
  * attn_device_error_flag -- read (and with reset != 0, clear) the device
  * error word of the current device: bit 0 = a block id outside
- * [0, num_blocks) was met, bit 1 = a slot outside the cache was met.
+ * [0, num_blocks) was met, bit 1 = a slot outside the cache was met, bit 2 =
+ * a pipeline wait in the tensor-core kernel gave up after 2 s (an internal
+ * error; that launch's output is invalid).
  * Returns -1 if the CUDA call failed.  Synchronises the device.
  */
 int attn_device_error_flag(int reset);

@@ -169,6 +169,13 @@ CASES = [
     ([129, 64, 1], [129, 500, 257], 4, 1, 128, 256, True),       # several row blocks, ragged tails
     ([7, 9], [20, 9], 6, 3, 64, 32, False),                      # non-causal (cascade prefix stage)
     ([2, 3], [2, 3], 1, 1, 128, 16, True),                       # one head
+    # rows-heavy requests (q_len * G > 64) run on the tcgen05 kernel
+    ([300, 70], [300, 500], 8, 2, 128, 16, True),                # 16-row pages, 4 per K/V tile
+    ([200], [100], 4, 1, 128, 64, True),                         # more queries than keys
+    ([90, 150], [90, 150], 2, 2, 128, 32, False),                # G = 1, non-causal
+    ([128, 129, 3], [1000, 129, 40], 16, 1, 128, 48, True),      # G = 16, block size 48
+    ([70, 1], [0, 33], 8, 2, 128, 16, True),                     # kv_len 0 with many rows
+    ([520], [777], 8, 2, 128, 256, True),                        # pages larger than a tile
 ]
 
 

@@ -24,7 +24,7 @@ __all__ = [
 ]
 
 ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3, ATTN_FP32 = 0, 1, 2, 3
-ERR_BLOCK_ID, ERR_SLOT = 1, 2
+ERR_BLOCK_ID, ERR_SLOT, ERR_TIMEOUT = 1, 2, 4
 
 _lib = None
 

@@ -58,23 +58,48 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t part_o_bytes(int T, int Hq, int D, int ns) { return align256((size_t)T * Hq * ns * D * sizeof(float)); }
 
-// the automatic split rule: without splitting, B * Hkv * row_blocks CTAs
-// run; when that is too few to fill the GPU several times over, cut each
-// request's keys into segments of at least two K/V tiles
-int auto_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int sms) {
-    if (B <= 0 || Hkv <= 0 || Hq <= 0 || max_seqlen_k <= 0) return 1;
-    const int G = Hq / Hkv;
-    const int rows = std::max(1, max_seqlen_q) * G;
-    const int rpc = mma_rows_per_cta(rows);
-    const long long row_blocks = (rows + rpc - 1) / rpc;
-    const long long base = (long long)B * Hkv * row_blocks;
-    const long long target = 4LL * sms;            // two resident CTAs per SM, two waves
+// packed rows (q_len * G) up to which a request runs on the mma.sync
+// kernel; larger requests run on the tcgen05 kernel when it supports the shape
+constexpr int kSmallRows = 64;
+
+// the automatic split rule: without splitting, `base` CTAs run; when that
+// is too few to fill the GPU several times over, cut each request's keys
+// into segments of at least two K/V tiles
+int auto_splits(long long base, int max_seqlen_k, long long target) {
+    if (base <= 0 || max_seqlen_k <= 0) return 1;
     if (base >= target) return 1;
     const int tiles = (max_seqlen_k + kTileN - 1) / kTileN;
     long long s = (2 * target + base - 1) / base;
     s = std::min<long long>(s, tiles / 2);
     s = std::min<long long>(s, kMaxSplits);
     return (int)std::max<long long>(s, 1);
+}
+
+struct Plan {
+    bool tc;              // rows-heavy requests go to the tcgen05 kernel
+    int rpc;              // rows per CTA of the mma kernel
+    int small_rows_hi;    // largest packed row count the mma kernel takes
+    long long base;       // CTAs of the dominant kernel without splitting
+    long long target;
+};
+
+Plan make_plan(int B, int max_q, int Hq, int Hkv, int D, int q_dtype, int kv_dtype, int sms) {
+    Plan pl{};
+    const int G = Hq / Hkv;
+    const int max_rows = std::max(1, max_q) * G;
+    pl.tc = tc_supported(D, q_dtype, kv_dtype, G) && max_rows > kSmallRows;
+    pl.small_rows_hi = pl.tc ? kSmallRows : INT32_MAX;
+    pl.rpc = mma_rows_per_cta(std::min(max_rows, pl.tc ? kSmallRows : max_rows));
+    if (pl.tc) {
+        const long long rb = (max_rows + tc_rows_per_cta() - 1) / tc_rows_per_cta();
+        pl.base = (long long)B * Hkv * rb;
+        pl.target = 2LL * sms;       // one resident CTA per SM, two waves
+    } else {
+        const long long rb = (max_rows + pl.rpc - 1) / pl.rpc;
+        pl.base = (long long)B * Hkv * rb;
+        pl.target = 4LL * sms;       // two resident CTAs per SM, two waves
+    }
+    return pl;
 }
 
 attn_status check_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
@@ -128,10 +153,11 @@ attn_status run_fwd(const FwdArgs &a) {
     if (st != ATTN_OK) return st;
 
     const int G = a.Hq / a.Hkv;
+    const Plan pl = make_plan(a.B, a.max_q, a.Hq, a.Hkv, a.D, a.q_dtype, a.kv_dtype, dev->sms);
     int ns = a.num_splits;
     const size_t per_split = (size_t)a.T * a.Hq * (a.D + 1) * sizeof(float) + 512;
     if (ns == 0) {
-        ns = auto_splits(a.B, a.max_q, a.max_k, a.Hq, a.Hkv, dev->sms);
+        ns = auto_splits(pl.base, a.max_k, pl.target);
         if (ns > 1) {
             const size_t fit = a.ws ? a.ws_bytes / per_split : 0;
             ns = (int)std::min<size_t>((size_t)ns, fit);
@@ -179,13 +205,23 @@ attn_status run_fwd(const FwdArgs &a) {
     }
 
     const int max_rows = std::max(1, a.max_q) * G;
-    const int rpc = mma_rows_per_cta(max_rows);
+    // rows-light requests: mma.sync kernel
     p.rows_lo = 0;
-    p.rows_hi = INT32_MAX;
-    p.n_row_blocks = (max_rows + rpc - 1) / rpc;
+    p.rows_hi = pl.small_rows_hi;
+    p.n_row_blocks = (std::min(max_rows, pl.small_rows_hi) + pl.rpc - 1) / pl.rpc;
     if ((long long)p.n_row_blocks * ns > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-    st = check_cuda(launch_fwd_mma(p, a.D, a.q_dtype, a.kv_dtype, rpc, a.stream));
+    st = check_cuda(launch_fwd_mma(p, a.D, a.q_dtype, a.kv_dtype, pl.rpc, a.stream));
     if (st != ATTN_OK) return st;
+    // rows-heavy requests: tcgen05 kernel
+    if (pl.tc) {
+        FwdParams t = p;
+        t.rows_lo = kSmallRows + 1;
+        t.rows_hi = INT32_MAX;
+        t.n_row_blocks = (max_rows + tc_rows_per_cta() - 1) / tc_rows_per_cta();
+        if ((long long)t.n_row_blocks * ns > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+        st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.T, a.stream));
+        if (st != ATTN_OK) return st;
+    }
 
     if (ns > 1) {
         CombineParams c{};
@@ -213,8 +249,9 @@ size_t attn_workspace_size(int total_q, int Hq, int D, int num_splits) {
 }
 
 int attn_num_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int num_sms) {
-    if (Hkv <= 0 || Hq % Hkv != 0) return 1;
-    return auto_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, num_sms);
+    if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || B <= 0) return 1;
+    const Plan pl = make_plan(B, max_seqlen_q, Hq, Hkv, 128, ATTN_BF16, ATTN_BF16, num_sms);
+    return auto_splits(pl.base, max_seqlen_k, pl.target);
 }
 
 int attn_tile_kind(int q_lo, int q_hi, int k_lo, int k_hi, int ctx) { return tile_kind(q_lo, q_hi, k_lo, k_hi, ctx); }

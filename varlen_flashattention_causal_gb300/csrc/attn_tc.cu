@@ -1,0 +1,520 @@
+// attn_tc.cu -- varlen causal attention over a paged KV cache on the
+// Blackwell tensor cores (tcgen05 MMAs, accumulators in TMEM, TMA loads).
+//
+// This kernel takes the rows-heavy side of the hot path: prefill and
+// chunked prefill, where S = Q K^T and O = P V are genuine dense
+// contractions.  One CTA owns one request x one KV head x 256 packed query
+// rows (two 128-row Q tiles; a row is a (query token, head-in-group) pair,
+// so each K/V tile serves all G query heads of its group) x one KV segment.
+//
+// Roles (10 warps):
+//   warp 0      TMA producer: Q once, then K_j and V_j tiles of 64 keys,
+//               each gathered page by page through the block table ("vLLM 中
+//               Attention Kernel 如何并行处理多个请求", sec. 11) into a ring of
+//               eight 16 KB shared-memory slots (four tiles of look-ahead)
+//   warp 1      MMA issuer (one thread) and TMEM owner.  Per K/V tile j it
+//               issues S_A(j) = Q_A K_j^T, O_A += P_A(j-1) V_(j-1),
+//               S_B(j) = Q_B K_j^T, O_B += P_B(j-1) V_(j-1): between S_X(j)
+//               landing and P_X(j) being needed there are four MMAs for the
+//               softmax of tile X to hide behind
+//   warps 2-5   softmax warpgroup of Q tile A, one thread per row
+//   warps 6-9   softmax warpgroup of Q tile B
+// TMEM columns: S_A [0,64), S_B [64,128), O_A [128,256), O_B [256,384).
+//
+// Softmax (sec. 7): each thread reads its row of S from TMEM, masks it in
+// registers from local positions with the bottom-right alignment of
+// sec. 10 (only on tiles that are not full, sec. 4), and keeps a running
+// maximum m and sum l.  O lives in TMEM and is rescaled only when a row's
+// maximum grows by more than 2^8 (in exp2 units); otherwise P is formed
+// against the stale maximum, which keeps every exponential <= 256 and is
+// exact because l and O share the same reference.  P (bf16/fp16) goes to
+// shared memory in the 128-byte-swizzled K-major layout the MMA reads.
+#include "common.cuh"
+#include "sm100.cuh"
+#include "tma_host.h"
+
+namespace attn {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kBM = 128;                               // rows per Q tile
+constexpr int kBN = 64;                                // keys per K/V tile
+constexpr int kD = 128;                                // head size handled here
+constexpr int kSlots = 8;                              // K/V ring slots
+constexpr int kThreads = 320;
+constexpr uint32_t kQBytes = kBM * kD * 2;             // one Q tile, 32 KB
+constexpr uint32_t kQHalf = kBM * 128;                 // 64 columns of a Q tile
+constexpr uint32_t kTileBytes = kBN * kD * 2;          // one K or V tile, 16 KB
+constexpr uint32_t kKVHalf = kBN * 128;                // 64 columns of a K/V tile
+constexpr uint32_t kPBytes = kBM * kBN * 2;            // one P tile, 16 KB
+constexpr float kRescaleThreshold = 8.0f;              // log2 units
+
+// shared memory map (offsets from a 1024-aligned base)
+constexpr uint32_t kOffQ = 0;                          // Q_A, Q_B
+constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;        // P_A, P_B
+constexpr uint32_t kOffKV = kOffP + 2 * kPBytes;       // ring slots
+constexpr uint32_t kOffBar = kOffKV + kSlots * kTileBytes;
+constexpr int kNumBars = 1 + 2 * kSlots + 4 * 2 + 1;
+constexpr uint32_t kOffMisc = kOffBar + 8 * 32;
+constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+static_assert(kNumBars <= 32, "barrier area");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+// TMEM column offsets of S_x and O_x
+__device__ __forceinline__ uint32_t col_s(int x) { return (uint32_t)x * 64u; }
+__device__ __forceinline__ uint32_t col_o(int x) { return 128u + (uint32_t)x * 128u; }
+
+}  // namespace
+
+struct TcParams {
+    FwdParams f;
+    int kv_rows;        // rows per TMA page load: gcd(block_size, 64)
+};
+
+// whole-warp wait: lane 0 polls, the result is broadcast, so every lane
+// takes the same path into the warp-collective tcgen05 instructions after it
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap qmap,
+                  const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+    const FwdParams &p = tp.f;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (sbase - raw);
+    auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
+    constexpr int B_Q = 0;
+    auto B_FULL = [](int s) { return 1 + s; };
+    auto B_EMPTY = [](int s) { return 1 + kSlots + s; };
+    auto B_SFULL = [](int x) { return 1 + 2 * kSlots + x; };
+    auto B_SFREE = [](int x) { return 3 + 2 * kSlots + x; };
+    auto B_PFULL = [](int x) { return 5 + 2 * kSlots + x; };
+    auto B_ODONE = [](int x) { return 7 + 2 * kSlots + x; };
+    constexpr int B_DRAIN = 9 + 2 * kSlots;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc);
+    uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc + 8);
+    volatile int *never = reinterpret_cast<volatile int *>(sm + kOffMisc + 16);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = blockIdx.z, kvh = blockIdx.y;
+    const int s_idx = blockIdx.x % p.nsplit;
+    const int rb = p.n_row_blocks - 1 - (int)(blockIdx.x / p.nsplit);
+
+    // ---- per-CTA work (uniform over the CTA)
+    const int q_start = p.cu_seqlens_q[r];
+    const int q_len = p.cu_seqlens_q[r + 1] - q_start;
+    const int kv_len = p.seqused_k[r];
+    const int G = p.G;
+    const int rows = q_len * G;
+    if (rows < p.rows_lo || rows > p.rows_hi) return;
+    const int row0 = rb * 2 * kBM;
+    if (row0 >= rows) return;
+    const int row_end = min(row0 + 2 * kBM, rows);
+    const int ntiles_q = (row_end - row0 + kBM - 1) / kBM;   // 1 or 2 active Q tiles
+    const int ctx = kv_len - q_len;
+    const int i_max = (row_end - 1) / G;
+    int kv_end = kv_len;
+    if (p.causal) kv_end = min(kv_len, ctx + i_max + 1);
+    const int kv_lo = s_idx * p.split_chunk;
+    const int kv_hi = min(kv_end, kv_lo + p.split_chunk);
+    const int n_kv = kv_hi > kv_lo ? (kv_hi - kv_lo + kBN - 1) / kBN : 0;
+
+    if (n_kv == 0) {
+        // no key for any row in this segment: empty state, no TMEM taken
+        for (int pr = row0 + tid; pr < row_end; pr += blockDim.x) {
+            const int64_t tok = q_start + pr / G;
+            const int h = kvh * G + pr % G;
+            if (p.nsplit > 1) {
+                p.part_lse[(tok * p.Hq + h) * p.nsplit + s_idx] = -INFINITY;
+            } else {
+                if (p.lse) p.lse[tok * p.Hq + h] = -INFINITY;
+                uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
+                                                     (tok * p.out_stride + (int64_t)h * kD) * 2);
+                for (int c = 0; c < kD / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        *never = 0;
+        mbar_init(bar(B_Q), 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(bar(B_FULL(s)), 1);
+            mbar_init(bar(B_EMPTY(s)), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(B_SFULL(x)), 1);
+            mbar_init(bar(B_SFREE(x)), 4);
+            mbar_init(bar(B_PFULL(x)), 4);
+            mbar_init(bar(B_ODONE(x)), 1);
+        }
+        mbar_init(bar(B_DRAIN), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + kOffMisc + 8, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *taddr_slot;
+
+    if (warp == 0) {
+        // =================================================== TMA producer
+        const int R = tp.kv_rows;
+        const int pages = kBN / R;               // page loads per tile (1..4)
+        const int64_t bt_base = (int64_t)r * p.bt_stride;
+        int issued = -1;                         // last K/V load index issued
+        if (lane == 0) {
+            tma_prefetch(&qmap);
+            tma_prefetch(&kmap);
+            tma_prefetch(&vmap);
+            mbar_expect_tx(bar(B_Q), (uint32_t)ntiles_q * kQBytes);
+            const int tok0 = q_start + row0 / G;
+            const int toks_per_tile = kBM / G;
+            for (int x = 0; x < ntiles_q; ++x)
+                for (int h = 0; h < 2; ++h)
+                    tma_load_3d(sbase + kOffQ + x * kQBytes + h * kQHalf, &qmap, h * 64, kvh * G,
+                                tok0 + x * toks_per_tile, bar(B_Q));
+        }
+        for (int j = 0; j < n_kv; ++j) {
+            const int n0 = kv_lo + j * kBN;
+            // lanes < pages each resolve one page of this tile
+            int coord = -1;
+            if (lane < pages) {
+                const int tok = n0 + lane * R;
+                if (tok < kv_hi) {
+                    int blk = p.block_table[bt_base + tok / p.bs];
+                    if ((unsigned)blk >= (unsigned)p.num_blocks) {
+                        raise_error(p.err, ERR_BLOCK_ID);
+                        blk = 0;                 // never dereference an id outside the pool
+                    }
+                    coord = blk * p.bs + tok % p.bs;
+                }
+            }
+            const int nvalid = __popc(__ballot_sync(0xffffffffu, coord >= 0));
+            bool ok = true;
+            for (int kv = 0; kv < 2 && ok; ++kv) {
+                const int L = 2 * j + kv;        // load index
+                const int slot = L % kSlots;
+                if (L >= kSlots) ok = warp_wait(bar(B_EMPTY(slot)), ((L / kSlots) - 1) & 1, abort_flag);
+                if (!ok) break;
+                if (lane == 0) mbar_expect_tx(bar(B_FULL(slot)), (uint32_t)nvalid * R * kD * 2);
+                __syncwarp();
+                if (coord >= 0) {
+                    const CUtensorMap *m = kv ? &vmap : &kmap;
+                    const uint32_t dst = sbase + kOffKV + slot * kTileBytes + lane * R * 128;
+                    tma_load_3d(dst, m, 0, kvh, coord, bar(B_FULL(slot)));
+                    tma_load_3d(dst + kKVHalf, m, 64, kvh, coord, bar(B_FULL(slot)));
+                }
+                issued = L;
+            }
+            if (!ok) break;
+        }
+        // drain: every load issued has landed before the CTA exits
+        if (lane == 0) {
+            for (int L = max(0, issued - kSlots + 1); L <= issued; ++L)
+                mbar_wait(bar(B_FULL(L % kSlots)), (L / kSlots) & 1, never);
+            mbar_wait(bar(B_Q), 0, never);
+        }
+    } else if (warp == 1) {
+        // ===================================================== MMA issuer
+        if (lane == 0) {
+            const uint32_t idS = idesc_f16(BF16, kBM, kBN, false, false);
+            const uint32_t idO = idesc_f16(BF16, kBM, kD, false, true);
+            auto qk = [&](int x, int slot) {
+                const uint32_t qa = sbase + kOffQ + x * kQBytes, ka = sbase + kOffKV + slot * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    umma_ss(tmem + col_s(x), sdesc_sw128(qa + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
+                            sdesc_sw128(ka + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024), idS,
+                            kk > 0 ? 1u : 0u);
+                }
+            };
+            auto pv = [&](int x, int slot, bool first) {
+                const uint32_t pa = sbase + kOffP + x * kPBytes, va = sbase + kOffKV + slot * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    umma_ss(tmem + col_o(x), sdesc_sw128(pa + kk * 32, 16, 1024),
+                            sdesc_sw128(va + kk * 2048, kKVHalf, 1024), idO, (first && kk == 0) ? 0u : 1u);
+                }
+            };
+            bool ok = mbar_wait(bar(B_Q), 0, abort_flag);
+            for (int j = 0; j <= n_kv && ok; ++j) {
+                const int sk = (2 * j) % kSlots;              // K_j
+                const int sv = (2 * (j - 1) + 1) % kSlots;    // V_(j-1)
+                if (j < n_kv) {
+                    ok = mbar_wait(bar(B_FULL(sk)), ((2 * j) / kSlots) & 1, abort_flag);
+                    if (ok && j > 0) ok = mbar_wait(bar(B_SFREE(0)), (j - 1) & 1, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    qk(0, sk);
+                    umma_commit(bar(B_SFULL(0)));
+                    if (ntiles_q == 1) umma_commit(bar(B_EMPTY(sk)));
+                }
+                if (j > 0) {
+                    ok = mbar_wait(bar(B_FULL(sv)), ((2 * (j - 1) + 1) / kSlots) & 1, abort_flag);
+                    if (ok) ok = mbar_wait(bar(B_PFULL(0)), (j - 1) & 1, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    pv(0, sv, j == 1);
+                    umma_commit(bar(B_ODONE(0)));
+                    if (ntiles_q == 1) umma_commit(bar(B_EMPTY(sv)));
+                }
+                if (ntiles_q == 2) {
+                    if (j < n_kv) {
+                        if (j > 0) ok = mbar_wait(bar(B_SFREE(1)), (j - 1) & 1, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        qk(1, sk);
+                        umma_commit(bar(B_SFULL(1)));
+                        umma_commit(bar(B_EMPTY(sk)));
+                    }
+                    if (j > 0) {
+                        ok = mbar_wait(bar(B_PFULL(1)), (j - 1) & 1, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        pv(1, sv, j == 1);
+                        umma_commit(bar(B_ODONE(1)));
+                        umma_commit(bar(B_EMPTY(sv)));
+                    }
+                }
+            }
+        }
+    } else {
+        // ================================================ softmax warpgroups
+        const int x = (warp - 2) >> 2;              // Q tile 0 (A) or 1 (B)
+        const int quarter = warp & 3;               // TMEM lane quarter this warp may access
+        const int trow = quarter * 32 + lane;       // row within the Q tile
+        const int prow = row0 + x * kBM + trow;     // packed row within the request
+        const bool row_ok = prow < row_end;
+        const int qi = prow / G;                    // local query index
+        const int lim = p.causal ? ctx + qi : INT_MAX;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_base + col_s(x);
+        const uint32_t tO = tmem + lane_base + col_o(x);
+        uint8_t *sP = sm + kOffP + x * kPBytes;
+        const float sl2 = p.scale_log2;
+        float m_ref = -INFINITY;                    // reference maximum (log2 units)
+        float l = 0.f;
+        bool ok = x < ntiles_q;
+        // query range of this Q tile, for the tile classification
+        const int tq_lo = (row0 + x * kBM) / G;
+        const int tq_hi = (min(row0 + (x + 1) * kBM, row_end) - 1) / G + 1;
+        const int nlim = min(kv_hi - 1, lim);       // last visible key of this row in the segment
+        for (int j = 0; j < n_kv && ok; ++j) {
+            const int n0 = kv_lo + j * kBN;
+            const bool need_mask =
+                (n0 + kBN > kv_hi) || (p.causal && tile_kind(tq_lo, tq_hi, n0, n0 + kBN, ctx) != 1);
+            ok = warp_wait(bar(B_SFULL(x)), j & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[kBN];
+            {
+                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+                uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+                tmem_ld32(tS, v0);
+                tmem_ld32(tS + 32, v1);
+                tmem_wait_ld();
+            }
+            // S is in registers: the MMA warp may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_SFREE(x)));
+            float mx = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < kBN; ++e) {
+                float s = __uint_as_float(v[e]);
+                if (need_mask && n0 + e > nlim) s = -INFINITY;
+                v[e] = __float_as_uint(s);
+                mx = fmaxf(mx, s);
+            }
+            mx *= sl2;
+            // rescale only when the maximum grows past the threshold
+            const bool bump = mx > m_ref + kRescaleThreshold;
+            const bool corr = bump && m_ref != -INFINITY;
+            const float m_new = bump ? mx : m_ref;
+            const float alpha = corr ? ex2(m_ref - m_new) : 1.f;
+            const float base = (m_new == -INFINITY) ? 0.f : m_new;
+            m_ref = m_new;
+            uint32_t pk[kBN / 2];
+            float rs = 0.f;
+#pragma unroll
+            for (int e = 0; e < kBN; e += 2) {
+                const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -base));
+                const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -base));
+                rs += p0 + p1;
+                pk[e / 2] = pack2<BF16>(p0, p1);
+            }
+            l = l * alpha + rs;
+            // the previous P V must be done before P_X and O_X are touched
+            if (j > 0) {
+                ok = warp_wait(bar(B_ODONE(x)), (j - 1) & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, corr)) {
+#pragma unroll
+                for (int c = 0; c < kD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tO + c * 32, o);
+                }
+                tmem_wait_st();
+            }
+            if (x == 0 && n0 + kBN > kv_hi) {
+                // keys past the segment end: their P is exactly 0, but the V
+                // rows there may hold anything (unwritten cache rows, pages
+                // not loaded) -- zero them so 0 * V cannot produce NaN
+                const int Lv = 2 * j + 1, sv = Lv % kSlots;
+                ok = warp_wait(bar(B_FULL(sv)), (Lv / kSlots) & 1, abort_flag);
+                if (!ok) break;
+                if (trow < kBN && trow >= kv_hi - n0) {
+                    uint4 *v0 = reinterpret_cast<uint4 *>(sm + kOffKV + sv * kTileBytes + trow * 128);
+                    uint4 *v1 = reinterpret_cast<uint4 *>(sm + kOffKV + sv * kTileBytes + kKVHalf + trow * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) v0[c] = v1[c] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            // P -> shared memory, 128-byte swizzle, K-major (row = trow)
+#pragma unroll
+            for (int c = 0; c < kBN / 8; ++c) {
+                const uint4 w = make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
+                *reinterpret_cast<uint4 *>(sP + trow * 128 + ((c ^ (trow & 7)) << 4)) = w;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PFULL(x)));
+        }
+        // ---- epilogue: O / l -> out (or the split partials)
+        if (ok && x < ntiles_q) {
+            ok = warp_wait(bar(B_ODONE(x)), (n_kv - 1) & 1, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                const float inv = l > 0.f ? p.v_descale / l : 0.f;
+                const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+                const int64_t tok = q_start + qi;
+                const int h = kvh * G + prow % G;
+#pragma unroll
+                for (int c = 0; c < kD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_wait_ld();
+                    if (!row_ok) continue;
+                    if (p.nsplit == 1) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
+                                                               (tok * p.out_stride + (int64_t)h * kD + c * 32) * 2);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w;
+                            w.x = pack2<BF16>(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
+                            w.y = pack2<BF16>(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
+                            w.z = pack2<BF16>(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
+                            w.w = pack2<BF16>(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
+                            dst[q4] = w;
+                        }
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            p.part_o + ((tok * p.Hq + h) * p.nsplit + s_idx) * kD + c * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            dst[q4] = make_float4(__uint_as_float(o[q4 * 4]) * inv, __uint_as_float(o[q4 * 4 + 1]) * inv,
+                                                  __uint_as_float(o[q4 * 4 + 2]) * inv,
+                                                  __uint_as_float(o[q4 * 4 + 3]) * inv);
+                    }
+                }
+                if (row_ok) {
+                    if (p.nsplit == 1) {
+                        if (p.lse) p.lse[tok * p.Hq + h] = lse_v;
+                    } else {
+                        p.part_lse[(tok * p.Hq + h) * p.nsplit + s_idx] = lse_v;
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown: every MMA has completed before TMEM is released
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        if (*abort_flag) {
+            // a stalled pipeline: wait (bounded) for the MMAs already issued
+            if (lane == 0) {
+                umma_commit(bar(B_DRAIN));
+                mbar_wait(bar(B_DRAIN), 0, never);
+            }
+            __syncwarp();
+        }
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (tid == 0 && *abort_flag) raise_error(p.err, ERR_TIMEOUT);
+}
+
+static int gcd_int(int a, int b) {
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+bool tc_supported(int D, int q_dtype, int kv_dtype, int G) {
+    if (D != kD) return false;
+    if (!((q_dtype == DT_BF16 && kv_dtype == DT_BF16) || (q_dtype == DT_FP16 && kv_dtype == DT_FP16))) return false;
+    if (G <= 0 || G > 128 || (128 % G) != 0) return false;
+    return true;
+}
+
+int tc_rows_per_cta() { return 2 * kBM; }
+
+cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int64_t T, cudaStream_t stream) {
+    TcParams tp{};
+    tp.f = f;
+    tp.kv_rows = gcd_int(f.bs, kBN);
+    const bool fp16 = q_dtype == DT_FP16;
+    CUtensorMap qmap, kmap, vmap;
+    // Q viewed as [T][Hq][D]: box = 64 columns x G heads x (128 / G) tokens
+    if (!encode_3d_bf16(&qmap, f.q, fp16, kD, (uint64_t)f.Hq, (uint64_t)T, (uint64_t)kD * 2,
+                        (uint64_t)f.q_stride * 2, 64, (uint32_t)f.G, (uint32_t)(kBM / f.G)))
+        return cudaErrorInvalidValue;
+    // caches viewed as [num_blocks * bs][Hkv][D]: box = 64 columns x 1 head x R rows
+    const uint64_t nslots = (uint64_t)f.num_blocks * f.bs;
+    if (!encode_3d_bf16(&kmap, f.k_cache, fp16, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD * 2,
+                        (uint64_t)f.Hkv * kD * 2, 64, 1, (uint32_t)tp.kv_rows))
+        return cudaErrorInvalidValue;
+    if (!encode_3d_bf16(&vmap, f.v_cache, fp16, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD * 2,
+                        (uint64_t)f.Hkv * kD * 2, 64, 1, (uint32_t)tp.kv_rows))
+        return cudaErrorInvalidValue;
+    dim3 grid((unsigned)(f.n_row_blocks * f.nsplit), (unsigned)f.Hkv, (unsigned)f.B);
+    cudaError_t e;
+    if (fp16) {
+        e = cudaFuncSetAttribute(fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        fwd_tc_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tp, qmap, kmap, vmap);
+    } else {
+        e = cudaFuncSetAttribute(fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        fwd_tc_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tp, qmap, kmap, vmap);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace attn

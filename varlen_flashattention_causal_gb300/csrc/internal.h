@@ -11,7 +11,7 @@ namespace attn {
 enum : int { DT_BF16 = 0, DT_FP16 = 1, DT_E4M3 = 2, DT_FP32 = 3 };
 
 // error bits of the device error word
-enum : unsigned { ERR_BLOCK_ID = 1u, ERR_SLOT = 2u };
+enum : unsigned { ERR_BLOCK_ID = 1u, ERR_SLOT = 2u, ERR_TIMEOUT = 4u };
 
 // One attention launch over the requests whose packed row count
 // rows = q_len * G lies in [rows_lo, rows_hi].  Packed row p of a request
@@ -76,5 +76,10 @@ __host__ __device__ inline int tile_kind(int q_lo, int q_hi, int k_lo, int k_hi,
 
 // rows per CTA of the mma kernel for a given largest packed row count
 int mma_rows_per_cta(int max_rows);
+
+// tcgen05 kernel: whether it handles this shape, rows per CTA, launcher
+bool tc_supported(int D, int q_dtype, int kv_dtype, int G);
+int tc_rows_per_cta();
+cudaError_t launch_fwd_tc(const FwdParams &p, int q_dtype, int64_t T, cudaStream_t stream);
 
 }  // namespace attn
