@@ -233,22 +233,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idS = idesc_f16(BF16, kBM, kBN, false, false);
             const uint32_t idO = idesc_f16(BF16, kBM, kD, false, true);
+            // descriptors of every operand base, built once; a K slice or a
+            // ring slot only adds a small offset to the start-address field
+            // (addresses stay below 2^18, so the 14-bit field never carries)
+            const uint64_t dQ = sdesc_sw128(sbase + kOffQ, 16, 1024);
+            const uint64_t dK = sdesc_sw128(sbase + kOffKV, 16, 1024);
+            const uint64_t dP = sdesc_sw128(sbase + kOffP, 16, 1024);
+            const uint64_t dV = sdesc_sw128(sbase + kOffKV, kKVHalf, 1024);
             auto qk = [&](int x, int slot) {
-                const uint32_t qa = sbase + kOffQ + x * kQBytes, ka = sbase + kOffKV + slot * kTileBytes;
+                const uint64_t a0 = dQ + ((x * kQBytes) >> 4), b0 = dK + ((slot * kTileBytes) >> 4);
+                const uint32_t d = tmem + col_s(x);
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    umma_ss(tmem + col_s(x), sdesc_sw128(qa + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
-                            sdesc_sw128(ka + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024), idS,
-                            kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    umma_ss(d, a0 + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
+                            b0 + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
             };
             auto pv = [&](int x, int slot, bool first) {
-                const uint32_t pa = sbase + kOffP + x * kPBytes, va = sbase + kOffKV + slot * kTileBytes;
+                const uint64_t a0 = dP + ((x * kPBytes) >> 4), b0 = dV + ((slot * kTileBytes) >> 4);
+                const uint32_t d = tmem + col_o(x);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    umma_ss(tmem + col_o(x), sdesc_sw128(pa + kk * 32, 16, 1024),
-                            sdesc_sw128(va + kk * 2048, kKVHalf, 1024), idO, (first && kk == 0) ? 0u : 1u);
-                }
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    umma_ss(d, a0 + ((kk * 32) >> 4), b0 + ((kk * 2048) >> 4), idO, (first && kk == 0) ? 0u : 1u);
             };
             bool ok = mbar_wait(bar(B_Q), 0, abort_flag);
             for (int j = 0; j <= n_kv && ok; ++j) {
@@ -332,14 +337,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_SFREE(x)));
-            float mx = -INFINITY;
+            // masked keys: this row sees keys n0 .. n0 + nv - 1 of the tile
+            const int nv = need_mask ? max(0, min(kBN, nlim - n0 + 1)) : kBN;
+            float mx8[8];
 #pragma unroll
-            for (int e = 0; e < kBN; ++e) {
-                float s = __uint_as_float(v[e]);
-                if (need_mask && n0 + e > nlim) s = -INFINITY;
-                v[e] = __float_as_uint(s);
-                mx = fmaxf(mx, s);
+            for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+            if (nv == kBN) {
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(v[e]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) {
+                    const float s = e < nv ? __uint_as_float(v[e]) : -INFINITY;
+                    v[e] = __float_as_uint(s);
+                    mx8[e & 7] = fmaxf(mx8[e & 7], s);
+                }
             }
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             mx *= sl2;
             // rescale only when the maximum grows past the threshold
             const bool bump = mx > m_ref + kRescaleThreshold;
@@ -349,14 +364,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float base = (m_new == -INFINITY) ? 0.f : m_new;
             m_ref = m_new;
             uint32_t pk[kBN / 2];
-            float rs = 0.f;
+            float rs8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
 #pragma unroll
             for (int e = 0; e < kBN; e += 2) {
                 const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -base));
                 const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -base));
-                rs += p0 + p1;
+                rs8[(e >> 1) & 7] += p0 + p1;
                 pk[e / 2] = pack2<BF16>(p0, p1);
             }
+            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l = l * alpha + rs;
             // the previous P V must be done before P_X and O_X are touched
             if (j > 0) {
