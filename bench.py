@@ -399,16 +399,30 @@ def _device_cache(b, dev, kv_dtype=torch.bfloat16, scale=(1.0, 1.0), seed=0):
     return kc, vc
 
 
+_LAST_CLOCKS = {}
+
+
 def _time(fn, steps, warmup):
-    for _ in range(warmup):
-        fn()
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, c in evs:
-        a.record()
-        fn()
-        c.record()
-    torch.cuda.synchronize()
+    """Median and mean CUDA-event time of fn over `steps` calls; the clocks
+    seen meanwhile are left in _LAST_CLOCKS."""
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_w = time.time()
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        while time.time() - t_w < 1.0:
+            fn()
+            torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        clk.mark("start")
+        for a, c in evs:
+            a.record()
+            fn()
+            c.record()
+        torch.cuda.synchronize()
+        clk.mark("stop")
+    _LAST_CLOCKS.clear()
+    _LAST_CLOCKS.update(clk.summary())
     t = [a.elapsed_time(c) for a, c in evs]
     return statistics.median(t), statistics.mean(t)
 
@@ -500,6 +514,7 @@ def run_workload(args):
         res.update(metric="fp8-KV mixed batch ms", value=round(med, 4), unit="ms", ms_per_step=round(med, 4),
                    decode_bytes=dec, prefill_flops=fl, num_splits=ns,
                    t_star_ms=round(max(dec / hbm / 1e6, fl / tc / 1e9), 4))
+    res["clocks"] = dict(_LAST_CLOCKS)
     print(json.dumps(res))
 
 

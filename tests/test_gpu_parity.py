@@ -411,3 +411,17 @@ def test_workload4_fp8_mixed_full_sampled():
     ro, rl = ref_attn(b, ck, cv, rows=rows)
     check(out, lse, ro, rl, TOL_FP8, rows=rows)
     assert_no_device_error()
+
+
+def test_short_segments_repeated_are_stable():
+    """Many tensor-core CTAs with only two K/V tiles each (64 queries x 4
+    heads against 4096 keys, 32 segments), called repeatedly: every call
+    must match the oracle -- a pipeline that reads O before its last P V
+    lands would fail intermittently here."""
+    b = W.make_batch([64], [4096], 32, 8, 128, 64, seed=15, causal=False)
+    kc, vc = gpu_cache(b)
+    ro, rl = ref_attn(b, *cpu_cache(b))
+    for it in range(12):
+        out, lse = gpu_attn(b, kc, vc, num_splits=(32, 0, 16)[it % 3])
+        check(out, lse, ro, rl, TOL)
+    assert_no_device_error()

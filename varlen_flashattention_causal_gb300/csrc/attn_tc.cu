@@ -11,15 +11,25 @@
 //   warp 0      TMA producer: Q once, then K_j and V_j tiles of 64 keys,
 //               each gathered page by page through the block table ("vLLM 中
 //               Attention Kernel 如何并行处理多个请求", sec. 11) into a ring of
-//               eight 16 KB shared-memory slots (four tiles of look-ahead)
-//   warp 1      MMA issuer (one thread) and TMEM owner.  Per K/V tile j it
-//               issues S_A(j) = Q_A K_j^T, O_A += P_A(j-1) V_(j-1),
-//               S_B(j) = Q_B K_j^T, O_B += P_B(j-1) V_(j-1): between S_X(j)
-//               landing and P_X(j) being needed there are four MMAs for the
-//               softmax of tile X to hide behind
+//               ten 16 KB shared-memory slots (five tiles of look-ahead)
+//   warp 1      MMA issuer of Q tile A (one thread) and TMEM owner
+//   warp 10     MMA issuer of Q tile B (one thread)
+//               Per K/V tile j each issuer X runs S_X(j) = Q_X K_j^T, then
+//               O_X += P_X(j-1) V_(j-1).  Two issuers keep the tensor pipe fed:
+//               a single thread spends tens of cycles per MMA, commit and
+//               barrier wait, and with one issuer those stalls show up as
+//               idle tensor cycles.  The two chains touch disjoint TMEM
+//               columns; a K/V slot is released when both have consumed it.
 //   warps 2-5   softmax warpgroup of Q tile A, one thread per row
 //   warps 6-9   softmax warpgroup of Q tile B
-// TMEM columns: S_A [0,64), S_B [64,128), O_A [128,256), O_B [256,384).
+// TMEM columns: S_A double buffer [0,64) [64,128), S_B [128,192) [192,256),
+// O_A [256,384), O_B [384,512).  P_X(j) (bf16/fp16, two per column) is
+// written over the first 32 columns of the S buffer it was computed from and
+// is the TMEM "A" operand of O_X += P_X V; only K, V (and Q) are read from
+// shared memory by the tensor core, which keeps shared-memory bandwidth
+// below the MMA rate.  S_X(j+2) reuses the buffer of P_X(j) only after
+// O_X += P_X(j) V has been issued, and tcgen05 MMAs of one thread run in
+// order.
 //
 // Softmax (sec. 7): each thread reads its row of S from TMEM, masks it in
 // registers from local positions with the bottom-right alignment of
@@ -27,8 +37,7 @@
 // maximum m and sum l.  O lives in TMEM and is rescaled only when a row's
 // maximum grows by more than 2^8 (in exp2 units); otherwise P is formed
 // against the stale maximum, which keeps every exponential <= 256 and is
-// exact because l and O share the same reference.  P (bf16/fp16) goes to
-// shared memory in the 128-byte-swizzled K-major layout the MMA reads.
+// exact because l and O share the same reference.
 #include "common.cuh"
 #include "sm100.cuh"
 #include "tma_host.h"
@@ -42,29 +51,27 @@ namespace {
 constexpr int kBM = 128;                               // rows per Q tile
 constexpr int kBN = 64;                                // keys per K/V tile
 constexpr int kD = 128;                                // head size handled here
-constexpr int kSlots = 8;                              // K/V ring slots
-constexpr int kThreads = 320;
+constexpr int kSlots = 10;                             // K/V ring slots
+constexpr int kThreads = 352;
 constexpr uint32_t kQBytes = kBM * kD * 2;             // one Q tile, 32 KB
 constexpr uint32_t kQHalf = kBM * 128;                 // 64 columns of a Q tile
 constexpr uint32_t kTileBytes = kBN * kD * 2;          // one K or V tile, 16 KB
 constexpr uint32_t kKVHalf = kBN * 128;                // 64 columns of a K/V tile
-constexpr uint32_t kPBytes = kBM * kBN * 2;            // one P tile, 16 KB
 constexpr float kRescaleThreshold = 8.0f;              // log2 units
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr uint32_t kOffQ = 0;                          // Q_A, Q_B
-constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;        // P_A, P_B
-constexpr uint32_t kOffKV = kOffP + 2 * kPBytes;       // ring slots
+constexpr uint32_t kOffKV = kOffQ + 2 * kQBytes;       // ring slots
 constexpr uint32_t kOffBar = kOffKV + kSlots * kTileBytes;
-constexpr int kNumBars = 1 + 2 * kSlots + 4 * 2 + 1;
-constexpr uint32_t kOffMisc = kOffBar + 8 * 32;
+constexpr int kNumBars = 1 + 2 * kSlots + 4 + 4 + 4 + 2;
+constexpr uint32_t kOffMisc = kOffBar + 8 * 40;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
-static_assert(kNumBars <= 32, "barrier area");
+static_assert(kNumBars <= 40, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-// TMEM column offsets of S_x and O_x
-__device__ __forceinline__ uint32_t col_s(int x) { return (uint32_t)x * 64u; }
-__device__ __forceinline__ uint32_t col_o(int x) { return 128u + (uint32_t)x * 128u; }
+// TMEM column offsets of S_x buffer b and O_x
+__device__ __forceinline__ uint32_t col_s(int x, int b) { return (uint32_t)x * 128u + (uint32_t)b * 64u; }
+__device__ __forceinline__ uint32_t col_o(int x) { return 256u + (uint32_t)x * 128u; }
 
 }  // namespace
 
@@ -94,11 +101,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int B_Q = 0;
     auto B_FULL = [](int s) { return 1 + s; };
     auto B_EMPTY = [](int s) { return 1 + kSlots + s; };
-    auto B_SFULL = [](int x) { return 1 + 2 * kSlots + x; };
-    auto B_SFREE = [](int x) { return 3 + 2 * kSlots + x; };
-    auto B_PFULL = [](int x) { return 5 + 2 * kSlots + x; };
-    auto B_ODONE = [](int x) { return 7 + 2 * kSlots + x; };
-    constexpr int B_DRAIN = 9 + 2 * kSlots;
+    // S_X, P_X and "O_X += P_X V done" barriers exist per TMEM buffer
+    // b = j & 1.  A parity wait is only sound if the barrier is neither two
+    // phases ahead of nor two phases behind the phase waited for; per buffer,
+    // the next phase always needs work the waiter has not released yet, and
+    // the previous one is implied by S_X(j) having landed (one issuer's MMAs
+    // complete in order).
+    auto B_SFULL = [](int x, int b) { return 1 + 2 * kSlots + 2 * x + b; };
+    auto B_PFULL = [](int x, int b) { return 5 + 2 * kSlots + 2 * x + b; };
+    auto B_ODONE = [](int x, int b) { return 9 + 2 * kSlots + 2 * x + b; };
+    auto B_DRAIN = [](int x) { return 13 + 2 * kSlots + x; };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc);
     uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc + 8);
     volatile int *never = reinterpret_cast<volatile int *>(sm + kOffMisc + 16);
@@ -150,15 +162,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(B_Q), 1);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(bar(B_FULL(s)), 1);
-            mbar_init(bar(B_EMPTY(s)), 1);
+            mbar_init(bar(B_EMPTY(s)), (uint32_t)ntiles_q);   // one release per active Q tile
         }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(bar(B_SFULL(x)), 1);
-            mbar_init(bar(B_SFREE(x)), 4);
-            mbar_init(bar(B_PFULL(x)), 4);
-            mbar_init(bar(B_ODONE(x)), 1);
+            mbar_init(bar(B_SFULL(x, 0)), 1);
+            mbar_init(bar(B_SFULL(x, 1)), 1);
+            mbar_init(bar(B_PFULL(x, 0)), 4);
+            mbar_init(bar(B_PFULL(x, 1)), 4);
+            mbar_init(bar(B_ODONE(x, 0)), 1);
+            mbar_init(bar(B_ODONE(x, 1)), 1);
         }
-        mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_DRAIN(0)), 1);
+        mbar_init(bar(B_DRAIN(1)), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -188,22 +203,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(sbase + kOffQ + x * kQBytes + h * kQHalf, &qmap, h * 64, kvh * G,
                                 tok0 + x * toks_per_tile, bar(B_Q));
         }
-        for (int j = 0; j < n_kv; ++j) {
-            const int n0 = kv_lo + j * kBN;
-            // lanes < pages each resolve one page of this tile
-            int coord = -1;
-            if (lane < pages) {
-                const int tok = n0 + lane * R;
-                if (tok < kv_hi) {
-                    int blk = p.block_table[bt_base + tok / p.bs];
-                    if ((unsigned)blk >= (unsigned)p.num_blocks) {
-                        raise_error(p.err, ERR_BLOCK_ID);
-                        blk = 0;                 // never dereference an id outside the pool
-                    }
-                    coord = blk * p.bs + tok % p.bs;
-                }
+        // Page coordinates are read from the block table 32 pages at a time
+        // (one per lane) and the next batch is requested a whole batch ahead,
+        // so the table's load latency never sits between two tiles.
+        const int total_pages = n_kv * pages;
+        auto page_coord = [&](int g) -> int {       // row of page g in the cache, -1 if absent
+            if (g >= total_pages) return -1;
+            const int tok = kv_lo + g * R;
+            if (tok >= kv_hi) return -1;
+            int blk = p.block_table[bt_base + tok / p.bs];
+            if ((unsigned)blk >= (unsigned)p.num_blocks) {
+                raise_error(p.err, ERR_BLOCK_ID);
+                blk = 0;                             // never dereference an id outside the pool
             }
-            const int nvalid = __popc(__ballot_sync(0xffffffffu, coord >= 0));
+            return blk * p.bs + tok % p.bs;
+        };
+        int batch = 0;                               // pages [batch, batch + 32) are in cur
+        int cur = page_coord(lane);
+        int nxt = page_coord(32 + lane);
+        for (int j = 0; j < n_kv; ++j) {
+            const int g0 = j * pages;
+            if (g0 >= batch + 32) {
+                batch += 32;
+                cur = nxt;
+                nxt = page_coord(batch + 32 + lane);
+            }
+            // lane pp < pages takes page g0 + pp of this tile (a tile never straddles a batch: 32 % pages == 0)
+            const int coord = __shfl_sync(0xffffffffu, cur, (g0 - batch + (lane < pages ? lane : 0)) & 31);
+            const int mine = lane < pages ? coord : -1;
+            const int nvalid = __popc(__ballot_sync(0xffffffffu, mine >= 0));
             bool ok = true;
             for (int kv = 0; kv < 2 && ok; ++kv) {
                 const int L = 2 * j + kv;        // load index
@@ -212,11 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 if (lane == 0) mbar_expect_tx(bar(B_FULL(slot)), (uint32_t)nvalid * R * kD * 2);
                 __syncwarp();
-                if (coord >= 0) {
+                if (mine >= 0) {
                     const CUtensorMap *m = kv ? &vmap : &kmap;
                     const uint32_t dst = sbase + kOffKV + slot * kTileBytes + lane * R * 128;
-                    tma_load_3d(dst, m, 0, kvh, coord, bar(B_FULL(slot)));
-                    tma_load_3d(dst + kKVHalf, m, 64, kvh, coord, bar(B_FULL(slot)));
+                    tma_load_3d(dst, m, 0, kvh, mine, bar(B_FULL(slot)));
+                    tma_load_3d(dst + kKVHalf, m, 64, kvh, mine, bar(B_FULL(slot)));
                 }
                 issued = L;
             }
@@ -228,73 +256,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(bar(B_FULL(L % kSlots)), (L / kSlots) & 1, never);
             mbar_wait(bar(B_Q), 0, never);
         }
-    } else if (warp == 1) {
-        // ===================================================== MMA issuer
-        if (lane == 0) {
+    } else if (warp == 1 || warp == 10) {
+        // ================================================ MMA issuers (tile x)
+        const int x = warp == 1 ? 0 : 1;
+        if (lane == 0 && x < ntiles_q) {
             const uint32_t idS = idesc_f16(BF16, kBM, kBN, false, false);
             const uint32_t idO = idesc_f16(BF16, kBM, kD, false, true);
             // descriptors of every operand base, built once; a K slice or a
             // ring slot only adds a small offset to the start-address field
             // (addresses stay below 2^18, so the 14-bit field never carries)
-            const uint64_t dQ = sdesc_sw128(sbase + kOffQ, 16, 1024);
+            const uint64_t dQ = sdesc_sw128(sbase + kOffQ + x * kQBytes, 16, 1024);
             const uint64_t dK = sdesc_sw128(sbase + kOffKV, 16, 1024);
-            const uint64_t dP = sdesc_sw128(sbase + kOffP, 16, 1024);
             const uint64_t dV = sdesc_sw128(sbase + kOffKV, kKVHalf, 1024);
-            auto qk = [&](int x, int slot) {
-                const uint64_t a0 = dQ + ((x * kQBytes) >> 4), b0 = dK + ((slot * kTileBytes) >> 4);
-                const uint32_t d = tmem + col_s(x);
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                    umma_ss(d, a0 + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
-                            b0 + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
-            };
-            auto pv = [&](int x, int slot, bool first) {
-                const uint64_t a0 = dP + ((x * kPBytes) >> 4), b0 = dV + ((slot * kTileBytes) >> 4);
-                const uint32_t d = tmem + col_o(x);
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    umma_ss(d, a0 + ((kk * 32) >> 4), b0 + ((kk * 2048) >> 4), idO, (first && kk == 0) ? 0u : 1u);
-            };
+            const uint32_t tOx = tmem + col_o(x);
             bool ok = mbar_wait(bar(B_Q), 0, abort_flag);
             for (int j = 0; j <= n_kv && ok; ++j) {
-                const int sk = (2 * j) % kSlots;              // K_j
-                const int sv = (2 * (j - 1) + 1) % kSlots;    // V_(j-1)
+                const int sk = (2 * j) % kSlots;                  // K_j
+                const int sv = (2 * j + kSlots - 1) % kSlots;     // V_(j-1)
                 if (j < n_kv) {
                     ok = mbar_wait(bar(B_FULL(sk)), ((2 * j) / kSlots) & 1, abort_flag);
-                    if (ok && j > 0) ok = mbar_wait(bar(B_SFREE(0)), (j - 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    qk(0, sk);
-                    umma_commit(bar(B_SFULL(0)));
-                    if (ntiles_q == 1) umma_commit(bar(B_EMPTY(sk)));
+                    const uint64_t b0 = dK + ((sk * kTileBytes) >> 4);
+                    const uint32_t d = tmem + col_s(x, j & 1);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk)
+                        umma_ss(d, dQ + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
+                                b0 + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
+                    umma_commit(bar(B_SFULL(x, j & 1)));
+                    umma_commit(bar(B_EMPTY(sk)));
                 }
                 if (j > 0) {
-                    ok = mbar_wait(bar(B_FULL(sv)), ((2 * (j - 1) + 1) / kSlots) & 1, abort_flag);
-                    if (ok) ok = mbar_wait(bar(B_PFULL(0)), (j - 1) & 1, abort_flag);
+                    ok = mbar_wait(bar(B_FULL(sv)), ((2 * j - 1) / kSlots) & 1, abort_flag);
+                    if (ok) ok = mbar_wait(bar(B_PFULL(x, (j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    pv(0, sv, j == 1);
-                    umma_commit(bar(B_ODONE(0)));
-                    if (ntiles_q == 1) umma_commit(bar(B_EMPTY(sv)));
+                    // A = P_X from TMEM (8 columns per 16 keys), B = V from shared memory
+                    const uint64_t b0 = dV + ((sv * kTileBytes) >> 4);
+                    const uint32_t a = tmem + col_s(x, (j - 1) & 1);
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        umma_ts(tOx, a + kk * 8, b0 + ((kk * 2048) >> 4), idO, (j == 1 && kk == 0) ? 0u : 1u);
+                    umma_commit(bar(B_ODONE(x, (j - 1) & 1)));
+                    umma_commit(bar(B_EMPTY(sv)));
                 }
-                if (ntiles_q == 2) {
-                    if (j < n_kv) {
-                        if (j > 0) ok = mbar_wait(bar(B_SFREE(1)), (j - 1) & 1, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                        qk(1, sk);
-                        umma_commit(bar(B_SFULL(1)));
-                        umma_commit(bar(B_EMPTY(sk)));
-                    }
-                    if (j > 0) {
-                        ok = mbar_wait(bar(B_PFULL(1)), (j - 1) & 1, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                        pv(1, sv, j == 1);
-                        umma_commit(bar(B_ODONE(1)));
-                        umma_commit(bar(B_EMPTY(sv)));
-                    }
-                }
+            }
+            if (*abort_flag) {
+                // a stalled pipeline: wait (bounded) for the MMAs this thread issued
+                umma_commit(bar(B_DRAIN(x)));
+                mbar_wait(bar(B_DRAIN(x)), 0, never);
             }
         }
     } else {
@@ -307,9 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qi = prow / G;                    // local query index
         const int lim = p.causal ? ctx + qi : INT_MAX;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_base + col_s(x);
         const uint32_t tO = tmem + lane_base + col_o(x);
-        uint8_t *sP = sm + kOffP + x * kPBytes;
         const float sl2 = p.scale_log2;
         float m_ref = -INFINITY;                    // reference maximum (log2 units)
         float l = 0.f;
@@ -320,9 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nlim = min(kv_hi - 1, lim);       // last visible key of this row in the segment
         for (int j = 0; j < n_kv && ok; ++j) {
             const int n0 = kv_lo + j * kBN;
+            const int b = j & 1;
+            const uint32_t tS = tmem + lane_base + col_s(x, b);
             const bool need_mask =
                 (n0 + kBN > kv_hi) || (p.causal && tile_kind(tq_lo, tq_hi, n0, n0 + kBN, ctx) != 1);
-            ok = warp_wait(bar(B_SFULL(x)), j & 1, abort_flag);
+            ok = warp_wait(bar(B_SFULL(x, b)), (j >> 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             uint32_t v[kBN];
@@ -333,10 +343,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tS + 32, v1);
                 tmem_wait_ld();
             }
-            // S is in registers: the MMA warp may overwrite it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_SFREE(x)));
             // masked keys: this row sees keys n0 .. n0 + nv - 1 of the tile
             const int nv = need_mask ? max(0, min(kBN, nlim - n0 + 1)) : kBN;
             float mx8[8];
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float alpha = corr ? ex2(m_ref - m_new) : 1.f;
             const float base = (m_new == -INFINITY) ? 0.f : m_new;
             m_ref = m_new;
-            uint32_t pk[kBN / 2];
+            uint32_t pk[32];
             float rs8[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
@@ -376,13 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l = l * alpha + rs;
-            // the previous P V must be done before P_X and O_X are touched
-            if (j > 0) {
-                ok = warp_wait(bar(B_ODONE(x)), (j - 1) & 1, abort_flag);
+            if (__any_sync(0xffffffffu, corr)) {
+                // O_X must hold P_X(j-1) V before it is rescaled
+                ok = warp_wait(bar(B_ODONE(x, (j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-            }
-            if (__any_sync(0xffffffffu, corr)) {
 #pragma unroll
                 for (int c = 0; c < kD / 32; ++c) {
                     uint32_t o[32];
@@ -392,12 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                     tmem_st32(tO + c * 32, o);
                 }
-                tmem_wait_st();
             }
-            if (x == 0 && n0 + kBN > kv_hi) {
+            if (n0 + kBN > kv_hi) {
                 // keys past the segment end: their P is exactly 0, but the V
                 // rows there may hold anything (unwritten cache rows, pages
-                // not loaded) -- zero them so 0 * V cannot produce NaN
+                // not loaded) -- zero them so 0 * V cannot produce NaN.  Both
+                // warpgroups write the same zeros, each before publishing its
+                // own P, because either issuer may read the tile first.
                 const int Lv = 2 * j + 1, sv = Lv % kSlots;
                 ok = warp_wait(bar(B_FULL(sv)), (Lv / kSlots) & 1, abort_flag);
                 if (!ok) break;
@@ -407,21 +412,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 8; ++c) v0[c] = v1[c] = make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();
             }
-            // P -> shared memory, 128-byte swizzle, K-major (row = trow)
-#pragma unroll
-            for (int c = 0; c < kBN / 8; ++c) {
-                const uint4 w = make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
-                *reinterpret_cast<uint4 *>(sP + trow * 128 + ((c ^ (trow & 7)) << 4)) = w;
-            }
-            fence_proxy_async_smem();
+            // P -> TMEM over the S buffer it came from (columns 0..31)
+            tmem_st32(tS, pk);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PFULL(x)));
+            if (lane == 0) mbar_arrive(bar(B_PFULL(x, b)));
         }
         // ---- epilogue: O / l -> out (or the split partials)
         if (ok && x < ntiles_q) {
-            ok = warp_wait(bar(B_ODONE(x)), (n_kv - 1) & 1, abort_flag);
+            // O_X += P_X(n-1) V done implies every earlier P V of this tile is done
+            ok = warp_wait(bar(B_ODONE(x, (n_kv - 1) & 1)), ((n_kv - 1) >> 1) & 1, abort_flag);
             if (ok) {
                 tc_fence_after();
                 const float inv = l > 0.f ? p.v_descale / l : 0.f;
@@ -471,14 +474,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        if (*abort_flag) {
-            // a stalled pipeline: wait (bounded) for the MMAs already issued
-            if (lane == 0) {
-                umma_commit(bar(B_DRAIN));
-                mbar_wait(bar(B_DRAIN), 0, never);
-            }
-            __syncwarp();
-        }
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
