@@ -486,9 +486,9 @@ def run_workload(args):
 
         def fn():
             va.attn_varlen_prefill(q, kc, vc, pre_o, cu0, su0, bt[:1], T, P, b.softmax_scale, causal=False,
-                                   lse_out=pre_l, num_splits=ns1, workspace=w1)
+                                   lse_out=pre_l, num_splits=0, workspace=w1)
             va.attn_varlen_prefill(q, kc, vc, suf_o, cu, su, bt[:, nblk:], 1, b.max_seqlen_k - P,
-                                   b.softmax_scale, causal=True, lse_out=suf_l, num_splits=ns2, workspace=w2)
+                                   b.softmax_scale, causal=True, lse_out=suf_l, num_splits=0, workspace=w2)
             va.attn_merge_states(out, lse, pre_o, pre_l, suf_o, suf_l)
 
         med, mean = _time(fn, args.steps, args.warmup)
@@ -507,7 +507,7 @@ def run_workload(args):
         wsp = torch.empty(max(1, va.attn_workspace_size(b.T, b.Hq, b.D, ns)), dtype=torch.uint8, device=dev)
         fn = lambda: va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt, b.max_seqlen_q, b.max_seqlen_k,
                                             b.softmax_scale, causal=True, k_descale=ks, v_descale=vs,
-                                            num_splits=ns, workspace=wsp)
+                                            num_splits=0, workspace=wsp)
         med, mean = _time(fn, args.steps, args.warmup)
         dec = sum(b.kv_lens[:128]) * b.Hkv * b.D * 2
         fl = prefill_flops(b)

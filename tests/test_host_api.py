@@ -162,8 +162,10 @@ def test_workspace_and_split_rules(lib):
     # decode with few (request, KV head) pairs and long contexts splits;
     # big prefill batches do not
     assert va.attn_num_splits(4, 1, 131072, 64, 8, 152) > 8
-    assert va.attn_num_splits(16, 8192, 12288, 32, 8, 152) == 1
+    assert va.attn_num_splits(1024, 1, 512, 32, 8, 152) == 1   # enough CTAs, short keys
     assert va.attn_num_splits(1, 1, 100, 32, 8, 152) == 1     # too short to split
+    # one long request among many short ones is still cut into segments
+    assert va.attn_num_splits(1024, 1, 16384, 32, 8, 152) >= 8
     for B, L in ((64, 4096), (4, 32768), (128, 16384), (1, 2048)):
         s = va.attn_num_splits(B, 1, L, 32, 8, 152)
         assert 1 <= s <= 256 and (L // 64) >= s or s == 1

@@ -141,16 +141,17 @@ def attn_varlen_prefill(q, k_cache, v_cache, out, cu_seqlens_q, seqused_k, block
     _i32(seqused_k, "seqused_k")
     if block_table.dtype != torch.int32 or block_table.stride(-1) != 1:
         raise TypeError("block_table must be int32 with unit column stride")
-    ns = num_splits
-    if ns == 0 and workspace is None:
-        ns = attn_num_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, _sms(q.device))
+    # the workspace is sized for the largest split count the library may
+    # choose; with num_splits = 0 it picks a count per request class itself
+    ns = num_splits if num_splits > 0 else attn_num_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv,
+                                                           _sms(q.device))
     ws, ws_bytes = _workspace(T, Hq, D, ns, q.device, workspace)
     st = lib.attn_varlen_prefill(
         _p(q), q.stride(0), _p(k_cache), _p(v_cache), _p(out), out.stride(0), _p(lse_out),
         _p(cu_seqlens_q), _p(seqused_k), _p(block_table), block_table.stride(0),
         B, T, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, bs, nb,
         _dt(q), _dt(k_cache), float(softmax_scale), int(bool(causal)),
-        float(k_descale), float(v_descale), int(ns), _p(ws), ws_bytes, _stream(stream))
+        float(k_descale), float(v_descale), int(num_splits), _p(ws), ws_bytes, _stream(stream))
     _check("attn_varlen_prefill", st)
     return out
 
@@ -165,14 +166,12 @@ def attn_paged_decode(q, k_cache, v_cache, out, seq_lens, block_table, max_seq_l
     _i32(seq_lens, "seq_lens")
     if block_table.dtype != torch.int32 or block_table.stride(-1) != 1:
         raise TypeError("block_table must be int32 with unit column stride")
-    ns = num_splits
-    if ns == 0 and workspace is None:
-        ns = attn_num_splits(B, 1, max_seq_len, Hq, Hkv, _sms(q.device))
+    ns = num_splits if num_splits > 0 else attn_num_splits(B, 1, max_seq_len, Hq, Hkv, _sms(q.device))
     ws, ws_bytes = _workspace(B, Hq, D, ns, q.device, workspace)
     st = lib.attn_paged_decode(
         _p(q), _p(k_cache), _p(v_cache), _p(out), _p(lse_out), _p(seq_lens), _p(block_table),
         block_table.stride(0), B, int(max_seq_len), Hq, Hkv, D, bs, nb, _dt(q), _dt(k_cache),
-        float(softmax_scale), float(k_descale), float(v_descale), int(ns), _p(ws), ws_bytes,
+        float(softmax_scale), float(k_descale), float(v_descale), int(num_splits), _p(ws), ws_bytes,
         _stream(stream))
     _check("attn_paged_decode", st)
     return out

@@ -62,42 +62,50 @@ size_t part_o_bytes(int T, int Hq, int D, int ns) { return align256((size_t)T * 
 // kernel; larger requests run on the tcgen05 kernel when it supports the shape
 constexpr int kSmallRows = 64;
 
-// the automatic split rule: without splitting, `base` CTAs run; when that
-// is too few to fill the GPU several times over, cut each request's keys
-// into segments of at least two K/V tiles
-int auto_splits(long long base, int max_seqlen_k, long long target) {
+// Split rule.  `base` CTAs run without splitting; `target` is the CTA count
+// that fills every SM twice.  Too few CTAs: cut each request's keys into
+// more segments, each at least `min_tiles` K/V tiles.  With `len_tiles` > 0
+// segments are also capped at that many tiles, so one long request in a
+// batch of short ones does not become the critical path.
+int split_rule(long long base, int max_seqlen_k, long long target, int min_tiles, int len_tiles) {
     if (base <= 0 || max_seqlen_k <= 0) return 1;
-    if (base >= target) return 1;
     const int tiles = (max_seqlen_k + kTileN - 1) / kTileN;
-    long long s = (2 * target + base - 1) / base;
-    s = std::min<long long>(s, tiles / 2);
+    long long s = 1;
+    if (base < target) s = (2 * target + base - 1) / base;
+    if (len_tiles > 0) s = std::max<long long>(s, (tiles + len_tiles - 1) / len_tiles);
+    s = std::min<long long>(s, std::max(1, tiles / min_tiles));
     s = std::min<long long>(s, kMaxSplits);
     return (int)std::max<long long>(s, 1);
 }
 
 struct Plan {
-    bool tc;              // rows-heavy requests go to the tcgen05 kernel
+    bool small, big;      // launch the mma.sync (rows <= small_rows_hi) / tcgen05 kernel
     int rpc;              // rows per CTA of the mma kernel
     int small_rows_hi;    // largest packed row count the mma kernel takes
-    long long base;       // CTAs of the dominant kernel without splitting
-    long long target;
+    int ns_small, ns_big; // segments per class (automatic choice)
 };
 
-Plan make_plan(int B, int max_q, int Hq, int Hkv, int D, int q_dtype, int kv_dtype, int sms) {
+// uniform: every request has exactly max_q query tokens (so all requests
+// fall in one class); only host scalars are used, nothing is read back
+Plan make_plan(int B, int max_q, int max_k, bool uniform, int Hq, int Hkv, int D, int q_dtype, int kv_dtype,
+               int sms) {
     Plan pl{};
     const int G = Hq / Hkv;
     const int max_rows = std::max(1, max_q) * G;
-    pl.tc = tc_supported(D, q_dtype, kv_dtype, G) && max_rows > kSmallRows;
-    pl.small_rows_hi = pl.tc ? kSmallRows : INT32_MAX;
-    pl.rpc = mma_rows_per_cta(std::min(max_rows, pl.tc ? kSmallRows : max_rows));
-    if (pl.tc) {
+    const bool tc = tc_supported(D, q_dtype, kv_dtype, G) && max_rows > kSmallRows;
+    pl.big = tc;
+    pl.small = !tc || !uniform;
+    pl.small_rows_hi = tc ? kSmallRows : INT32_MAX;
+    pl.rpc = mma_rows_per_cta(std::min(max_rows, tc ? kSmallRows : max_rows));
+    pl.ns_small = pl.ns_big = 1;
+    if (pl.small) {
+        const long long rb = (std::min(max_rows, pl.small_rows_hi) + pl.rpc - 1) / pl.rpc;
+        // decode-like rows: also bound the keys per segment (32 tiles)
+        pl.ns_small = split_rule((long long)B * Hkv * rb, max_k, 4LL * sms, 2, rb == 1 ? 32 : 0);
+    }
+    if (pl.big) {
         const long long rb = (max_rows + tc_rows_per_cta() - 1) / tc_rows_per_cta();
-        pl.base = (long long)B * Hkv * rb;
-        pl.target = 2LL * sms;       // one resident CTA per SM, two waves
-    } else {
-        const long long rb = (max_rows + pl.rpc - 1) / pl.rpc;
-        pl.base = (long long)B * Hkv * rb;
-        pl.target = 4LL * sms;       // two resident CTAs per SM, two waves
+        pl.ns_big = split_rule((long long)B * Hkv * rb, max_k, 2LL * sms, 4, 0);
     }
     return pl;
 }
@@ -153,21 +161,23 @@ attn_status run_fwd(const FwdArgs &a) {
     if (st != ATTN_OK) return st;
 
     const int G = a.Hq / a.Hkv;
-    const Plan pl = make_plan(a.B, a.max_q, a.Hq, a.Hkv, a.D, a.q_dtype, a.kv_dtype, dev->sms);
-    int ns = a.num_splits;
-    const size_t per_split = (size_t)a.T * a.Hq * (a.D + 1) * sizeof(float) + 512;
-    if (ns == 0) {
-        ns = auto_splits(pl.base, a.max_k, pl.target);
-        if (ns > 1) {
-            const size_t fit = a.ws ? a.ws_bytes / per_split : 0;
-            ns = (int)std::min<size_t>((size_t)ns, fit);
-            if (ns < 2) ns = 1;
-        }
+    const bool uniform = (long long)a.T == (long long)a.B * a.max_q;
+    const Plan pl = make_plan(a.B, a.max_q, a.max_k, uniform, a.Hq, a.Hkv, a.D, a.q_dtype, a.kv_dtype, dev->sms);
+    int ns_s = pl.small ? pl.ns_small : 1, ns_b = pl.big ? pl.ns_big : 1;
+    if (a.num_splits > 0) {
+        ns_s = pl.small ? std::min(a.num_splits, kMaxSplits) : 1;
+        ns_b = pl.big ? std::min(a.num_splits, kMaxSplits) : 1;
+    } else {
+        // automatic: cap to what the workspace holds
+        const size_t per_split = (size_t)a.T * a.Hq * (a.D + 1) * sizeof(float) + 512;
+        const size_t fit = a.ws ? a.ws_bytes / per_split : 0;
+        if ((size_t)ns_s > fit) ns_s = fit >= 2 ? (int)fit : 1;
+        if ((size_t)ns_b > fit) ns_b = fit >= 2 ? (int)fit : 1;
     }
-    ns = std::min(ns, kMaxSplits);
-    if (ns > 1) {
+    const int stride = std::max(ns_s, ns_b);
+    if (stride > 1) {
         if (!a.ws) return ATTN_ERR_WORKSPACE;
-        if (a.ws_bytes < attn_workspace_size(a.T, a.Hq, a.D, ns)) return ATTN_ERR_WORKSPACE;
+        if (a.ws_bytes < attn_workspace_size(a.T, a.Hq, a.D, stride)) return ATTN_ERR_WORKSPACE;
         if (!aligned16(a.ws)) return ATTN_ERR_ALIGN;
     }
 
@@ -193,47 +203,60 @@ attn_status run_fwd(const FwdArgs &a) {
     p.scale_log2 = a.scale * a.k_descale * 1.4426950408889634f;
     p.v_descale = a.v_descale;
     p.err = dev->err;
-    p.nsplit = ns;
-    if (ns > 1) {
-        // every segment spans a whole number of K/V tiles
-        const int per = (a.max_k + ns - 1) / ns;
-        p.split_chunk = ((per + kTileN - 1) / kTileN) * kTileN;
+    p.part_stride = stride;
+    if (stride > 1) {
         p.part_o = static_cast<float *>(a.ws);
-        p.part_lse = reinterpret_cast<float *>(static_cast<char *>(a.ws) + part_o_bytes(a.T, a.Hq, a.D, ns));
-    } else {
-        p.split_chunk = 1 << 30;
+        p.part_lse = reinterpret_cast<float *>(static_cast<char *>(a.ws) + part_o_bytes(a.T, a.Hq, a.D, stride));
     }
+    // every segment spans a whole number of K/V tiles
+    auto chunk_for = [&](int ns) {
+        if (ns <= 1) return 1 << 30;
+        const int per = (a.max_k + ns - 1) / ns;
+        return ((per + kTileN - 1) / kTileN) * kTileN;
+    };
 
     const int max_rows = std::max(1, a.max_q) * G;
-    // rows-light requests: mma.sync kernel
-    p.rows_lo = 0;
-    p.rows_hi = pl.small_rows_hi;
-    p.n_row_blocks = (std::min(max_rows, pl.small_rows_hi) + pl.rpc - 1) / pl.rpc;
-    if ((long long)p.n_row_blocks * ns > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-    st = check_cuda(launch_fwd_mma(p, a.D, a.q_dtype, a.kv_dtype, pl.rpc, a.stream));
-    if (st != ATTN_OK) return st;
-    // rows-heavy requests: tcgen05 kernel
-    if (pl.tc) {
+    if (pl.small) {
+        // rows-light requests: mma.sync kernel
+        FwdParams m = p;
+        m.nsplit = ns_s;
+        m.split_chunk = chunk_for(ns_s);
+        m.rows_lo = 0;
+        m.rows_hi = pl.small_rows_hi;
+        m.n_row_blocks = (std::min(max_rows, pl.small_rows_hi) + pl.rpc - 1) / pl.rpc;
+        if ((long long)m.n_row_blocks * ns_s > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+        st = check_cuda(launch_fwd_mma(m, a.D, a.q_dtype, a.kv_dtype, pl.rpc, a.stream));
+        if (st != ATTN_OK) return st;
+    }
+    if (pl.big) {
+        // rows-heavy requests: tcgen05 kernel
         FwdParams t = p;
+        t.nsplit = ns_b;
+        t.split_chunk = chunk_for(ns_b);
         t.rows_lo = kSmallRows + 1;
         t.rows_hi = INT32_MAX;
         t.n_row_blocks = (max_rows + tc_rows_per_cta() - 1) / tc_rows_per_cta();
-        if ((long long)t.n_row_blocks * ns > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+        if ((long long)t.n_row_blocks * ns_b > 0x7fffffffLL) return ATTN_ERR_SHAPE;
         st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.T, a.stream));
         if (st != ATTN_OK) return st;
     }
-
-    if (ns > 1) {
+    if (stride > 1) {
         CombineParams c{};
         c.part_o = p.part_o;
         c.part_lse = p.part_lse;
         c.out = a.out;
         c.out_stride = a.out_stride;
         c.lse = a.lse;
+        c.cu_seqlens_q = a.cu_seqlens_q;
+        c.B = a.B;
         c.T = a.T;
         c.Hq = a.Hq;
         c.D = a.D;
-        c.nsplit = ns;
+        c.G = G;
+        c.small_rows_hi = pl.small ? pl.small_rows_hi : 0;
+        c.ns_small = ns_s;
+        c.ns_big = ns_b;
+        c.part_stride = stride;
         st = check_cuda(launch_combine(c, a.q_dtype, a.stream));
     }
     return st;
@@ -250,8 +273,9 @@ size_t attn_workspace_size(int total_q, int Hq, int D, int num_splits) {
 
 int attn_num_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int num_sms) {
     if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || B <= 0) return 1;
-    const Plan pl = make_plan(B, max_seqlen_q, Hq, Hkv, 128, ATTN_BF16, ATTN_BF16, num_sms);
-    return auto_splits(pl.base, max_seqlen_k, pl.target);
+    // both request classes may be present: the larger count sizes the workspace
+    const Plan pl = make_plan(B, max_seqlen_q, max_seqlen_k, false, Hq, Hkv, 128, ATTN_BF16, ATTN_BF16, num_sms);
+    return std::max(pl.small ? pl.ns_small : 1, pl.big ? pl.ns_big : 1);
 }
 
 int attn_tile_kind(int q_lo, int q_hi, int k_lo, int k_hi, int ctx) { return tile_kind(q_lo, q_hi, k_lo, k_hi, ctx); }

@@ -136,58 +136,78 @@ __device__ __forceinline__ void store4<__half>(__half *p, float4 v) {
 
 // One warp per (token, query head).  Segment s contributes with weight
 // exp(lse_s - lse), lse = log sum_s exp(lse_s); segments with lse_s = -inf
-// (no visible key) contribute nothing.
+// (no visible key) contribute nothing.  Tokens of requests that ran with a
+// single segment already hold their final output and are skipped.
 template <class OT>
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     const int warp_global = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (warp_global >= p.T * p.Hq) return;
-    const int64_t t = warp_global / p.Hq;
+    const int t = warp_global / p.Hq;
     const int h = warp_global % p.Hq;
-    const int64_t base = (t * p.Hq + h) * (int64_t)p.nsplit;
+    int q_len = 1;
+    if (p.cu_seqlens_q) {
+        int lo = 0, hi = p.B - 1;                 // last r with cu[r] <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.cu_seqlens_q[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        q_len = p.cu_seqlens_q[lo + 1] - p.cu_seqlens_q[lo];
+    }
+    const int ns = (q_len * p.G <= p.small_rows_hi) ? p.ns_small : p.ns_big;
+    if (ns <= 1) return;
+    const int64_t base = ((int64_t)t * p.Hq + h) * (int64_t)p.part_stride;
     const float *ls = p.part_lse + base;
     float mx = -INFINITY;
-    for (int s = lane; s < p.nsplit; s += 32) mx = fmaxf(mx, ls[s]);
+    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, ls[s]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     const int D = p.D;
-    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    const int d = lane * 4;                       // this lane's four columns
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
-    if (mx != -INFINITY) {
-        for (int s = 0; s < p.nsplit; ++s) {
+    if (mx != -INFINITY && d < D) {
+        const float *po = p.part_o + base * D + d;
+        int s = 0;
+        for (; s + 4 <= ns; s += 4) {             // four segments in flight
+            float w[4];
+            float4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float l = ls[s + k];
+                w[k] = l == -INFINITY ? 0.f : expf(l - mx);
+                v[k] = *reinterpret_cast<const float4 *>(po + (int64_t)(s + k) * D);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                // an empty segment wrote only its lse: its O slot is never read
+                if (w[k] == 0.f) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                wsum += w[k];
+                acc.x += w[k] * v[k].x;
+                acc.y += w[k] * v[k].y;
+                acc.z += w[k] * v[k].z;
+                acc.w += w[k] * v[k].w;
+            }
+        }
+        for (; s < ns; ++s) {
             const float l = ls[s];
             if (l == -INFINITY) continue;
             const float w = expf(l - mx);
+            const float4 v = *reinterpret_cast<const float4 *>(po + (int64_t)s * D);
             wsum += w;
-            const float *po = p.part_o + (base + s) * D;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int d = (lane + 32 * k) * 4;
-                if (d < D) {
-                    const float4 v = *reinterpret_cast<const float4 *>(po + d);
-                    acc[k].x += w * v.x;
-                    acc[k].y += w * v.y;
-                    acc[k].z += w * v.z;
-                    acc[k].w += w * v.w;
-                }
-            }
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    OT *out = reinterpret_cast<OT *>(p.out) + t * p.out_stride + (int64_t)h * D;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int d = (lane + 32 * k) * 4;
-        if (d < D) {
-            float4 v = acc[k];
-            v.x *= inv;
-            v.y *= inv;
-            v.z *= inv;
-            v.w *= inv;
-            store4<OT>(out + d, v);
-        }
+    if (d < D) {
+        OT *out = reinterpret_cast<OT *>(p.out) + (int64_t)t * p.out_stride + (int64_t)h * D;
+        store4<OT>(out + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
     }
-    if (lane == 0 && p.lse) p.lse[t * p.Hq + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+    if (lane == 0 && p.lse) p.lse[(int64_t)t * p.Hq + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 cudaError_t launch_combine(const CombineParams &p, int out_dtype, cudaStream_t stream) {

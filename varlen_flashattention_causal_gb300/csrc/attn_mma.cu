@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
             const int64_t tok = q_start + pr / G;
             const int h = kvh * G + pr % G;
             if (p.nsplit > 1) {
-                p.part_lse[(tok * p.Hq + h) * p.nsplit + s_idx] = -INFINITY;
+                p.part_lse[(tok * p.Hq + h) * p.part_stride + s_idx] = -INFINITY;
             } else {
                 if (p.lse) p.lse[tok * p.Hq + h] = -INFINITY;
                 using OT = typename Elem<C::QT>::T;
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
             *reinterpret_cast<uint2 *>(dst) = pk;
             if (c4 == 0 && p.lse) p.lse[tok * p.Hq + h] = lse_v;
         } else {
-            const int64_t slot = (tok * p.Hq + h) * p.nsplit + s_idx;
+            const int64_t slot = (tok * p.Hq + h) * p.part_stride + s_idx;
             *reinterpret_cast<float4 *>(p.part_o + slot * D + c4 * 4) = acc;
             if (c4 == 0) p.part_lse[slot] = lse_v;
         }

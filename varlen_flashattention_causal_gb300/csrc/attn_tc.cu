@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t tok = q_start + pr / G;
             const int h = kvh * G + pr % G;
             if (p.nsplit > 1) {
-                p.part_lse[(tok * p.Hq + h) * p.nsplit + s_idx] = -INFINITY;
+                p.part_lse[(tok * p.Hq + h) * p.part_stride + s_idx] = -INFINITY;
             } else {
                 if (p.lse) p.lse[tok * p.Hq + h] = -INFINITY;
                 uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     } else {
                         float4 *dst = reinterpret_cast<float4 *>(
-                            p.part_o + ((tok * p.Hq + h) * p.nsplit + s_idx) * kD + c * 32);
+                            p.part_o + ((tok * p.Hq + h) * p.part_stride + s_idx) * kD + c * 32);
 #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4)
                             dst[q4] = make_float4(__uint_as_float(o[q4 * 4]) * inv, __uint_as_float(o[q4 * 4 + 1]) * inv,
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.nsplit == 1) {
                         if (p.lse) p.lse[tok * p.Hq + h] = lse_v;
                     } else {
-                        p.part_lse[(tok * p.Hq + h) * p.nsplit + s_idx] = lse_v;
+                        p.part_lse[(tok * p.Hq + h) * p.part_stride + s_idx] = lse_v;
                     }
                 }
             }

@@ -35,21 +35,28 @@ struct FwdParams {
     float v_descale;
     int nsplit;                  // KV segments per (request, KV head, row block)
     int split_chunk;             // keys per segment (multiple of the KV tile)
-    float *part_o;               // [T, Hq, nsplit, D] fp32 (nsplit > 1)
-    float *part_lse;             // [T, Hq, nsplit]
+    int part_stride;             // segment slots per (token, head) in the workspace
+    float *part_o;               // [T, Hq, part_stride, D] fp32 (used when nsplit > 1)
+    float *part_lse;             // [T, Hq, part_stride]
     int rows_lo, rows_hi;
     int n_row_blocks;            // grid.x = n_row_blocks * nsplit
     unsigned *err;
 };
 
+// Split-KV reduction over the partial states of every token whose request
+// ran with more than one segment.  A token's request is found from
+// cu_seqlens_q (nullptr: token t is request t); its class -- packed rows
+// q_len * G up to small_rows_hi, or above -- gives its segment count.
 struct CombineParams {
     const float *part_o;
     const float *part_lse;
     void *out;
     int64_t out_stride;
     float *lse;
-    int T, Hq, D, nsplit;
-    float v_scale_unused;
+    const int32_t *cu_seqlens_q;
+    int B, T, Hq, D, G;
+    int small_rows_hi;
+    int ns_small, ns_big, part_stride;
 };
 
 // launchers (return the launch error)
