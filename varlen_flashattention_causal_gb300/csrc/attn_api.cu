@@ -79,9 +79,10 @@ int split_rule(long long base, int max_seqlen_k, long long target, int min_tiles
 }
 
 struct Plan {
-    bool small, big;      // launch the mma.sync (rows <= small_rows_hi) / tcgen05 kernel
-    int rpc;              // rows per CTA of the mma kernel
-    int small_rows_hi;    // largest packed row count the mma kernel takes
+    bool small, big;      // launch the rows-light class (packed rows <= small_rows_hi) / rows-heavy class
+    bool big_tc;          // rows-heavy class on the tcgen05 kernel (else the 64-row mma.sync kernel)
+    int rpc;              // rows per CTA of the rows-light mma kernel
+    int small_rows_hi;    // largest packed row count of the rows-light class
     int ns_small, ns_big; // segments per class (automatic choice)
 };
 
@@ -92,20 +93,21 @@ Plan make_plan(int B, int max_q, int max_k, bool uniform, int Hq, int Hkv, int D
     Plan pl{};
     const int G = Hq / Hkv;
     const int max_rows = std::max(1, max_q) * G;
-    const bool tc = tc_supported(D, q_dtype, kv_dtype, G) && max_rows > kSmallRows;
-    pl.big = tc;
-    pl.small = !tc || !uniform;
-    pl.small_rows_hi = tc ? kSmallRows : INT32_MAX;
-    pl.rpc = mma_rows_per_cta(std::min(max_rows, tc ? kSmallRows : max_rows));
+    pl.big = max_rows > kSmallRows;
+    pl.big_tc = pl.big && tc_supported(D, q_dtype, kv_dtype, G);
+    pl.small = !pl.big || !uniform;
+    pl.small_rows_hi = pl.big ? kSmallRows : INT32_MAX;
+    pl.rpc = mma_rows_per_cta(std::min(max_rows, kSmallRows));
     pl.ns_small = pl.ns_big = 1;
     if (pl.small) {
-        const long long rb = (std::min(max_rows, pl.small_rows_hi) + pl.rpc - 1) / pl.rpc;
+        const long long rb = (std::min(max_rows, kSmallRows) + pl.rpc - 1) / pl.rpc;
         // decode-like rows: also bound the keys per segment (32 tiles)
         pl.ns_small = split_rule((long long)B * Hkv * rb, max_k, 4LL * sms, 2, rb == 1 ? 32 : 0);
     }
     if (pl.big) {
-        const long long rb = (max_rows + tc_rows_per_cta() - 1) / tc_rows_per_cta();
-        pl.ns_big = split_rule((long long)B * Hkv * rb, max_k, 2LL * sms, 4, 0);
+        const int rpc_big = pl.big_tc ? tc_rows_per_cta() : mma_rows_per_cta(max_rows);
+        const long long rb = (max_rows + rpc_big - 1) / rpc_big;
+        pl.ns_big = split_rule((long long)B * Hkv * rb, max_k, (pl.big_tc ? 2LL : 4LL) * sms, 4, 0);
     }
     return pl;
 }
@@ -229,15 +231,21 @@ attn_status run_fwd(const FwdArgs &a) {
         if (st != ATTN_OK) return st;
     }
     if (pl.big) {
-        // rows-heavy requests: tcgen05 kernel
+        // rows-heavy requests: tcgen05 kernel, or the 64-row mma.sync kernel
+        // for shapes it does not take (head size 64, e4m3 caches, G not
+        // dividing 128)
         FwdParams t = p;
         t.nsplit = ns_b;
         t.split_chunk = chunk_for(ns_b);
         t.rows_lo = kSmallRows + 1;
         t.rows_hi = INT32_MAX;
-        t.n_row_blocks = (max_rows + tc_rows_per_cta() - 1) / tc_rows_per_cta();
+        const int rpc_big = pl.big_tc ? tc_rows_per_cta() : mma_rows_per_cta(max_rows);
+        t.n_row_blocks = (max_rows + rpc_big - 1) / rpc_big;
         if ((long long)t.n_row_blocks * ns_b > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-        st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.T, a.stream));
+        if (pl.big_tc)
+            st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.T, a.stream));
+        else
+            st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, rpc_big, a.stream));
         if (st != ATTN_OK) return st;
     }
     if (stride > 1) {
