@@ -425,3 +425,22 @@ def test_short_segments_repeated_are_stable():
         out, lse = gpu_attn(b, kc, vc, num_splits=(32, 0, 16)[it % 3])
         check(out, lse, ro, rl, TOL)
     assert_no_device_error()
+
+
+@pytest.mark.parametrize("q_dtype,bs", [(torch.bfloat16, 32), (torch.float16, 16), (torch.bfloat16, 48),
+                                        (torch.bfloat16, 256)])
+def test_fp8_kv_rows_heavy(q_dtype, bs):
+    """e4m3 caches under rows-heavy requests (the tensor-core path widens
+    the staged e4m3 tiles to fp16): prefill, chunked prefill with context,
+    a ragged tail, next to decode rows in the same batch."""
+    b = W.make_batch([300, 70, 1, 129], [300, 500, 1000, 200], 8, 2, 128, bs, seed=16, kv_dtype="fp8",
+                     q_dtype=q_dtype)
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    assert torch.equal(kc.view(torch.uint8).cpu(), ck.view(torch.uint8))
+    ro, rl = ref_attn(b, ck, cv)
+    for ns in (1, 3, 0):
+        out, lse = gpu_attn(b, kc, vc, num_splits=ns)
+        assert out.dtype == q_dtype
+        check(out, lse, ro, rl, TOL_FP8)
+    assert_no_device_error()

@@ -243,7 +243,7 @@ attn_status run_fwd(const FwdArgs &a) {
         t.n_row_blocks = (max_rows + rpc_big - 1) / rpc_big;
         if ((long long)t.n_row_blocks * ns_b > 0x7fffffffLL) return ATTN_ERR_SHAPE;
         if (pl.big_tc)
-            st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.T, a.stream));
+            st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.kv_dtype, a.T, a.stream));
         else
             st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, rpc_big, a.stream));
         if (st != ATTN_OK) return st;

@@ -54,13 +54,6 @@ struct MmaCfg {
     static_assert((RPW * CH) % 32 == 0, "whole warp copy rounds");
 };
 
-// two e4m3 values (low byte first) -> two fp16 values in one register; the
-// conversion is exact (every e4m3 value is an fp16 value)
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
-
 template <class C>
 __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     constexpr int D = C::D, ROWS = C::ROWS, BN = C::BN, STAGES = C::STAGES;

@@ -51,23 +51,34 @@ namespace {
 constexpr int kBM = 128;                               // rows per Q tile
 constexpr int kBN = 64;                                // keys per K/V tile
 constexpr int kD = 128;                                // head size handled here
-constexpr int kSlots = 10;                             // K/V ring slots
-constexpr int kThreads = 352;
 constexpr uint32_t kQBytes = kBM * kD * 2;             // one Q tile, 32 KB
 constexpr uint32_t kQHalf = kBM * 128;                 // 64 columns of a Q tile
-constexpr uint32_t kTileBytes = kBN * kD * 2;          // one K or V tile, 16 KB
+constexpr uint32_t kTileBytes = kBN * kD * 2;          // one 16-bit K or V tile, 16 KB
 constexpr uint32_t kKVHalf = kBN * 128;                // 64 columns of a K/V tile
+constexpr uint32_t kStageBytes = kBN * kD;             // one e4m3 K or V tile, 8 KB
 constexpr float kRescaleThreshold = 8.0f;              // log2 units
 
-// shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t kOffQ = 0;                          // Q_A, Q_B
-constexpr uint32_t kOffKV = kOffQ + 2 * kQBytes;       // ring slots
-constexpr uint32_t kOffBar = kOffKV + kSlots * kTileBytes;
-constexpr int kNumBars = 1 + 2 * kSlots + 4 + 4 + 4 + 2;
-constexpr uint32_t kOffMisc = kOffBar + 8 * 40;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
-static_assert(kNumBars <= 40, "barrier area");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+// Shared memory map (offsets from a 1024-aligned base).  16-bit caches:
+// Q_A, Q_B, then a ring of ten 16 KB K/V slots the TMA fills directly.
+// e4m3 caches: Q_A, Q_B, a ring of eight 16 KB fp16 slots, and a ring of
+// four 8 KB staging slots the TMA fills with e4m3 pages; two converter
+// warps widen each staged tile into the fp16 ring (exact: every e4m3
+// value is an fp16 value).
+template <bool FP8>
+struct TcLayout {
+    static constexpr int kSlots = FP8 ? 8 : 10;
+    static constexpr int kStages = FP8 ? 4 : 0;
+    static constexpr int kThreads = FP8 ? 416 : 352;
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffKV = kOffQ + 2 * kQBytes;
+    static constexpr uint32_t kOffStage = kOffKV + kSlots * kTileBytes;
+    static constexpr uint32_t kOffBar = kOffStage + kStages * kStageBytes;
+    static constexpr int kNumBars = 16 + 2 * kSlots + 2 * kStages;
+    static constexpr uint32_t kOffMisc = kOffBar + 8 * 48;
+    static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;   // + alignment slack
+    static_assert(kNumBars <= 48, "barrier area");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
 
 // TMEM column offsets of S_x buffer b and O_x
 __device__ __forceinline__ uint32_t col_s(int x, int b) { return (uint32_t)x * 128u + (uint32_t)b * 64u; }
@@ -88,10 +99,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+// MMA_BF16: tensor-core operand type (bf16, else fp16); OUT_BF16: output
+// type (that of q); FP8: e4m3 caches, widened to fp16 in shared memory.
+template <bool MMA_BF16, bool OUT_BF16, bool FP8>
+__global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap qmap,
                   const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+    using Lay = TcLayout<FP8>;
+    constexpr int kSlots = Lay::kSlots, kStages = Lay::kStages;
+    constexpr uint32_t kOffQ = Lay::kOffQ, kOffKV = Lay::kOffKV, kOffStage = Lay::kOffStage;
+    constexpr uint32_t kOffBar = Lay::kOffBar, kOffMisc = Lay::kOffMisc;
     const FwdParams &p = tp.f;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -111,6 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto B_PFULL = [](int x, int b) { return 5 + 2 * kSlots + 2 * x + b; };
     auto B_ODONE = [](int x, int b) { return 9 + 2 * kSlots + 2 * x + b; };
     auto B_DRAIN = [](int x) { return 13 + 2 * kSlots + x; };
+    // e4m3 mode: staging ring (TMA -> converters) and "Q is fp16" barriers
+    auto B_STFULL = [](int t) { return 15 + 2 * kSlots + t; };
+    auto B_STEMPTY = [](int t) { return 15 + 2 * kSlots + kStages + t; };
+    constexpr int B_QREADY = 15 + 2 * kSlots + 2 * kStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc);
     uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc + 8);
     volatile int *never = reinterpret_cast<volatile int *>(sm + kOffMisc + 16);
@@ -161,9 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         *never = 0;
         mbar_init(bar(B_Q), 1);
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(bar(B_FULL(s)), 1);
+            mbar_init(bar(B_FULL(s)), FP8 ? 2u : 1u);          // TMA bytes, or the two converter warps
             mbar_init(bar(B_EMPTY(s)), (uint32_t)ntiles_q);   // one release per active Q tile
         }
+        for (int t = 0; t < kStages; ++t) {
+            mbar_init(bar(B_STFULL(t)), 1);
+            mbar_init(bar(B_STEMPTY(t)), 2);
+        }
+        if (FP8) mbar_init(bar(B_QREADY), 2);
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(B_SFULL(x, 0)), 1);
             mbar_init(bar(B_SFULL(x, 1)), 1);
@@ -235,16 +261,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int kv = 0; kv < 2 && ok; ++kv) {
                 const int L = 2 * j + kv;        // load index
-                const int slot = L % kSlots;
-                if (L >= kSlots) ok = warp_wait(bar(B_EMPTY(slot)), ((L / kSlots) - 1) & 1, abort_flag);
-                if (!ok) break;
-                if (lane == 0) mbar_expect_tx(bar(B_FULL(slot)), (uint32_t)nvalid * R * kD * 2);
-                __syncwarp();
-                if (mine >= 0) {
-                    const CUtensorMap *m = kv ? &vmap : &kmap;
-                    const uint32_t dst = sbase + kOffKV + slot * kTileBytes + lane * R * 128;
-                    tma_load_3d(dst, m, 0, kvh, mine, bar(B_FULL(slot)));
-                    tma_load_3d(dst + kKVHalf, m, 64, kvh, mine, bar(B_FULL(slot)));
+                const CUtensorMap *m = kv ? &vmap : &kmap;
+                if constexpr (FP8) {
+                    // e4m3 pages -> staging slot (one 128-byte row per key, no swizzle)
+                    const int st = L % kStages;
+                    if (L >= kStages) ok = warp_wait(bar(B_STEMPTY(st)), ((L / kStages) - 1) & 1, abort_flag);
+                    if (!ok) break;
+                    if (lane == 0) mbar_expect_tx(bar(B_STFULL(st)), (uint32_t)nvalid * R * kD);
+                    __syncwarp();
+                    if (mine >= 0)
+                        tma_load_3d(sbase + kOffStage + st * kStageBytes + lane * R * 128, m, 0, kvh, mine,
+                                    bar(B_STFULL(st)));
+                } else {
+                    const int slot = L % kSlots;
+                    if (L >= kSlots) ok = warp_wait(bar(B_EMPTY(slot)), ((L / kSlots) - 1) & 1, abort_flag);
+                    if (!ok) break;
+                    if (lane == 0) mbar_expect_tx(bar(B_FULL(slot)), (uint32_t)nvalid * R * kD * 2);
+                    __syncwarp();
+                    if (mine >= 0) {
+                        const uint32_t dst = sbase + kOffKV + slot * kTileBytes + lane * R * 128;
+                        tma_load_3d(dst, m, 0, kvh, mine, bar(B_FULL(slot)));
+                        tma_load_3d(dst + kKVHalf, m, 64, kvh, mine, bar(B_FULL(slot)));
+                    }
                 }
                 issued = L;
             }
@@ -252,16 +290,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // drain: every load issued has landed before the CTA exits
         if (lane == 0) {
-            for (int L = max(0, issued - kSlots + 1); L <= issued; ++L)
-                mbar_wait(bar(B_FULL(L % kSlots)), (L / kSlots) & 1, never);
+            if constexpr (FP8) {
+                for (int L = max(0, issued - kStages + 1); L <= issued; ++L)
+                    mbar_wait(bar(B_STFULL(L % kStages)), (L / kStages) & 1, never);
+            } else {
+                for (int L = max(0, issued - kSlots + 1); L <= issued; ++L)
+                    mbar_wait(bar(B_FULL(L % kSlots)), (L / kSlots) & 1, never);
+            }
             mbar_wait(bar(B_Q), 0, never);
         }
     } else if (warp == 1 || warp == 10) {
         // ================================================ MMA issuers (tile x)
         const int x = warp == 1 ? 0 : 1;
         if (lane == 0 && x < ntiles_q) {
-            const uint32_t idS = idesc_f16(BF16, kBM, kBN, false, false);
-            const uint32_t idO = idesc_f16(BF16, kBM, kD, false, true);
+            const uint32_t idS = idesc_f16(MMA_BF16, kBM, kBN, false, false);
+            const uint32_t idO = idesc_f16(MMA_BF16, kBM, kD, false, true);
             // descriptors of every operand base, built once; a K slice or a
             // ring slot only adds a small offset to the start-address field
             // (addresses stay below 2^18, so the 14-bit field never carries)
@@ -269,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dK = sdesc_sw128(sbase + kOffKV, 16, 1024);
             const uint64_t dV = sdesc_sw128(sbase + kOffKV, kKVHalf, 1024);
             const uint32_t tOx = tmem + col_o(x);
-            bool ok = mbar_wait(bar(B_Q), 0, abort_flag);
+            bool ok = mbar_wait(bar(FP8 ? B_QREADY : B_Q), 0, abort_flag);
             for (int j = 0; j <= n_kv && ok; ++j) {
                 const int sk = (2 * j) % kSlots;                  // K_j
                 const int sv = (2 * j + kSlots - 1) % kSlots;     // V_(j-1)
@@ -307,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(bar(B_DRAIN(x)), 0, never);
             }
         }
-    } else {
+    } else if (warp >= 2 && warp <= 9) {
         // ================================================ softmax warpgroups
         const int x = (warp - 2) >> 2;              // Q tile 0 (A) or 1 (B)
         const int quarter = warp & 3;               // TMEM lane quarter this warp may access
@@ -378,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -base));
                 const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -base));
                 rs8[(e >> 1) & 7] += p0 + p1;
-                pk[e / 2] = pack2<BF16>(p0, p1);
+                pk[e / 2] = pack2<MMA_BF16>(p0, p1);
             }
             const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l = l * alpha + rs;
@@ -443,10 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             uint4 w;
-                            w.x = pack2<BF16>(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
-                            w.y = pack2<BF16>(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
-                            w.z = pack2<BF16>(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
-                            w.w = pack2<BF16>(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
+                            w.x = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
+                            w.y = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
+                            w.z = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
+                            w.w = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
                             dst[q4] = w;
                         }
                     } else {
@@ -466,6 +509,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.part_lse[(tok * p.Hq + h) * p.part_stride + s_idx] = lse_v;
                     }
                 }
+            }
+        }
+    } else if (FP8) {
+        // ============================== e4m3 -> fp16 converters (warps 11, 12)
+        const int cid = tid - 352;                 // 0 .. 63
+        bool ok = warp_wait(bar(B_Q), 0, abort_flag);
+        if (ok) {
+            if constexpr (OUT_BF16) {
+                // q arrived as bf16; the MMAs run on fp16 operands: convert in place
+                uint4 *qv = reinterpret_cast<uint4 *>(sm + kOffQ);
+                for (int c = cid; c < ntiles_q * (int)(kQBytes / 16); c += 64) {
+                    const uint4 raw = qv[c];
+                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                    uint4 w;
+                    uint32_t *wu = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 f = __bfloat1622float2(b2[k]);
+                        wu[k] = pack2<false>(f.x, f.y);
+                    }
+                    qv[c] = w;
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_QREADY));
+        }
+        for (int L = 0; L < 2 * n_kv && ok; ++L) {
+            const int st = L % kStages, sl = L % kSlots;
+            ok = warp_wait(bar(B_STFULL(st)), (L / kStages) & 1, abort_flag);
+            if (ok && L >= kSlots) ok = warp_wait(bar(B_EMPTY(sl)), ((L / kSlots) - 1) & 1, abort_flag);
+            if (!ok) break;
+            const uint8_t *src = sm + kOffStage + st * kStageBytes;
+            uint8_t *dst = sm + kOffKV + sl * kTileBytes;
+            for (int i = cid; i < kBN * 8; i += 64) {
+                const int row = i >> 3, c = i & 7;          // e4m3 columns 16c .. 16c + 15 of one key
+                const uint4 raw = *reinterpret_cast<const uint4 *>(src + row * 128 + c * 16);
+                const uint16_t *b = reinterpret_cast<const uint16_t *>(&raw);
+                const uint4 lo = make_uint4(e4m3x2_to_h2(b[0]), e4m3x2_to_h2(b[1]), e4m3x2_to_h2(b[2]),
+                                            e4m3x2_to_h2(b[3]));
+                const uint4 hi = make_uint4(e4m3x2_to_h2(b[4]), e4m3x2_to_h2(b[5]), e4m3x2_to_h2(b[6]),
+                                            e4m3x2_to_h2(b[7]));
+                // fp16 columns 16c .. 16c + 15: 64-column half c / 4, 16-byte
+                // chunks 2 (c % 4) and 2 (c % 4) + 1 of that half, 128-byte swizzle
+                const int q = 2 * (c & 3);
+                uint8_t *rowp = dst + (c >> 2) * kKVHalf + row * 128;
+                *reinterpret_cast<uint4 *>(rowp + ((q ^ (row & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4 *>(rowp + (((q + 1) ^ (row & 7)) << 4)) = hi;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(B_STEMPTY(st)));
+                mbar_arrive(bar(B_FULL(sl)));
             }
         }
     }
@@ -491,43 +588,60 @@ static int gcd_int(int a, int b) {
 
 bool tc_supported(int D, int q_dtype, int kv_dtype, int G) {
     if (D != kD) return false;
-    if (!((q_dtype == DT_BF16 && kv_dtype == DT_BF16) || (q_dtype == DT_FP16 && kv_dtype == DT_FP16))) return false;
+    const bool ok_types = (q_dtype == DT_BF16 && kv_dtype == DT_BF16) || (q_dtype == DT_FP16 && kv_dtype == DT_FP16) ||
+                          ((q_dtype == DT_BF16 || q_dtype == DT_FP16) && kv_dtype == DT_E4M3);
+    if (!ok_types) return false;
     if (G <= 0 || G > 128 || (128 % G) != 0) return false;
     return true;
 }
 
 int tc_rows_per_cta() { return 2 * kBM; }
 
-cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int64_t T, cudaStream_t stream) {
+template <bool MMA_BF16, bool OUT_BF16, bool FP8>
+static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                             const CUtensorMap &vmap, dim3 grid, cudaStream_t stream) {
+    using Lay = TcLayout<FP8>;
+    auto kern = fwd_tc_kernel<MMA_BF16, OUT_BF16, FP8>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, Lay::kThreads, Lay::kSmemBytes, stream>>>(tp, qmap, kmap, vmap);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int kv_dtype, int64_t T, cudaStream_t stream) {
     TcParams tp{};
     tp.f = f;
     tp.kv_rows = gcd_int(f.bs, kBN);
-    const bool fp16 = q_dtype == DT_FP16;
+    const bool q16 = q_dtype == DT_FP16;
+    const bool fp8 = kv_dtype == DT_E4M3;
     CUtensorMap qmap, kmap, vmap;
     // Q viewed as [T][Hq][D]: box = 64 columns x G heads x (128 / G) tokens
-    if (!encode_3d_bf16(&qmap, f.q, fp16, kD, (uint64_t)f.Hq, (uint64_t)T, (uint64_t)kD * 2,
+    if (!encode_3d_bf16(&qmap, f.q, q16, kD, (uint64_t)f.Hq, (uint64_t)T, (uint64_t)kD * 2,
                         (uint64_t)f.q_stride * 2, 64, (uint32_t)f.G, (uint32_t)(kBM / f.G)))
         return cudaErrorInvalidValue;
-    // caches viewed as [num_blocks * bs][Hkv][D]: box = 64 columns x 1 head x R rows
+    // caches viewed as [num_blocks * bs][Hkv][D]: box = 1 head x R rows and
+    // 64 columns (16-bit, swizzled) or all 128 bytes of a row (e4m3)
     const uint64_t nslots = (uint64_t)f.num_blocks * f.bs;
-    if (!encode_3d_bf16(&kmap, f.k_cache, fp16, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD * 2,
-                        (uint64_t)f.Hkv * kD * 2, 64, 1, (uint32_t)tp.kv_rows))
-        return cudaErrorInvalidValue;
-    if (!encode_3d_bf16(&vmap, f.v_cache, fp16, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD * 2,
-                        (uint64_t)f.Hkv * kD * 2, 64, 1, (uint32_t)tp.kv_rows))
-        return cudaErrorInvalidValue;
-    dim3 grid((unsigned)(f.n_row_blocks * f.nsplit), (unsigned)f.Hkv, (unsigned)f.B);
-    cudaError_t e;
-    if (fp16) {
-        e = cudaFuncSetAttribute(fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        fwd_tc_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tp, qmap, kmap, vmap);
+    const uint32_t R = (uint32_t)tp.kv_rows;
+    if (fp8) {
+        if (!encode_3d_u8(&kmap, f.k_cache, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD, (uint64_t)f.Hkv * kD, kD, 1, R) ||
+            !encode_3d_u8(&vmap, f.v_cache, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD, (uint64_t)f.Hkv * kD, kD, 1, R))
+            return cudaErrorInvalidValue;
     } else {
-        e = cudaFuncSetAttribute(fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        fwd_tc_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tp, qmap, kmap, vmap);
+        if (!encode_3d_bf16(&kmap, f.k_cache, q16, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD * 2,
+                            (uint64_t)f.Hkv * kD * 2, 64, 1, R) ||
+            !encode_3d_bf16(&vmap, f.v_cache, q16, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD * 2,
+                            (uint64_t)f.Hkv * kD * 2, 64, 1, R))
+            return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+    dim3 grid((unsigned)(f.n_row_blocks * f.nsplit), (unsigned)f.Hkv, (unsigned)f.B);
+    if (fp8) {
+        // e4m3 caches: fp16 MMAs (the widening is exact); output in q's type
+        return q16 ? launch_tc<false, false, true>(tp, qmap, kmap, vmap, grid, stream)
+                   : launch_tc<false, true, true>(tp, qmap, kmap, vmap, grid, stream);
+    }
+    return q16 ? launch_tc<false, false, false>(tp, qmap, kmap, vmap, grid, stream)
+               : launch_tc<true, true, false>(tp, qmap, kmap, vmap, grid, stream);
 }
 
 }  // namespace attn

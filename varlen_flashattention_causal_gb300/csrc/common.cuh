@@ -39,6 +39,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// two e4m3 values (low byte first) -> two fp16 values in one register; the
+// conversion is exact (every e4m3 value is an fp16 value)
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
 // ------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

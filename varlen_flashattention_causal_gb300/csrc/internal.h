@@ -87,6 +87,6 @@ int mma_rows_per_cta(int max_rows);
 // tcgen05 kernel: whether it handles this shape, rows per CTA, launcher
 bool tc_supported(int D, int q_dtype, int kv_dtype, int G);
 int tc_rows_per_cta();
-cudaError_t launch_fwd_tc(const FwdParams &p, int q_dtype, int64_t T, cudaStream_t stream);
+cudaError_t launch_fwd_tc(const FwdParams &p, int q_dtype, int kv_dtype, int64_t T, cudaStream_t stream);
 
 }  // namespace attn
