@@ -21,6 +21,12 @@
  *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
  *    does no host synchronisation, so a call can be captured in a CUDA graph
  *    when its pointers and host scalars stay fixed.
+ *  - The tensor-core kernel schedules its work with a ticket counter taken
+ *    from a pool of 64 per device, one per call in turn.  So at most 64
+ *    attention calls may run on one device at the same moment (different
+ *    streams or host threads).  A captured graph keeps its counter: do not
+ *    replay one graph on two streams at once.  The same holds for its
+ *    workspace anyway.
  *  - Arguments are validated on the host before anything is launched.  On a
  *    non-zero status nothing was launched and no memory was touched.
  *  - Block ids and slots are also checked inside the kernels: an id outside

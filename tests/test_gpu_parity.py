@@ -444,3 +444,66 @@ def test_fp8_kv_rows_heavy(q_dtype, bs):
         assert out.dtype == q_dtype
         check(out, lse, ro, rl, TOL_FP8)
     assert_no_device_error()
+
+
+def test_cuda_graph_capture_and_replay():
+    """A whole step -- the KV write of the batch's tokens, then one mixed
+    call (decode rows, a chunk with context, a prefill; split-KV and its
+    combine) -- captured once in a CUDA graph and replayed.  Capture fails
+    if the path synchronises the host or allocates; every replay reuses the
+    tensor-core kernel's ticket counter, which must have rewound itself."""
+    b = W.make_batch([300, 1, 1, 40, 1], [700, 900, 64, 40, 2000], 32, 8, 128, 16, seed=17)
+    kc, vc = gpu_cache(b)
+    ro, rl = ref_attn(b, *cpu_cache(b))
+    dev = torch.device("cuda")
+    q = b.q.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    cu, su, bt = b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev)
+    kt, vt, sl = b.k_tok.to(dev), b.v_tok.to(dev), b.slot_mapping.to(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ns = va.attn_num_splits(b.B, b.max_seqlen_q, b.max_seqlen_k, b.Hq, b.Hkv, sms)
+    ws = torch.empty(max(1, va.attn_workspace_size(b.T, b.Hq, b.D, max(ns, 2))), dtype=torch.uint8, device=dev)
+
+    def step():
+        va.kv_cache_write(kt, vt, kc, vc, sl)
+        va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt, b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale,
+                               causal=True, lse_out=lse, num_splits=0, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(4):
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        check(out, lse, ro, rl, TOL)
+    assert_no_device_error()
+
+
+def test_tensor_core_schedule_slots_cycle():
+    """More consecutive calls than the tensor-core kernel has schedule slots
+    (64): every call takes a slot in turn and must find its counter rewound,
+    so every output is bitwise the first one (which matches the oracle)."""
+    b = W.make_batch([130, 200, 1], [400, 260, 300], 8, 2, 128, 16, seed=18)
+    kc, vc = gpu_cache(b)
+    ro, rl = ref_attn(b, *cpu_cache(b))
+    first = None
+    for it in range(140):
+        out, lse = gpu_attn(b, kc, vc, num_splits=1 + it % 2)
+        if first is None:
+            check(out, lse, ro, rl, TOL)
+            first = {1: (out, lse)}
+        elif (1 + it % 2) not in first:
+            check(out, lse, ro, rl, TOL)
+            first[1 + it % 2] = (out, lse)
+        else:
+            o0, l0 = first[1 + it % 2]
+            assert torch.equal(out, o0) and torch.equal(lse, l0), "call %d differs" % it
+    assert_no_device_error()

@@ -58,9 +58,11 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t part_o_bytes(int T, int Hq, int D, int ns) { return align256((size_t)T * Hq * ns * D * sizeof(float)); }
 
-// packed rows (q_len * G) up to which a request runs on the mma.sync
-// kernel; larger requests run on the tcgen05 kernel when it supports the shape
-constexpr int kSmallRows = 64;
+// packed rows (q_len * G) up to which a request runs in the rows-light
+// class: the mma.sync kernel with 16-row CTAs (decode: one token x up to 16
+// heads of a group).  Larger requests run on the tcgen05 kernel when it
+// supports the shape, else on the mma.sync kernel sized for the largest one.
+constexpr int kSmallRows = 16;
 
 // Split rule.  `base` CTAs run without splitting; `target` is the CTA count
 // that fills every SM twice.  Too few CTAs: cut each request's keys into
@@ -80,7 +82,7 @@ int split_rule(long long base, int max_seqlen_k, long long target, int min_tiles
 
 struct Plan {
     bool small, big;      // launch the rows-light class (packed rows <= small_rows_hi) / rows-heavy class
-    bool big_tc;          // rows-heavy class on the tcgen05 kernel (else the 64-row mma.sync kernel)
+    bool big_tc;          // rows-heavy class on the tcgen05 kernel (else the mma.sync kernel)
     int rpc;              // rows per CTA of the rows-light mma kernel
     int small_rows_hi;    // largest packed row count of the rows-light class
     int ns_small, ns_big; // segments per class (automatic choice)
@@ -95,14 +97,15 @@ Plan make_plan(int B, int max_q, int max_k, bool uniform, int Hq, int Hkv, int D
     const int max_rows = std::max(1, max_q) * G;
     pl.big = max_rows > kSmallRows;
     pl.big_tc = pl.big && tc_supported(D, q_dtype, kv_dtype, G);
-    pl.small = !pl.big || !uniform;
+    // a group wider than the class bound leaves the rows-light class empty
+    pl.small = !pl.big || (!uniform && G <= kSmallRows);
     pl.small_rows_hi = pl.big ? kSmallRows : INT32_MAX;
     pl.rpc = mma_rows_per_cta(std::min(max_rows, kSmallRows));
     pl.ns_small = pl.ns_big = 1;
     if (pl.small) {
         const long long rb = (std::min(max_rows, kSmallRows) + pl.rpc - 1) / pl.rpc;
         // decode-like rows: also bound the keys per segment (32 tiles)
-        pl.ns_small = split_rule((long long)B * Hkv * rb, max_k, 4LL * sms, 2, rb == 1 ? 32 : 0);
+        pl.ns_small = split_rule((long long)B * Hkv * rb, max_k, 6LL * sms, 2, rb == 1 ? 32 : 0);
     }
     if (pl.big) {
         const int rpc_big = pl.big_tc ? tc_rows_per_cta() : mma_rows_per_cta(max_rows);
@@ -170,11 +173,13 @@ attn_status run_fwd(const FwdArgs &a) {
         ns_s = pl.small ? std::min(a.num_splits, kMaxSplits) : 1;
         ns_b = pl.big ? std::min(a.num_splits, kMaxSplits) : 1;
     } else {
-        // automatic: cap to what the workspace holds
-        const size_t per_split = (size_t)a.T * a.Hq * (a.D + 1) * sizeof(float) + 512;
-        const size_t fit = a.ws ? a.ws_bytes / per_split : 0;
-        if ((size_t)ns_s > fit) ns_s = fit >= 2 ? (int)fit : 1;
-        if ((size_t)ns_b > fit) ns_b = fit >= 2 ? (int)fit : 1;
+        // automatic: cap to what the workspace holds (the layout is sized
+        // by the larger of the two counts)
+        auto fits = [&](int n) { return n <= 1 || (a.ws && a.ws_bytes >= attn_workspace_size(a.T, a.Hq, a.D, n)); };
+        while (!fits(std::max(ns_s, ns_b))) {
+            if (ns_s >= ns_b) --ns_s;
+            else --ns_b;
+        }
     }
     const int stride = std::max(ns_s, ns_b);
     if (stride > 1) {
@@ -231,9 +236,9 @@ attn_status run_fwd(const FwdArgs &a) {
         if (st != ATTN_OK) return st;
     }
     if (pl.big) {
-        // rows-heavy requests: tcgen05 kernel, or the 64-row mma.sync kernel
-        // for shapes it does not take (head size 64, e4m3 caches, G not
-        // dividing 128)
+        // rows-heavy requests: tcgen05 kernel, or, for shapes it does not
+        // take (head size 64, G not dividing 128), the mma.sync kernel sized
+        // for the largest request
         FwdParams t = p;
         t.nsplit = ns_b;
         t.split_chunk = chunk_for(ns_b);
@@ -243,7 +248,7 @@ attn_status run_fwd(const FwdArgs &a) {
         t.n_row_blocks = (max_rows + rpc_big - 1) / rpc_big;
         if ((long long)t.n_row_blocks * ns_b > 0x7fffffffLL) return ATTN_ERR_SHAPE;
         if (pl.big_tc)
-            st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.kv_dtype, a.T, a.stream));
+            st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.kv_dtype, a.T, dev->sms, a.stream));
         else
             st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, rpc_big, a.stream));
         if (st != ATTN_OK) return st;

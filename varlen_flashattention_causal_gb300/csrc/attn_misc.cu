@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint8_t *__restrict
                                                         const int64_t *__restrict__ slot_mapping, int T, int Hkv,
                                                         int D, int bs, int num_blocks, float k_scale, float v_scale,
                                                         unsigned *err) {
+    pdl_wait();
+    pdl_trigger();
     const int chunks = D / 8;
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = (int64_t)T * Hkv * chunks;
@@ -85,15 +87,14 @@ cudaError_t launch_kv_write(const void *key, int64_t ks, const void *value, int6
     auto *kc = reinterpret_cast<uint8_t *>(k_cache);
     auto *vc = reinterpret_cast<uint8_t *>(v_cache);
 #define KVW(ST, CT)                                                                                          \
-    kv_write_kernel<ST, CT><<<blocks, 256, 0, stream>>>(k, ks, v, vs, kc, vc, slot, T, Hkv, D, bs, num_blocks, \
-                                                         k_scale, v_scale, err)
-    if (src_dtype == DT_BF16 && kv_dtype == DT_BF16) KVW(DT_BF16, DT_BF16);
-    else if (src_dtype == DT_FP16 && kv_dtype == DT_FP16) KVW(DT_FP16, DT_FP16);
-    else if (src_dtype == DT_BF16 && kv_dtype == DT_E4M3) KVW(DT_BF16, DT_E4M3);
-    else if (src_dtype == DT_FP16 && kv_dtype == DT_E4M3) KVW(DT_FP16, DT_E4M3);
-    else return cudaErrorInvalidValue;
+    launch_pdl(kv_write_kernel<ST, CT>, dim3(blocks), dim3(256), 0, stream, k, ks, v, vs, kc, vc, slot, T, Hkv, D, \
+               bs, num_blocks, k_scale, v_scale, err)
+    if (src_dtype == DT_BF16 && kv_dtype == DT_BF16) return KVW(DT_BF16, DT_BF16);
+    if (src_dtype == DT_FP16 && kv_dtype == DT_FP16) return KVW(DT_FP16, DT_FP16);
+    if (src_dtype == DT_BF16 && kv_dtype == DT_E4M3) return KVW(DT_BF16, DT_E4M3);
+    if (src_dtype == DT_FP16 && kv_dtype == DT_E4M3) return KVW(DT_FP16, DT_E4M3);
 #undef KVW
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 // ------------------------------------------------------------ state merges
@@ -134,12 +135,16 @@ __device__ __forceinline__ void store4<__half>(__half *p, float4 v) {
     *reinterpret_cast<uint2 *>(p) = make_uint2(pack2<false>(v.x, v.y), pack2<false>(v.z, v.w));
 }
 
+constexpr int kCombineBatch = 8;   // segments whose partial rows a lane loads at once
+
 // One warp per (token, query head).  Segment s contributes with weight
 // exp(lse_s - lse), lse = log sum_s exp(lse_s); segments with lse_s = -inf
 // (no visible key) contribute nothing.  Tokens of requests that ran with a
 // single segment already hold their final output and are skipped.
 template <class OT>
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+    pdl_wait();
+    pdl_trigger();
     const int warp_global = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (warp_global >= p.T * p.Hq) return;
@@ -169,37 +174,28 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     float wsum = 0.f;
     if (mx != -INFINITY && d < D) {
         const float *po = p.part_o + base * D + d;
-        int s = 0;
-        for (; s + 4 <= ns; s += 4) {             // four segments in flight
-            float w[4];
-            float4 v[4];
+        for (int s0 = 0; s0 < ns; s0 += kCombineBatch) {
+            // a batch of segments in flight: all loads first, then the sums
+            float l[kCombineBatch];
+            float4 v[kCombineBatch];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float l = ls[s + k];
-                w[k] = l == -INFINITY ? 0.f : expf(l - mx);
-                v[k] = *reinterpret_cast<const float4 *>(po + (int64_t)(s + k) * D);
+            for (int k = 0; k < kCombineBatch; ++k) {
+                const bool in = s0 + k < ns;
+                l[k] = in ? ls[s0 + k] : -INFINITY;
+                v[k] = in ? *reinterpret_cast<const float4 *>(po + (int64_t)(s0 + k) * D)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < kCombineBatch; ++k) {
                 // an empty segment wrote only its lse: its O slot is never read
-                if (w[k] == 0.f) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                wsum += w[k];
-                acc.x += w[k] * v[k].x;
-                acc.y += w[k] * v[k].y;
-                acc.z += w[k] * v[k].z;
-                acc.w += w[k] * v[k].w;
+                const float w = l[k] == -INFINITY ? 0.f : expf(l[k] - mx);
+                if (w == 0.f) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                wsum += w;
+                acc.x += w * v[k].x;
+                acc.y += w * v[k].y;
+                acc.z += w * v[k].z;
+                acc.w += w * v[k].w;
             }
-        }
-        for (; s < ns; ++s) {
-            const float l = ls[s];
-            if (l == -INFINITY) continue;
-            const float w = expf(l - mx);
-            const float4 v = *reinterpret_cast<const float4 *>(po + (int64_t)s * D);
-            wsum += w;
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -214,16 +210,17 @@ cudaError_t launch_combine(const CombineParams &p, int out_dtype, cudaStream_t s
     const int64_t threads = (int64_t)p.T * p.Hq * 32;
     if (threads == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((threads + 127) / 128);
-    if (out_dtype == DT_BF16) combine_kernel<__nv_bfloat16><<<blocks, 128, 0, stream>>>(p);
-    else if (out_dtype == DT_FP16) combine_kernel<__half><<<blocks, 128, 0, stream>>>(p);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    if (out_dtype == DT_BF16) return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(128), 0, stream, p);
+    if (out_dtype == DT_FP16) return launch_pdl(combine_kernel<__half>, dim3(blocks), dim3(128), 0, stream, p);
+    return cudaErrorInvalidValue;
 }
 
 // merge_attn_states: two states per (token, head), one warp each
 template <class T>
 __global__ void __launch_bounds__(128) merge_kernel(T *out, float *lse_out, const T *o1, const float *lse1,
                                                     const T *o2, const float *lse2, int T_, int Hq, int D) {
+    pdl_wait();
+    pdl_trigger();
     const int warp_global = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (warp_global >= T_ * Hq) return;
@@ -257,15 +254,13 @@ cudaError_t launch_merge(void *out, float *lse_out, const void *o1, const float 
     if (threads == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((threads + 127) / 128);
 #define MRG(TYPE)                                                                                              \
-    merge_kernel<TYPE><<<blocks, 128, 0, stream>>>(reinterpret_cast<TYPE *>(out), lse_out,                     \
-                                                   reinterpret_cast<const TYPE *>(o1), lse1,                   \
-                                                   reinterpret_cast<const TYPE *>(o2), lse2, T, Hq, D)
-    if (dtype == DT_BF16) MRG(__nv_bfloat16);
-    else if (dtype == DT_FP16) MRG(__half);
-    else if (dtype == DT_FP32) MRG(float);
-    else return cudaErrorInvalidValue;
+    launch_pdl(merge_kernel<TYPE>, dim3(blocks), dim3(128), 0, stream, reinterpret_cast<TYPE *>(out), lse_out,  \
+               reinterpret_cast<const TYPE *>(o1), lse1, reinterpret_cast<const TYPE *>(o2), lse2, T, Hq, D)
+    if (dtype == DT_BF16) return MRG(__nv_bfloat16);
+    if (dtype == DT_FP16) return MRG(__half);
+    if (dtype == DT_FP32) return MRG(float);
 #undef MRG
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace attn

@@ -21,6 +21,9 @@
 // that need it (sec. 4), and the softmax is the online recurrence of sec. 7.
 // With WN > 1 the warps split each K/V tile's keys (flash-decoding inside
 // the CTA) and merge their states through shared memory at the end; with
+// WN = 4 (decode shapes) each warp also fetches exactly its own keys, so the
+// warps stream their slices independently, synchronising only at the start
+// (Q) and at the end (the merge); with
 // nsplit > 1 each CTA writes a normalised partial state that the combine
 // kernel merges by log-sum-exp (sec. 12).
 #include "common.cuh"
@@ -49,6 +52,10 @@ struct MmaCfg {
     static constexpr int KT = D / 16;                    // k16 steps of Q K^T
     static constexpr int RPW = BN / 4;                   // K/V rows each warp fetches
     static constexpr int CH = KV_ROW / 16;               // 16-byte chunks per cached row
+    // One row block of 16 rows: warp w fetches K/V rows [16w, 16w + 16) of
+    // every tile and is also the only warp that reads them (its key slice),
+    // so the main loop needs no CTA-wide barrier.
+    static constexpr bool WARP_LOCAL = (WM == 1 && RPW == NW);
     static_assert(WM * WN == 4, "4 warps");
     static_assert(NT % 2 == 0, "n-tile pairs");
     static_assert((RPW * CH) % 32 == 0, "whole warp copy rounds");
@@ -61,6 +68,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     uint8_t *sQ = smem;
     uint8_t *sMain = smem + C::Q_BYTES;
 
+    pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wm = warp % C::WM, wn = warp / C::WM;
     const int r = blockIdx.z, kvh = blockIdx.y;
@@ -131,6 +139,10 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         *reinterpret_cast<int4 *>(sQ + swz(lr, ch, C::ROW16)) = v;
     }
 
+    // e4m3 tiles hold value * 2^-8 (see e4m3x4_to_h2x2_lo8): scale S and O back
+    const float sl2 = (C::KVT == DT_E4M3) ? p.scale_log2 * kE4m3Lo8Scale : p.scale_log2;
+    const float vds = (C::KVT == DT_E4M3) ? p.v_descale * kE4m3Lo8Scale : p.v_descale;
+
     // ---- K/V tile gather through the block table
     const int64_t bt_base = (int64_t)r * p.bt_stride;
     const uint8_t *kbase = reinterpret_cast<const uint8_t *>(p.k_cache);
@@ -168,28 +180,31 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         }
     };
 
-    // e4m3 tiles are widened to fp16 (exact) into a swizzled tile for ldmatrix
+    // e4m3 tiles are widened to fp16 (exact) into a swizzled tile for
+    // ldmatrix.  Warp-local mode: each warp widens only its own rows.
     uint8_t *cK = sMain + STAGES * C::STAGE_BYTES;
     uint8_t *cV = cK + C::TILE16;
     auto convert_tile = [&](int stage) {
         const uint8_t *sK = sMain + stage * C::STAGE_BYTES;
         const uint8_t *sV = sK + C::TILE_RAW;
-        for (int c = tid; c < BN * D / 16; c += blockDim.x) {
-            const int row = c / (D / 16), ch = c % (D / 16);
+        constexpr int kChunks = (C::WARP_LOCAL ? C::RPW : BN) * (D / 16);
+        const int c0 = C::WARP_LOCAL ? lane : tid;
+        const int cstep = C::WARP_LOCAL ? 32 : (int)blockDim.x;
+        const int rbase = C::WARP_LOCAL ? warp * C::RPW : 0;
+        for (int c = c0; c < kChunks; c += cstep) {
+            const int row = rbase + c / (D / 16), ch = c % (D / 16);
             const int4 rk = *reinterpret_cast<const int4 *>(sK + row * D + ch * 16);
             const int4 rv = *reinterpret_cast<const int4 *>(sV + row * D + ch * 16);
-            const uint16_t *bk = reinterpret_cast<const uint16_t *>(&rk);
-            const uint16_t *bv = reinterpret_cast<const uint16_t *>(&rv);
+            // fp16 patterns of value * 2^-8 (the 2^8 is in the scales)
             int4 k0, k1, v0, v1;
-            uint32_t *uk0 = reinterpret_cast<uint32_t *>(&k0), *uk1 = reinterpret_cast<uint32_t *>(&k1);
-            uint32_t *uv0 = reinterpret_cast<uint32_t *>(&v0), *uv1 = reinterpret_cast<uint32_t *>(&v1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uk0[k] = e4m3x2_to_h2(bk[k]);
-                uk1[k] = e4m3x2_to_h2(bk[k + 4]);
-                uv0[k] = e4m3x2_to_h2(bv[k]);
-                uv1[k] = e4m3x2_to_h2(bv[k + 4]);
-            }
+            e4m3x4_to_h2x2_lo8((uint32_t)rk.x, reinterpret_cast<uint32_t &>(k0.x), reinterpret_cast<uint32_t &>(k0.y));
+            e4m3x4_to_h2x2_lo8((uint32_t)rk.y, reinterpret_cast<uint32_t &>(k0.z), reinterpret_cast<uint32_t &>(k0.w));
+            e4m3x4_to_h2x2_lo8((uint32_t)rk.z, reinterpret_cast<uint32_t &>(k1.x), reinterpret_cast<uint32_t &>(k1.y));
+            e4m3x4_to_h2x2_lo8((uint32_t)rk.w, reinterpret_cast<uint32_t &>(k1.z), reinterpret_cast<uint32_t &>(k1.w));
+            e4m3x4_to_h2x2_lo8((uint32_t)rv.x, reinterpret_cast<uint32_t &>(v0.x), reinterpret_cast<uint32_t &>(v0.y));
+            e4m3x4_to_h2x2_lo8((uint32_t)rv.y, reinterpret_cast<uint32_t &>(v0.z), reinterpret_cast<uint32_t &>(v0.w));
+            e4m3x4_to_h2x2_lo8((uint32_t)rv.z, reinterpret_cast<uint32_t &>(v1.x), reinterpret_cast<uint32_t &>(v1.y));
+            e4m3x4_to_h2x2_lo8((uint32_t)rv.w, reinterpret_cast<uint32_t &>(v1.z), reinterpret_cast<uint32_t &>(v1.w));
             *reinterpret_cast<int4 *>(cK + swz(row, 2 * ch, C::ROW16)) = k0;
             *reinterpret_cast<int4 *>(cK + swz(row, 2 * ch + 1, C::ROW16)) = k1;
             *reinterpret_cast<int4 *>(cV + swz(row, 2 * ch, C::ROW16)) = v0;
@@ -227,7 +242,9 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
 
     for (int t = 0; t < n_tiles; ++t) {
         cp_async_wait<STAGES - 2>();
-        __syncthreads();
+        // warp-local mode: the stage and the widened rows this warp reads
+        // were written by this warp alone
+        if constexpr (C::WARP_LOCAL) __syncwarp(); else __syncthreads();
         {
             const int tn = t + STAGES - 1;
             if (tn < n_tiles) load_tile(tn, tn % STAGES);
@@ -236,7 +253,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         const uint8_t *tK, *tV;
         if constexpr (C::KVT == DT_E4M3) {
             convert_tile(t % STAGES);
-            __syncthreads();
+            if constexpr (C::WARP_LOCAL) __syncwarp(); else __syncthreads();
             tK = cK;
             tV = cV;
         } else {
@@ -270,7 +287,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         for (int nt = 0; nt < C::NT; ++nt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float v = s[nt][e] * p.scale_log2;
+                float v = s[nt][e] * sl2;
                 if (need_mask) {
                     const int key = n0 + wn * C::NW + nt * 8 + 2 * (lane & 3) + (e & 1);
                     const int lim = (e >> 1) ? lim1 : lim0;
@@ -338,6 +355,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
             }
         }
     }
+    pdl_trigger();     // the next kernel may be scheduled; it waits for this grid's completion
     cp_async_wait<0>();
     __syncthreads();   // all shared-memory tiles consumed; reuse for the epilogue
 
@@ -389,7 +407,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
                 acc.w += sc * v.w;
             }
         }
-        const float inv = lf > 0.f ? p.v_descale / lf : 0.f;
+        const float inv = lf > 0.f ? vds / lf : 0.f;
         acc.x *= inv;
         acc.y *= inv;
         acc.z *= inv;
@@ -424,8 +442,7 @@ static cudaError_t launch_cfg(const FwdParams &p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.n_row_blocks * p.nsplit), (unsigned)p.Hkv, (unsigned)p.B);
-    kern<<<grid, 128, C::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(128), C::SMEM, stream, p);
 }
 
 template <int D, int QT, int KVT>

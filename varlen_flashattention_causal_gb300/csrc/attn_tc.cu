@@ -3,15 +3,28 @@
 //
 // This kernel takes the rows-heavy side of the hot path: prefill and
 // chunked prefill, where S = Q K^T and O = P V are genuine dense
-// contractions.  One CTA owns one request x one KV head x 256 packed query
-// rows (two 128-row Q tiles; a row is a (query token, head-in-group) pair,
-// so each K/V tile serves all G query heads of its group) x one KV segment.
+// contractions.  A work item is one request x one KV head x 256 packed
+// query rows (two 128-row Q tiles; a row is a (query token, head-in-group)
+// pair, so each K/V tile serves all G query heads of its group) x one KV
+// segment.
 //
-// Roles (10 warps):
-//   warp 0      TMA producer: Q once, then K_j and V_j tiles of 64 keys,
-//               each gathered page by page through the block table ("vLLM 中
-//               Attention Kernel 如何并行处理多个请求", sec. 11) into a ring of
-//               ten 16 KB shared-memory slots (five tiles of look-ahead)
+// The kernel is persistent: one CTA per SM draws work items of its class
+// from a ticket counter until none is left.  Items are numbered request by
+// request (within a request: KV head, then row block from the last -- the
+// most keys under the causal mask -- to the first, then segment).  Requests
+// outside the class cost one step of a scan, not CTA launches, which
+// matters in batches that mix a few long prefill chunks with many decode
+// rows.  TMEM, the barriers and the pipeline state persist across items, so
+// the next item's Q and K/V loads overlap the current item's last tiles
+// and epilogue.
+//
+// Roles (11 warps, 13 with e4m3 caches):
+//   warp 0      scheduler and TMA producer: finds the CTA's next item,
+//               publishes it in a two-entry ring in shared memory, then
+//               loads Q once per item and the K_j and V_j tiles of 64 keys,
+//               each gathered page by page through the block table ("vLLM
+//               中 Attention Kernel 如何并行处理多个请求", sec. 11) into a
+//               ring of ten 16 KB shared-memory slots
 //   warp 1      MMA issuer of Q tile A (one thread) and TMEM owner
 //   warp 10     MMA issuer of Q tile B (one thread)
 //               Per K/V tile j each issuer X runs S_X(j) = Q_X K_j^T, then
@@ -19,9 +32,13 @@
 //               a single thread spends tens of cycles per MMA, commit and
 //               barrier wait, and with one issuer those stalls show up as
 //               idle tensor cycles.  The two chains touch disjoint TMEM
-//               columns; a K/V slot is released when both have consumed it.
+//               columns; a K/V slot is released when both have passed it.
+//               An issuer whose Q tile is empty in an item (fewer than 129
+//               rows) still waits for every slot of the item and releases it.
 //   warps 2-5   softmax warpgroup of Q tile A, one thread per row
 //   warps 6-9   softmax warpgroup of Q tile B
+//   warps 11-12 (e4m3 caches only) converters: Q to fp16 in place, then
+//               every staged e4m3 tile to fp16 in a ring slot
 // TMEM columns: S_A double buffer [0,64) [64,128), S_B [128,192) [192,256),
 // O_A [256,384), O_B [384,512).  P_X(j) (bf16/fp16, two per column) is
 // written over the first 32 columns of the S buffer it was computed from and
@@ -29,7 +46,14 @@
 // shared memory by the tensor core, which keeps shared-memory bandwidth
 // below the MMA rate.  S_X(j+2) reuses the buffer of P_X(j) only after
 // O_X += P_X(j) V has been issued, and tcgen05 MMAs of one thread run in
-// order.
+// order.  The first O_X += P V of an item overwrites O_X only after the
+// softmax warpgroup has read out the previous item's O_X.
+//
+// Every barrier phase is counted across items (load index L over all K/V
+// loads of the CTA, tile index per chain, item index), so a parity wait
+// never runs two phases behind or ahead: each waiter passes every phase of
+// its barriers in order, and the phase after next needs the waiter's own
+// release.
 //
 // Softmax (sec. 7): each thread reads its row of S from TMEM, masks it in
 // registers from local positions with the bottom-right alignment of
@@ -41,6 +65,9 @@
 #include "common.cuh"
 #include "sm100.cuh"
 #include "tma_host.h"
+
+#include <algorithm>
+#include <atomic>
 
 namespace attn {
 
@@ -56,27 +83,30 @@ constexpr uint32_t kQHalf = kBM * 128;                 // 64 columns of a Q tile
 constexpr uint32_t kTileBytes = kBN * kD * 2;          // one 16-bit K or V tile, 16 KB
 constexpr uint32_t kKVHalf = kBN * 128;                // 64 columns of a K/V tile
 constexpr uint32_t kStageBytes = kBN * kD;             // one e4m3 K or V tile, 8 KB
+constexpr int kConvChunks = kBN * kD / 16 / 64;        // 16-byte chunks of a staged tile per converter thread
 constexpr float kRescaleThreshold = 8.0f;              // log2 units
 
 // Shared memory map (offsets from a 1024-aligned base).  16-bit caches:
 // Q_A, Q_B, then a ring of ten 16 KB K/V slots the TMA fills directly.
-// e4m3 caches: Q_A, Q_B, a ring of eight 16 KB fp16 slots, and a ring of
-// four 8 KB staging slots the TMA fills with e4m3 pages; two converter
+// e4m3 caches: Q_A, Q_B, a ring of seven 16 KB fp16 slots, and a ring of
+// six 8 KB staging slots the TMA fills with e4m3 pages; two converter
 // warps widen each staged tile into the fp16 ring (exact: every e4m3
-// value is an fp16 value).
+// value is an fp16 value).  The misc area holds the abort flag, the TMEM
+// address and the two-entry work-item ring.
 template <bool FP8>
 struct TcLayout {
-    static constexpr int kSlots = FP8 ? 8 : 10;
-    static constexpr int kStages = FP8 ? 4 : 0;
+    static constexpr int kSlots = FP8 ? 7 : 10;
+    static constexpr int kStages = FP8 ? 6 : 0;
     static constexpr int kThreads = FP8 ? 416 : 352;
+    static constexpr int kConsumerWarps = kThreads / 32 - 1;   // every warp but the producer
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffKV = kOffQ + 2 * kQBytes;
     static constexpr uint32_t kOffStage = kOffKV + kSlots * kTileBytes;
     static constexpr uint32_t kOffBar = kOffStage + kStages * kStageBytes;
-    static constexpr int kNumBars = 16 + 2 * kSlots + 2 * kStages;
-    static constexpr uint32_t kOffMisc = kOffBar + 8 * 48;
-    static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;   // + alignment slack
-    static_assert(kNumBars <= 48, "barrier area");
+    static constexpr int kNumBars = 23 + 2 * kSlots + 2 * kStages;
+    static constexpr uint32_t kOffMisc = kOffBar + 8 * 64;
+    static constexpr uint32_t kSmemBytes = kOffMisc + 128 + 1024;   // + alignment slack
+    static_assert(kNumBars <= 64, "barrier area");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -84,12 +114,41 @@ struct TcLayout {
 __device__ __forceinline__ uint32_t col_s(int x, int b) { return (uint32_t)x * 128u + (uint32_t)b * 64u; }
 __device__ __forceinline__ uint32_t col_o(int x) { return 256u + (uint32_t)x * 128u; }
 
+// One work item and the quantities every role derives from it.
+struct Item {
+    int r, kvh, rb, s;              // request, KV head, row block (256 packed rows), KV segment
+    int q_start, q_len, kv_len;
+    int row0, row_end, ntiles_q;    // packed rows [row0, row_end), 1 or 2 active Q tiles
+    int ctx, kv_lo, kv_hi, n_kv;    // keys [kv_lo, kv_hi) in n_kv tiles
+};
+
+__device__ __forceinline__ void derive(const FwdParams &p, Item &it) {
+    const int rows = it.q_len * p.G;
+    it.row0 = it.rb * 2 * kBM;
+    it.row_end = min(it.row0 + 2 * kBM, rows);
+    it.ntiles_q = (it.row_end - it.row0 + kBM - 1) / kBM;
+    it.ctx = it.kv_len - it.q_len;
+    const int i_max = (it.row_end - 1) / p.G;
+    int kv_end = it.kv_len;
+    if (p.causal) kv_end = min(it.kv_len, it.ctx + i_max + 1);
+    it.kv_lo = it.s * p.split_chunk;
+    it.kv_hi = min(kv_end, it.kv_lo + p.split_chunk);
+    it.n_kv = it.kv_hi > it.kv_lo ? (it.kv_hi - it.kv_lo + kBN - 1) / kBN : 0;
+}
+
 }  // namespace
 
 struct TcParams {
     FwdParams f;
-    int kv_rows;        // rows per TMA page load: gcd(block_size, 64)
+    int kv_rows;                  // rows per TMA page load: gcd(block_size, 64)
+    unsigned long long *sched;    // {next ticket, CTAs done} of this launch's schedule slot
 };
+
+// Ticket counters of the persistent schedule.  Each launch takes the next
+// slot of its device in turn; the slot's counters are zero when a launch
+// starts because the previous launch on it rewound them as it finished.
+constexpr int kSchedSlots = 64;
+__device__ unsigned long long g_tc_sched[kSchedSlots][2];
 
 // whole-warp wait: lane 0 polls, the result is broadcast, so every lane
 // takes the same path into the warp-collective tcgen05 instructions after it
@@ -115,67 +174,32 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t *sm = smem_raw + (sbase - raw);
     auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
-    constexpr int B_Q = 0;
+    constexpr int B_Q = 0;                                   // Q tiles landed, one phase per item with keys
     auto B_FULL = [](int s) { return 1 + s; };
     auto B_EMPTY = [](int s) { return 1 + kSlots + s; };
+    constexpr int kB = 1 + 2 * kSlots;
     // S_X, P_X and "O_X += P_X V done" barriers exist per TMEM buffer
-    // b = j & 1.  A parity wait is only sound if the barrier is neither two
-    // phases ahead of nor two phases behind the phase waited for; per buffer,
-    // the next phase always needs work the waiter has not released yet, and
-    // the previous one is implied by S_X(j) having landed (one issuer's MMAs
-    // complete in order).
-    auto B_SFULL = [](int x, int b) { return 1 + 2 * kSlots + 2 * x + b; };
-    auto B_PFULL = [](int x, int b) { return 5 + 2 * kSlots + 2 * x + b; };
-    auto B_ODONE = [](int x, int b) { return 9 + 2 * kSlots + 2 * x + b; };
-    auto B_DRAIN = [](int x) { return 13 + 2 * kSlots + x; };
-    // e4m3 mode: staging ring (TMA -> converters) and "Q is fp16" barriers
-    auto B_STFULL = [](int t) { return 15 + 2 * kSlots + t; };
-    auto B_STEMPTY = [](int t) { return 15 + 2 * kSlots + kStages + t; };
-    constexpr int B_QREADY = 15 + 2 * kSlots + 2 * kStages;
+    // b = (chain tile index) & 1.  Per buffer, the next phase always needs
+    // work the waiter has not released yet, and the previous one is implied
+    // by S_X(j) having landed (one issuer's MMAs complete in order).
+    auto B_SFULL = [](int x, int b) { return kB + 2 * x + b; };
+    auto B_PFULL = [](int x, int b) { return kB + 4 + 2 * x + b; };
+    auto B_ODONE = [](int x, int b) { return kB + 8 + 2 * x + b; };
+    auto B_DRAIN = [](int x) { return kB + 12 + x; };
+    auto B_OFREE = [](int x) { return kB + 14 + x; };        // softmax X has read O_X out
+    constexpr int B_QFREE = kB + 16;                         // both chains are done with the Q tiles
+    auto B_ITEMF = [](int i) { return kB + 17 + i; };        // ring entry i written
+    auto B_ITEME = [](int i) { return kB + 19 + i; };        // ring entry i read by every consumer warp
+    constexpr int B_QREADY = kB + 21;                        // e4m3 mode: Q converted to fp16
+    auto B_STFULL = [](int t) { return kB + 22 + t; };       // e4m3 staging ring
+    auto B_STEMPTY = [](int t) { return kB + 22 + kStages + t; };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc);
     uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc + 8);
     volatile int *never = reinterpret_cast<volatile int *>(sm + kOffMisc + 16);
+    volatile int *ring = reinterpret_cast<volatile int *>(sm + kOffMisc + 32);   // 2 entries x 8 ints
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = blockIdx.z, kvh = blockIdx.y;
-    const int s_idx = blockIdx.x % p.nsplit;
-    const int rb = p.n_row_blocks - 1 - (int)(blockIdx.x / p.nsplit);
-
-    // ---- per-CTA work (uniform over the CTA)
-    const int q_start = p.cu_seqlens_q[r];
-    const int q_len = p.cu_seqlens_q[r + 1] - q_start;
-    const int kv_len = p.seqused_k[r];
     const int G = p.G;
-    const int rows = q_len * G;
-    if (rows < p.rows_lo || rows > p.rows_hi) return;
-    const int row0 = rb * 2 * kBM;
-    if (row0 >= rows) return;
-    const int row_end = min(row0 + 2 * kBM, rows);
-    const int ntiles_q = (row_end - row0 + kBM - 1) / kBM;   // 1 or 2 active Q tiles
-    const int ctx = kv_len - q_len;
-    const int i_max = (row_end - 1) / G;
-    int kv_end = kv_len;
-    if (p.causal) kv_end = min(kv_len, ctx + i_max + 1);
-    const int kv_lo = s_idx * p.split_chunk;
-    const int kv_hi = min(kv_end, kv_lo + p.split_chunk);
-    const int n_kv = kv_hi > kv_lo ? (kv_hi - kv_lo + kBN - 1) / kBN : 0;
-
-    if (n_kv == 0) {
-        // no key for any row in this segment: empty state, no TMEM taken
-        for (int pr = row0 + tid; pr < row_end; pr += blockDim.x) {
-            const int64_t tok = q_start + pr / G;
-            const int h = kvh * G + pr % G;
-            if (p.nsplit > 1) {
-                p.part_lse[(tok * p.Hq + h) * p.part_stride + s_idx] = -INFINITY;
-            } else {
-                if (p.lse) p.lse[tok * p.Hq + h] = -INFINITY;
-                uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
-                                                     (tok * p.out_stride + (int64_t)h * kD) * 2);
-                for (int c = 0; c < kD / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        return;
-    }
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -183,7 +207,7 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
         mbar_init(bar(B_Q), 1);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(bar(B_FULL(s)), FP8 ? 2u : 1u);          // TMA bytes, or the two converter warps
-            mbar_init(bar(B_EMPTY(s)), (uint32_t)ntiles_q);   // one release per active Q tile
+            mbar_init(bar(B_EMPTY(s)), 2u);                    // one release per chain
         }
         for (int t = 0; t < kStages; ++t) {
             mbar_init(bar(B_STFULL(t)), 1);
@@ -197,9 +221,14 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
             mbar_init(bar(B_PFULL(x, 1)), 4);
             mbar_init(bar(B_ODONE(x, 0)), 1);
             mbar_init(bar(B_ODONE(x, 1)), 1);
+            mbar_init(bar(B_DRAIN(x)), 1);
+            mbar_init(bar(B_OFREE(x)), 4);
         }
-        mbar_init(bar(B_DRAIN(0)), 1);
-        mbar_init(bar(B_DRAIN(1)), 1);
+        mbar_init(bar(B_QFREE), 2);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_ITEMF(i)), 1);
+            mbar_init(bar(B_ITEME(i)), (uint32_t)Lay::kConsumerWarps);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -210,83 +239,196 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *taddr_slot;
+    // set-up above touched no global memory; the inputs (and the ticket
+    // counter) are used only once the previous kernel has completed
+    pdl_wait();
+
+    // consumer warps: take item k from the ring; false on abort, it.r < 0
+    // ends the walk
+    auto read_item = [&](int k, Item &it) -> bool {
+        if (!warp_wait(bar(B_ITEMF(k & 1)), (k >> 1) & 1, abort_flag)) return false;
+        __syncwarp();
+        const volatile int *e = ring + (k & 1) * 8;
+        it.r = e[0];
+        it.kvh = e[1];
+        it.rb = e[2];
+        it.s = e[3];
+        it.q_start = e[4];
+        it.q_len = e[5];
+        it.kv_len = e[6];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_ITEME(k & 1)));
+        if (it.r >= 0) derive(p, it);
+        return true;
+    };
 
     if (warp == 0) {
-        // =================================================== TMA producer
+        // ======================================= scheduler and TMA producer
         const int R = tp.kv_rows;
         const int pages = kBN / R;               // page loads per tile (1..4)
-        const int64_t bt_base = (int64_t)r * p.bt_stride;
-        int issued = -1;                         // last K/V load index issued
+        // Dynamic schedule: the first item of CTA c is item c, every later
+        // one a ticket P + n drawn from the launch's counter, so a CTA that
+        // drew long items takes fewer.  Tickets of one CTA only grow, which
+        // lets the request scan below move forward only: requests are
+        // scanned 32 at a time (one per lane), sc_incl being the inclusive
+        // prefix of the item counts in the chunk.
+        const long long P = gridDim.x;
+        int sc_chunk = -32;
+        long long sc_base = 0, sc_total = 0, sc_incl = 0, sc_cnt = 0;
+        int sc_q0 = 0, sc_ql = 0, sc_kv = 0, sc_nrb = 0;
+        int npipe = 0;                           // items with keys published so far
+        int Lbase = 0;                           // K/V loads of earlier items
+        int issued = -1;                         // last load index issued
+        bool ok = true;
         if (lane == 0) {
             tma_prefetch(&qmap);
             tma_prefetch(&kmap);
             tma_prefetch(&vmap);
-            mbar_expect_tx(bar(B_Q), (uint32_t)ntiles_q * kQBytes);
-            const int tok0 = q_start + row0 / G;
-            const int toks_per_tile = kBM / G;
-            for (int x = 0; x < ntiles_q; ++x)
-                for (int h = 0; h < 2; ++h)
-                    tma_load_3d(sbase + kOffQ + x * kQBytes + h * kQHalf, &qmap, h * 64, kvh * G,
-                                tok0 + x * toks_per_tile, bar(B_Q));
         }
-        // Page coordinates are read from the block table 32 pages at a time
-        // (one per lane) and the next batch is requested a whole batch ahead,
-        // so the table's load latency never sits between two tiles.
-        const int total_pages = n_kv * pages;
-        auto page_coord = [&](int g) -> int {       // row of page g in the cache, -1 if absent
-            if (g >= total_pages) return -1;
-            const int tok = kv_lo + g * R;
-            if (tok >= kv_hi) return -1;
-            int blk = p.block_table[bt_base + tok / p.bs];
-            if ((unsigned)blk >= (unsigned)p.num_blocks) {
-                raise_error(p.err, ERR_BLOCK_ID);
-                blk = 0;                             // never dereference an id outside the pool
+        for (int k = 0; ok; ++k) {
+            // ---- item k of this CTA
+            long long v = blockIdx.x;
+            if (k > 0) {
+                unsigned long long t = 0;
+                if (lane == 0) t = atomicAdd(tp.sched, 1ull);
+                v = P + (long long)__shfl_sync(0xffffffffu, t, 0);
             }
-            return blk * p.bs + tok % p.bs;
-        };
-        int batch = 0;                               // pages [batch, batch + 32) are in cur
-        int cur = page_coord(lane);
-        int nxt = page_coord(32 + lane);
-        for (int j = 0; j < n_kv; ++j) {
-            const int g0 = j * pages;
-            if (g0 >= batch + 32) {
-                batch += 32;
-                cur = nxt;
-                nxt = page_coord(batch + 32 + lane);
-            }
-            // lane pp < pages takes page g0 + pp of this tile (a tile never straddles a batch: 32 % pages == 0)
-            const int coord = __shfl_sync(0xffffffffu, cur, (g0 - batch + (lane < pages ? lane : 0)) & 31);
-            const int mine = lane < pages ? coord : -1;
-            const int nvalid = __popc(__ballot_sync(0xffffffffu, mine >= 0));
-            bool ok = true;
-            for (int kv = 0; kv < 2 && ok; ++kv) {
-                const int L = 2 * j + kv;        // load index
-                const CUtensorMap *m = kv ? &vmap : &kmap;
-                if constexpr (FP8) {
-                    // e4m3 pages -> staging slot (one 128-byte row per key, no swizzle)
-                    const int st = L % kStages;
-                    if (L >= kStages) ok = warp_wait(bar(B_STEMPTY(st)), ((L / kStages) - 1) & 1, abort_flag);
-                    if (!ok) break;
-                    if (lane == 0) mbar_expect_tx(bar(B_STFULL(st)), (uint32_t)nvalid * R * kD);
-                    __syncwarp();
-                    if (mine >= 0)
-                        tma_load_3d(sbase + kOffStage + st * kStageBytes + lane * R * 128, m, 0, kvh, mine,
-                                    bar(B_STFULL(st)));
-                } else {
-                    const int slot = L % kSlots;
-                    if (L >= kSlots) ok = warp_wait(bar(B_EMPTY(slot)), ((L / kSlots) - 1) & 1, abort_flag);
-                    if (!ok) break;
-                    if (lane == 0) mbar_expect_tx(bar(B_FULL(slot)), (uint32_t)nvalid * R * kD * 2);
-                    __syncwarp();
-                    if (mine >= 0) {
-                        const uint32_t dst = sbase + kOffKV + slot * kTileBytes + lane * R * 128;
-                        tma_load_3d(dst, m, 0, kvh, mine, bar(B_FULL(slot)));
-                        tma_load_3d(dst + kKVHalf, m, 64, kvh, mine, bar(B_FULL(slot)));
+            while (sc_chunk < p.B && v >= sc_base + sc_total) {
+                sc_base += sc_total;
+                sc_chunk += 32;
+                const int r = sc_chunk + lane;
+                sc_cnt = 0;
+                sc_nrb = 0;
+                if (r < p.B) {
+                    sc_q0 = p.cu_seqlens_q ? p.cu_seqlens_q[r] : r;
+                    sc_ql = (p.cu_seqlens_q ? p.cu_seqlens_q[r + 1] : r + 1) - sc_q0;
+                    sc_kv = p.seqused_k[r];
+                    const int rows = sc_ql * G;
+                    if (rows > 0 && rows >= p.rows_lo && rows <= p.rows_hi) {
+                        sc_nrb = (rows + 2 * kBM - 1) / (2 * kBM);
+                        sc_cnt = (long long)sc_nrb * p.Hkv * p.nsplit;
                     }
                 }
-                issued = L;
+                sc_incl = sc_cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long t = __shfl_up_sync(0xffffffffu, sc_incl, o);
+                    if (lane >= o) sc_incl += t;
+                }
+                sc_total = __shfl_sync(0xffffffffu, sc_incl, 31);
             }
+            Item it{};
+            it.r = -1;
+            if (v < sc_base + sc_total) {
+                const long long rel = v - sc_base;
+                const int src = __ffs(__ballot_sync(0xffffffffu, sc_incl > rel)) - 1;
+                const long long u =
+                    rel - (__shfl_sync(0xffffffffu, sc_incl, src) - __shfl_sync(0xffffffffu, sc_cnt, src));
+                const int nrb = __shfl_sync(0xffffffffu, sc_nrb, src);
+                it.r = sc_chunk + src;
+                it.q_start = __shfl_sync(0xffffffffu, sc_q0, src);
+                it.q_len = __shfl_sync(0xffffffffu, sc_ql, src);
+                it.kv_len = __shfl_sync(0xffffffffu, sc_kv, src);
+                it.s = (int)(u % p.nsplit);
+                const long long t = u / p.nsplit;
+                it.rb = nrb - 1 - (int)(t % nrb);
+                it.kvh = (int)(t / nrb);
+            }
+            // ---- publish it: entry k & 1 is free once every consumer warp has read item k - 2
+            if (k >= 2) ok = warp_wait(bar(B_ITEME(k & 1)), ((k >> 1) - 1) & 1, abort_flag);
             if (!ok) break;
+            if (lane == 0) {
+                volatile int *e = ring + (k & 1) * 8;
+                e[0] = it.r;
+                e[1] = it.kvh;
+                e[2] = it.rb;
+                e[3] = it.s;
+                e[4] = it.q_start;
+                e[5] = it.q_len;
+                e[6] = it.kv_len;
+                mbar_arrive(bar(B_ITEMF(k & 1)));
+            }
+            __syncwarp();
+            if (it.r < 0) break;
+            derive(p, it);
+            if (it.n_kv == 0) continue;
+
+            // ---- Q tiles, once both chains are done with the previous item's
+            if (npipe > 0) ok = warp_wait(bar(B_QFREE), (npipe - 1) & 1, abort_flag);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_expect_tx(bar(B_Q), (uint32_t)it.ntiles_q * kQBytes);
+                const int tok0 = it.q_start + it.row0 / G;
+                const int toks_per_tile = kBM / G;
+                for (int x = 0; x < it.ntiles_q; ++x)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(sbase + kOffQ + x * kQBytes + h * kQHalf, &qmap, h * 64, it.kvh * G,
+                                    tok0 + x * toks_per_tile, bar(B_Q));
+            }
+            __syncwarp();
+            ++npipe;
+
+            // ---- K/V tiles.  Page coordinates are read from the block table
+            // 32 pages at a time (one per lane) and the next batch is
+            // requested a whole batch ahead, so the table's load latency
+            // never sits between two tiles.
+            const int64_t bt_base = (int64_t)it.r * p.bt_stride;
+            const int total_pages = it.n_kv * pages;
+            const int kv_lo = it.kv_lo, kv_hi = it.kv_hi;
+            auto page_coord = [&](int g) -> int {       // row of page g in the cache, -1 if absent
+                if (g >= total_pages) return -1;
+                const int tok = kv_lo + g * R;
+                if (tok >= kv_hi) return -1;
+                int blk = p.block_table[bt_base + tok / p.bs];
+                if ((unsigned)blk >= (unsigned)p.num_blocks) {
+                    raise_error(p.err, ERR_BLOCK_ID);
+                    blk = 0;                             // never dereference an id outside the pool
+                }
+                return blk * p.bs + tok % p.bs;
+            };
+            int batch = 0;                               // pages [batch, batch + 32) are in cur
+            int cur = page_coord(lane);
+            int nxt = page_coord(32 + lane);
+            for (int j = 0; j < it.n_kv && ok; ++j) {
+                const int g0 = j * pages;
+                if (g0 >= batch + 32) {
+                    batch += 32;
+                    cur = nxt;
+                    nxt = page_coord(batch + 32 + lane);
+                }
+                // lane pp < pages takes page g0 + pp of this tile (a tile never straddles a batch: 32 % pages == 0)
+                const int coord = __shfl_sync(0xffffffffu, cur, (g0 - batch + (lane < pages ? lane : 0)) & 31);
+                const int mine = lane < pages ? coord : -1;
+                const int nvalid = __popc(__ballot_sync(0xffffffffu, mine >= 0));
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const int L = Lbase + 2 * j + kv;    // load index
+                    const CUtensorMap *m = kv ? &vmap : &kmap;
+                    if constexpr (FP8) {
+                        // e4m3 pages -> staging slot (one 128-byte row per key, no swizzle)
+                        const int st = L % kStages;
+                        if (L >= kStages) ok = warp_wait(bar(B_STEMPTY(st)), ((L / kStages) - 1) & 1, abort_flag);
+                        if (!ok) break;
+                        if (lane == 0) mbar_expect_tx(bar(B_STFULL(st)), (uint32_t)nvalid * R * kD);
+                        __syncwarp();
+                        if (mine >= 0)
+                            tma_load_3d(sbase + kOffStage + st * kStageBytes + lane * R * 128, m, 0, it.kvh, mine,
+                                        bar(B_STFULL(st)));
+                    } else {
+                        const int slot = L % kSlots;
+                        if (L >= kSlots) ok = warp_wait(bar(B_EMPTY(slot)), ((L / kSlots) - 1) & 1, abort_flag);
+                        if (!ok) break;
+                        if (lane == 0) mbar_expect_tx(bar(B_FULL(slot)), (uint32_t)nvalid * R * kD * 2);
+                        __syncwarp();
+                        if (mine >= 0) {
+                            const uint32_t dst = sbase + kOffKV + slot * kTileBytes + lane * R * 128;
+                            tma_load_3d(dst, m, 0, it.kvh, mine, bar(B_FULL(slot)));
+                            tma_load_3d(dst + kKVHalf, m, 64, it.kvh, mine, bar(B_FULL(slot)));
+                        }
+                    }
+                    issued = L;
+                }
+            }
+            Lbase += 2 * it.n_kv;
         }
         // drain: every load issued has landed before the CTA exits
         if (lane == 0) {
@@ -297,237 +439,323 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                 for (int L = max(0, issued - kSlots + 1); L <= issued; ++L)
                     mbar_wait(bar(B_FULL(L % kSlots)), (L / kSlots) & 1, never);
             }
-            mbar_wait(bar(B_Q), 0, never);
+            if (npipe > 0) mbar_wait(bar(B_Q), (npipe - 1) & 1, never);
         }
     } else if (warp == 1 || warp == 10) {
         // ================================================ MMA issuers (tile x)
         const int x = warp == 1 ? 0 : 1;
-        if (lane == 0 && x < ntiles_q) {
-            const uint32_t idS = idesc_f16(MMA_BF16, kBM, kBN, false, false);
-            const uint32_t idO = idesc_f16(MMA_BF16, kBM, kD, false, true);
-            // descriptors of every operand base, built once; a K slice or a
-            // ring slot only adds a small offset to the start-address field
-            // (addresses stay below 2^18, so the 14-bit field never carries)
-            const uint64_t dQ = sdesc_sw128(sbase + kOffQ + x * kQBytes, 16, 1024);
-            const uint64_t dK = sdesc_sw128(sbase + kOffKV, 16, 1024);
-            const uint64_t dV = sdesc_sw128(sbase + kOffKV, kKVHalf, 1024);
-            const uint32_t tOx = tmem + col_o(x);
-            bool ok = mbar_wait(bar(FP8 ? B_QREADY : B_Q), 0, abort_flag);
-            for (int j = 0; j <= n_kv && ok; ++j) {
-                const int sk = (2 * j) % kSlots;                  // K_j
-                const int sv = (2 * j + kSlots - 1) % kSlots;     // V_(j-1)
-                if (j < n_kv) {
-                    ok = mbar_wait(bar(B_FULL(sk)), ((2 * j) / kSlots) & 1, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t b0 = dK + ((sk * kTileBytes) >> 4);
-                    const uint32_t d = tmem + col_s(x, j & 1);
-#pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk)
-                        umma_ss(d, dQ + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
-                                b0 + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
-                    umma_commit(bar(B_SFULL(x, j & 1)));
-                    umma_commit(bar(B_EMPTY(sk)));
+        const uint32_t idS = idesc_f16(MMA_BF16, kBM, kBN, false, false);
+        const uint32_t idO = idesc_f16(MMA_BF16, kBM, kD, false, true);
+        // descriptors of every operand base, built once; a K slice or a
+        // ring slot only adds a small offset to the start-address field
+        // (addresses stay below 2^18, so the 14-bit field never carries)
+        const uint64_t dQ = sdesc_sw128(sbase + kOffQ + x * kQBytes, 16, 1024);
+        const uint64_t dK = sdesc_sw128(sbase + kOffKV, 16, 1024);
+        const uint64_t dV = sdesc_sw128(sbase + kOffKV, kKVHalf, 1024);
+        const uint32_t tOx = tmem + col_o(x);
+        int npipe = 0, Lbase = 0;
+        int jx = 0;                              // tiles of this chain in earlier items
+        int ax = 0;                              // earlier items in which this chain had rows
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            Item it;
+            ok = read_item(k, it);
+            if (!ok || it.r < 0) break;
+            if (it.n_kv == 0) continue;
+            const int n_kv = it.n_kv;
+            const bool active = x < it.ntiles_q;
+            if (lane == 0) {
+                ok = mbar_wait(bar(FP8 ? B_QREADY : B_Q), npipe & 1, abort_flag);
+                if (ok && !active) {
+                    // no rows of this chain in the item: release Q and pass
+                    // every slot in order (the other chain's MMAs gate the reuse)
+                    mbar_arrive(bar(B_QFREE));
+                    for (int L = Lbase; L < Lbase + 2 * n_kv && ok; ++L) {
+                        ok = mbar_wait(bar(B_FULL(L % kSlots)), (L / kSlots) & 1, abort_flag);
+                        if (ok) mbar_arrive(bar(B_EMPTY(L % kSlots)));
+                    }
                 }
-                if (j > 0) {
-                    ok = mbar_wait(bar(B_FULL(sv)), ((2 * j - 1) / kSlots) & 1, abort_flag);
-                    if (ok) ok = mbar_wait(bar(B_PFULL(x, (j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // A = P_X from TMEM (8 columns per 16 keys), B = V from shared memory
-                    const uint64_t b0 = dV + ((sv * kTileBytes) >> 4);
-                    const uint32_t a = tmem + col_s(x, (j - 1) & 1);
+                for (int j = 0; active && j <= n_kv && ok; ++j) {
+                    const int LK = Lbase + 2 * j;          // load index of K_j
+                    const int LV = LK - 1;                 // load index of V_(j-1)
+                    const int jg = jx + j;                 // chain tile index of K_j
+                    if (j < n_kv) {
+                        const int sk = LK % kSlots;
+                        ok = mbar_wait(bar(B_FULL(sk)), (LK / kSlots) & 1, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t b0 = dK + ((sk * kTileBytes) >> 4);
+                        const uint32_t d = tmem + col_s(x, jg & 1);
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        umma_ts(tOx, a + kk * 8, b0 + ((kk * 2048) >> 4), idO, (j == 1 && kk == 0) ? 0u : 1u);
-                    umma_commit(bar(B_ODONE(x, (j - 1) & 1)));
-                    umma_commit(bar(B_EMPTY(sv)));
+                        for (int kk = 0; kk < kD / 16; ++kk)
+                            umma_ss(d, dQ + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
+                                    b0 + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
+                        umma_commit(bar(B_SFULL(x, jg & 1)));
+                        umma_commit(bar(B_EMPTY(sk)));
+                        if (j == n_kv - 1) umma_commit(bar(B_QFREE));
+                    }
+                    if (j > 0) {
+                        const int sv = LV % kSlots;
+                        ok = mbar_wait(bar(B_FULL(sv)), (LV / kSlots) & 1, abort_flag);
+                        if (ok) ok = mbar_wait(bar(B_PFULL(x, (jg - 1) & 1)), ((jg - 1) >> 1) & 1, abort_flag);
+                        // the item's first P V overwrites O_X: the previous
+                        // item's epilogue must have read it out
+                        if (ok && j == 1 && ax > 0) ok = mbar_wait(bar(B_OFREE(x)), (ax - 1) & 1, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // A = P_X from TMEM (8 columns per 16 keys), B = V from shared memory
+                        const uint64_t b0 = dV + ((sv * kTileBytes) >> 4);
+                        const uint32_t a = tmem + col_s(x, (jg - 1) & 1);
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            umma_ts(tOx, a + kk * 8, b0 + ((kk * 2048) >> 4), idO, (j == 1 && kk == 0) ? 0u : 1u);
+                        umma_commit(bar(B_ODONE(x, (jg - 1) & 1)));
+                        umma_commit(bar(B_EMPTY(sv)));
+                    }
                 }
             }
-            if (*abort_flag) {
-                // a stalled pipeline: wait (bounded) for the MMAs this thread issued
-                umma_commit(bar(B_DRAIN(x)));
-                mbar_wait(bar(B_DRAIN(x)), 0, never);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            Lbase += 2 * n_kv;
+            ++npipe;
+            if (active) {
+                jx += n_kv;
+                ++ax;
             }
+        }
+        if (lane == 0 && *abort_flag) {
+            // a stalled pipeline: wait (bounded) for the MMAs this thread issued
+            umma_commit(bar(B_DRAIN(x)));
+            mbar_wait(bar(B_DRAIN(x)), 0, never);
         }
     } else if (warp >= 2 && warp <= 9) {
         // ================================================ softmax warpgroups
         const int x = (warp - 2) >> 2;              // Q tile 0 (A) or 1 (B)
         const int quarter = warp & 3;               // TMEM lane quarter this warp may access
         const int trow = quarter * 32 + lane;       // row within the Q tile
-        const int prow = row0 + x * kBM + trow;     // packed row within the request
-        const bool row_ok = prow < row_end;
-        const int qi = prow / G;                    // local query index
-        const int lim = p.causal ? ctx + qi : INT_MAX;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const uint32_t tO = tmem + lane_base + col_o(x);
-        const float sl2 = p.scale_log2;
-        float m_ref = -INFINITY;                    // reference maximum (log2 units)
-        float l = 0.f;
-        bool ok = x < ntiles_q;
-        // query range of this Q tile, for the tile classification
-        const int tq_lo = (row0 + x * kBM) / G;
-        const int tq_hi = (min(row0 + (x + 1) * kBM, row_end) - 1) / G + 1;
-        const int nlim = min(kv_hi - 1, lim);       // last visible key of this row in the segment
-        for (int j = 0; j < n_kv && ok; ++j) {
-            const int n0 = kv_lo + j * kBN;
-            const int b = j & 1;
-            const uint32_t tS = tmem + lane_base + col_s(x, b);
-            const bool need_mask =
-                (n0 + kBN > kv_hi) || (p.causal && tile_kind(tq_lo, tq_hi, n0, n0 + kBN, ctx) != 1);
-            ok = warp_wait(bar(B_SFULL(x, b)), (j >> 1) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t v[kBN];
-            {
-                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-                uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-                tmem_ld32(tS, v0);
-                tmem_ld32(tS + 32, v1);
-                tmem_wait_ld();
-            }
-            // masked keys: this row sees keys n0 .. n0 + nv - 1 of the tile
-            const int nv = need_mask ? max(0, min(kBN, nlim - n0 + 1)) : kBN;
-            float mx8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-            if (nv == kBN) {
-#pragma unroll
-                for (int e = 0; e < kBN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(v[e]));
-            } else {
-#pragma unroll
-                for (int e = 0; e < kBN; ++e) {
-                    const float s = e < nv ? __uint_as_float(v[e]) : -INFINITY;
-                    v[e] = __float_as_uint(s);
-                    mx8[e & 7] = fmaxf(mx8[e & 7], s);
+        // e4m3 tiles hold value * 2^-8 (see e4m3x4_to_h2x2_lo8): scale S and O back
+        const float sl2 = FP8 ? p.scale_log2 * kE4m3Lo8Scale : p.scale_log2;
+        const float vds = FP8 ? p.v_descale * kE4m3Lo8Scale : p.v_descale;
+        int Lbase = 0, jx = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            Item it;
+            ok = read_item(k, it);
+            if (!ok || it.r < 0) break;
+            if (it.n_kv == 0) {
+                // no key for any row in this segment: empty state, no pipeline work
+                for (int pr = it.row0 + (tid - 64); pr < it.row_end; pr += 256) {
+                    const int64_t tok = it.q_start + pr / G;
+                    const int h = it.kvh * G + pr % G;
+                    if (p.nsplit > 1) {
+                        p.part_lse[(tok * p.Hq + h) * p.part_stride + it.s] = -INFINITY;
+                    } else {
+                        if (p.lse) p.lse[tok * p.Hq + h] = -INFINITY;
+                        uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
+                                                             (tok * p.out_stride + (int64_t)h * kD) * 2);
+                        for (int c = 0; c < kD / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+                    }
                 }
+                continue;
             }
-            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            mx *= sl2;
-            // rescale only when the maximum grows past the threshold
-            const bool bump = mx > m_ref + kRescaleThreshold;
-            const bool corr = bump && m_ref != -INFINITY;
-            const float m_new = bump ? mx : m_ref;
-            const float alpha = corr ? ex2(m_ref - m_new) : 1.f;
-            const float base = (m_new == -INFINITY) ? 0.f : m_new;
-            m_ref = m_new;
-            uint32_t pk[32];
-            float rs8[8];
+            const int n_kv = it.n_kv, kv_lo = it.kv_lo, kv_hi = it.kv_hi;
+            if (x < it.ntiles_q) {
+                const int prow = it.row0 + x * kBM + trow;  // packed row within the request
+                const bool row_ok = prow < it.row_end;
+                const int qi = prow / G;                    // local query index
+                const int lim = p.causal ? it.ctx + qi : INT_MAX;
+                float m_ref = -INFINITY;                    // reference maximum (log2 units)
+                float l = 0.f;
+                // query range of this Q tile, for the tile classification
+                const int tq_lo = (it.row0 + x * kBM) / G;
+                const int tq_hi = (min(it.row0 + (x + 1) * kBM, it.row_end) - 1) / G + 1;
+                const int nlim = min(kv_hi - 1, lim);       // last visible key of this row in the segment
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    const int n0 = kv_lo + j * kBN;
+                    const int jg = jx + j;
+                    const int b = jg & 1;
+                    const uint32_t tS = tmem + lane_base + col_s(x, b);
+                    const bool need_mask =
+                        (n0 + kBN > kv_hi) || (p.causal && tile_kind(tq_lo, tq_hi, n0, n0 + kBN, it.ctx) != 1);
+                    ok = warp_wait(bar(B_SFULL(x, b)), (jg >> 1) & 1, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    uint32_t v[kBN];
+                    {
+                        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+                        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+                        tmem_ld32(tS, v0);
+                        tmem_ld32(tS + 32, v1);
+                        tmem_wait_ld();
+                    }
+                    // masked keys: this row sees keys n0 .. n0 + nv - 1 of the tile
+                    const int nv = need_mask ? max(0, min(kBN, nlim - n0 + 1)) : kBN;
+                    float mx8[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
+                    for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+                    if (nv == kBN) {
 #pragma unroll
-            for (int e = 0; e < kBN; e += 2) {
-                const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -base));
-                const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -base));
-                rs8[(e >> 1) & 7] += p0 + p1;
-                pk[e / 2] = pack2<MMA_BF16>(p0, p1);
-            }
-            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-            l = l * alpha + rs;
-            if (__any_sync(0xffffffffu, corr)) {
-                // O_X must hold P_X(j-1) V before it is rescaled
-                ok = warp_wait(bar(B_ODONE(x, (j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
+                        for (int e = 0; e < kBN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(v[e]));
+                    } else {
 #pragma unroll
-                for (int c = 0; c < kD / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(tO + c * 32, o);
-                }
-            }
-            if (n0 + kBN > kv_hi) {
-                // keys past the segment end: their P is exactly 0, but the V
-                // rows there may hold anything (unwritten cache rows, pages
-                // not loaded) -- zero them so 0 * V cannot produce NaN.  Both
-                // warpgroups write the same zeros, each before publishing its
-                // own P, because either issuer may read the tile first.
-                const int Lv = 2 * j + 1, sv = Lv % kSlots;
-                ok = warp_wait(bar(B_FULL(sv)), (Lv / kSlots) & 1, abort_flag);
-                if (!ok) break;
-                if (trow < kBN && trow >= kv_hi - n0) {
-                    uint4 *v0 = reinterpret_cast<uint4 *>(sm + kOffKV + sv * kTileBytes + trow * 128);
-                    uint4 *v1 = reinterpret_cast<uint4 *>(sm + kOffKV + sv * kTileBytes + kKVHalf + trow * 128);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) v0[c] = v1[c] = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
-            // P -> TMEM over the S buffer it came from (columns 0..31)
-            tmem_st32(tS, pk);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PFULL(x, b)));
-        }
-        // ---- epilogue: O / l -> out (or the split partials)
-        if (ok && x < ntiles_q) {
-            // O_X += P_X(n-1) V done implies every earlier P V of this tile is done
-            ok = warp_wait(bar(B_ODONE(x, (n_kv - 1) & 1)), ((n_kv - 1) >> 1) & 1, abort_flag);
-            if (ok) {
-                tc_fence_after();
-                const float inv = l > 0.f ? p.v_descale / l : 0.f;
-                const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-                const int64_t tok = q_start + qi;
-                const int h = kvh * G + prow % G;
-#pragma unroll
-                for (int c = 0; c < kD / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c * 32, o);
-                    tmem_wait_ld();
-                    if (!row_ok) continue;
-                    if (p.nsplit == 1) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
-                                                               (tok * p.out_stride + (int64_t)h * kD + c * 32) * 2);
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 w;
-                            w.x = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
-                            w.y = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
-                            w.z = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
-                            w.w = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-                            dst[q4] = w;
+                        for (int e = 0; e < kBN; ++e) {
+                            const float s = e < nv ? __uint_as_float(v[e]) : -INFINITY;
+                            v[e] = __float_as_uint(s);
+                            mx8[e & 7] = fmaxf(mx8[e & 7], s);
                         }
-                    } else {
-                        float4 *dst = reinterpret_cast<float4 *>(
-                            p.part_o + ((tok * p.Hq + h) * p.part_stride + s_idx) * kD + c * 32);
+                    }
+                    float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                    mx *= sl2;
+                    // rescale only when the maximum grows past the threshold
+                    const bool bump = mx > m_ref + kRescaleThreshold;
+                    const bool corr = bump && m_ref != -INFINITY;
+                    const float m_new = bump ? mx : m_ref;
+                    const float alpha = corr ? ex2(m_ref - m_new) : 1.f;
+                    const float base = (m_new == -INFINITY) ? 0.f : m_new;
+                    m_ref = m_new;
+                    uint32_t pk[32];
+                    float rs8[8];
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4)
-                            dst[q4] = make_float4(__uint_as_float(o[q4 * 4]) * inv, __uint_as_float(o[q4 * 4 + 1]) * inv,
-                                                  __uint_as_float(o[q4 * 4 + 2]) * inv,
-                                                  __uint_as_float(o[q4 * 4 + 3]) * inv);
+                    for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < kBN; e += 2) {
+                        const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -base));
+                        const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -base));
+                        rs8[(e >> 1) & 7] += p0 + p1;
+                        pk[e / 2] = pack2<MMA_BF16>(p0, p1);
                     }
-                }
-                if (row_ok) {
-                    if (p.nsplit == 1) {
-                        if (p.lse) p.lse[tok * p.Hq + h] = lse_v;
-                    } else {
-                        p.part_lse[(tok * p.Hq + h) * p.part_stride + s_idx] = lse_v;
+                    const float rs =
+                        ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                    l = l * alpha + rs;
+                    if (__any_sync(0xffffffffu, corr)) {
+                        // O_X must hold P_X(j-1) V before it is rescaled (corr implies j > 0)
+                        ok = warp_wait(bar(B_ODONE(x, (jg - 1) & 1)), ((jg - 1) >> 1) & 1, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < kD / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tO + c * 32, o);
+                        }
                     }
+                    if (n0 + kBN > kv_hi) {
+                        // keys past the segment end: their P is exactly 0, but the V
+                        // rows there may hold anything (unwritten cache rows, pages
+                        // not loaded) -- zero them so 0 * V cannot produce NaN.  Both
+                        // warpgroups write the same zeros, each before publishing its
+                        // own P, because either issuer may read the tile first.
+                        const int Lv = Lbase + 2 * j + 1, sv = Lv % kSlots;
+                        ok = warp_wait(bar(B_FULL(sv)), (Lv / kSlots) & 1, abort_flag);
+                        if (!ok) break;
+                        __syncwarp();
+                        if (trow < kBN && trow >= kv_hi - n0) {
+                            uint4 *v0 = reinterpret_cast<uint4 *>(sm + kOffKV + sv * kTileBytes + trow * 128);
+                            uint4 *v1 =
+                                reinterpret_cast<uint4 *>(sm + kOffKV + sv * kTileBytes + kKVHalf + trow * 128);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) v0[c] = v1[c] = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    // P -> TMEM over the S buffer it came from (columns 0..31)
+                    tmem_st32(tS, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_PFULL(x, b)));
                 }
+                // ---- epilogue: O / l -> out (or the split partials)
+                if (ok) {
+                    // O_X += P_X(last) V done implies every earlier P V of this item is done
+                    const int jl = jx + n_kv - 1;
+                    ok = warp_wait(bar(B_ODONE(x, jl & 1)), (jl >> 1) & 1, abort_flag);
+                }
+                if (ok) {
+                    tc_fence_after();
+                    const float inv = l > 0.f ? vds / l : 0.f;
+                    const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+                    const int64_t tok = it.q_start + qi;
+                    const int h = it.kvh * G + prow % G;
+#pragma unroll
+                    for (int c = 0; c < kD / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_wait_ld();
+                        if (!row_ok) continue;
+                        if (p.nsplit == 1) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
+                                                                   (tok * p.out_stride + (int64_t)h * kD + c * 32) * 2);
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                uint4 w;
+                                w.x = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 0]) * inv,
+                                                      __uint_as_float(o[q4 * 8 + 1]) * inv);
+                                w.y = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 2]) * inv,
+                                                      __uint_as_float(o[q4 * 8 + 3]) * inv);
+                                w.z = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 4]) * inv,
+                                                      __uint_as_float(o[q4 * 8 + 5]) * inv);
+                                w.w = pack2<OUT_BF16>(__uint_as_float(o[q4 * 8 + 6]) * inv,
+                                                      __uint_as_float(o[q4 * 8 + 7]) * inv);
+                                dst[q4] = w;
+                            }
+                        } else {
+                            float4 *dst = reinterpret_cast<float4 *>(
+                                p.part_o + ((tok * p.Hq + h) * p.part_stride + it.s) * kD + c * 32);
+#pragma unroll
+                            for (int q4 = 0; q4 < 8; ++q4)
+                                dst[q4] = make_float4(__uint_as_float(o[q4 * 4]) * inv,
+                                                      __uint_as_float(o[q4 * 4 + 1]) * inv,
+                                                      __uint_as_float(o[q4 * 4 + 2]) * inv,
+                                                      __uint_as_float(o[q4 * 4 + 3]) * inv);
+                        }
+                    }
+                    if (row_ok) {
+                        if (p.nsplit == 1) {
+                            if (p.lse) p.lse[tok * p.Hq + h] = lse_v;
+                        } else {
+                            p.part_lse[(tok * p.Hq + h) * p.part_stride + it.s] = lse_v;
+                        }
+                    }
+                    // O_X has been read out: the chain may start the next item's P V
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_OFREE(x)));
+                }
+                jx += n_kv;
             }
+            Lbase += 2 * n_kv;
         }
-    } else if (FP8) {
+    } else if constexpr (FP8) {
         // ============================== e4m3 -> fp16 converters (warps 11, 12)
         const int cid = tid - 352;                 // 0 .. 63
-        bool ok = warp_wait(bar(B_Q), 0, abort_flag);
-        if (ok) {
+        int npipe = 0, Lbase = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            Item it;
+            ok = read_item(k, it);
+            if (!ok || it.r < 0) break;
+            if (it.n_kv == 0) continue;
+            ok = warp_wait(bar(B_Q), npipe & 1, abort_flag);
+            if (!ok) break;
+            __syncwarp();
             if constexpr (OUT_BF16) {
                 // q arrived as bf16; the MMAs run on fp16 operands: convert in place
                 uint4 *qv = reinterpret_cast<uint4 *>(sm + kOffQ);
-                for (int c = cid; c < ntiles_q * (int)(kQBytes / 16); c += 64) {
-                    const uint4 raw = qv[c];
-                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                for (int c = cid; c < it.ntiles_q * (int)(kQBytes / 16); c += 64) {
+                    const uint4 raw4 = qv[c];
+                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw4);
                     uint4 w;
                     uint32_t *wu = reinterpret_cast<uint32_t *>(&w);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 f = __bfloat1622float2(b2[k]);
-                        wu[k] = pack2<false>(f.x, f.y);
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(b2[e]);
+                        wu[e] = pack2<false>(f.x, f.y);
                     }
                     qv[c] = w;
                 }
@@ -535,47 +763,73 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_QREADY));
-        }
-        for (int L = 0; L < 2 * n_kv && ok; ++L) {
-            const int st = L % kStages, sl = L % kSlots;
-            ok = warp_wait(bar(B_STFULL(st)), (L / kStages) & 1, abort_flag);
-            if (ok && L >= kSlots) ok = warp_wait(bar(B_EMPTY(sl)), ((L / kSlots) - 1) & 1, abort_flag);
-            if (!ok) break;
-            const uint8_t *src = sm + kOffStage + st * kStageBytes;
-            uint8_t *dst = sm + kOffKV + sl * kTileBytes;
-            for (int i = cid; i < kBN * 8; i += 64) {
-                const int row = i >> 3, c = i & 7;          // e4m3 columns 16c .. 16c + 15 of one key
-                const uint4 raw = *reinterpret_cast<const uint4 *>(src + row * 128 + c * 16);
-                const uint16_t *b = reinterpret_cast<const uint16_t *>(&raw);
-                const uint4 lo = make_uint4(e4m3x2_to_h2(b[0]), e4m3x2_to_h2(b[1]), e4m3x2_to_h2(b[2]),
-                                            e4m3x2_to_h2(b[3]));
-                const uint4 hi = make_uint4(e4m3x2_to_h2(b[4]), e4m3x2_to_h2(b[5]), e4m3x2_to_h2(b[6]),
-                                            e4m3x2_to_h2(b[7]));
-                // fp16 columns 16c .. 16c + 15: 64-column half c / 4, 16-byte
-                // chunks 2 (c % 4) and 2 (c % 4) + 1 of that half, 128-byte swizzle
-                const int q = 2 * (c & 3);
-                uint8_t *rowp = dst + (c >> 2) * kKVHalf + row * 128;
-                *reinterpret_cast<uint4 *>(rowp + ((q ^ (row & 7)) << 4)) = lo;
-                *reinterpret_cast<uint4 *>(rowp + (((q + 1) ^ (row & 7)) << 4)) = hi;
+            for (int L = Lbase; L < Lbase + 2 * it.n_kv && ok; ++L) {
+                const int st = L % kStages, sl = L % kSlots;
+                ok = warp_wait(bar(B_STFULL(st)), (L / kStages) & 1, abort_flag);
+                if (!ok) break;
+                __syncwarp();
+                // the staged tile goes to registers (8 x 16 bytes a thread) and
+                // the stage back to the producer at once, so the TMA loads in
+                // flight never wait on the fp16 ring
+                const uint8_t *src = sm + kOffStage + st * kStageBytes;
+                uint4 raw8[kConvChunks];
+#pragma unroll
+                for (int u = 0; u < kConvChunks; ++u) {
+                    const int i = cid + 64 * u;
+                    raw8[u] = *reinterpret_cast<const uint4 *>(src + (i >> 3) * 128 + (i & 7) * 16);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_STEMPTY(st)));
+                if (L >= kSlots) ok = warp_wait(bar(B_EMPTY(sl)), ((L / kSlots) - 1) & 1, abort_flag);
+                if (!ok) break;
+                uint8_t *dst = sm + kOffKV + sl * kTileBytes;
+#pragma unroll
+                for (int u = 0; u < kConvChunks; ++u) {
+                    const int i = cid + 64 * u;
+                    const int row = i >> 3, c = i & 7;          // e4m3 columns 16c .. 16c + 15 of one key
+                    const uint4 raw4 = raw8[u];
+                    uint4 lo, hi;                                // fp16 patterns of value * 2^-8
+                    e4m3x4_to_h2x2_lo8(raw4.x, lo.x, lo.y);
+                    e4m3x4_to_h2x2_lo8(raw4.y, lo.z, lo.w);
+                    e4m3x4_to_h2x2_lo8(raw4.z, hi.x, hi.y);
+                    e4m3x4_to_h2x2_lo8(raw4.w, hi.z, hi.w);
+                    // fp16 columns 16c .. 16c + 15: 64-column half c / 4, 16-byte
+                    // chunks 2 (c % 4) and 2 (c % 4) + 1 of that half, 128-byte swizzle
+                    const int q = 2 * (c & 3);
+                    uint8_t *rowp = dst + (c >> 2) * kKVHalf + row * 128;
+                    *reinterpret_cast<uint4 *>(rowp + ((q ^ (row & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(rowp + (((q + 1) ^ (row & 7)) << 4)) = hi;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_FULL(sl)));
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(B_STEMPTY(st)));
-                mbar_arrive(bar(B_FULL(sl)));
-            }
+            Lbase += 2 * it.n_kv;
+            ++npipe;
         }
     }
 
     // ---- teardown: every MMA has completed before TMEM is released
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    if (tid == 0 && *abort_flag) raise_error(p.err, ERR_TIMEOUT);
+    if (tid == 0) {
+        if (*abort_flag) raise_error(p.err, ERR_TIMEOUT);
+        // the last CTA to finish rewinds the ticket counter for the slot's next launch
+        // (every CTA has drawn its last ticket before it counts itself done)
+        __threadfence();
+        if (atomicAdd(tp.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+            atomicExch(tp.sched, 0ull);
+            atomicExch(tp.sched + 1, 0ull);
+        }
+    }
 }
+
+constexpr int kMaxSchedDevices = 64;
 
 static int gcd_int(int a, int b) {
     while (b) {
@@ -604,14 +858,29 @@ static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &qmap, const 
     auto kern = fwd_tc_kernel<MMA_BF16, OUT_BF16, FP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, Lay::kThreads, Lay::kSmemBytes, stream>>>(tp, qmap, kmap, vmap);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(Lay::kThreads), Lay::kSmemBytes, stream, tp, qmap, kmap, vmap);
 }
 
-cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int kv_dtype, int64_t T, cudaStream_t stream) {
+cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int kv_dtype, int64_t T, int num_sms,
+                          cudaStream_t stream) {
     TcParams tp{};
     tp.f = f;
     tp.kv_rows = gcd_int(f.bs, kBN);
+    {
+        static unsigned long long *slots[kMaxSchedDevices] = {};
+        static std::atomic<unsigned> next[kMaxSchedDevices];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxSchedDevices) return cudaErrorInvalidDevice;
+        if (!slots[dev]) {
+            void *a = nullptr;
+            e = cudaGetSymbolAddress(&a, g_tc_sched);
+            if (e != cudaSuccess) return e;
+            slots[dev] = static_cast<unsigned long long *>(a);
+        }
+        tp.sched = slots[dev] + 2 * (next[dev].fetch_add(1u) % kSchedSlots);
+    }
     const bool q16 = q_dtype == DT_FP16;
     const bool fp8 = kv_dtype == DT_E4M3;
     CUtensorMap qmap, kmap, vmap;
@@ -634,7 +903,9 @@ cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int kv_dtype, int64_t
                             (uint64_t)f.Hkv * kD * 2, 64, 1, R))
             return cudaErrorInvalidValue;
     }
-    dim3 grid((unsigned)(f.n_row_blocks * f.nsplit), (unsigned)f.Hkv, (unsigned)f.B);
+    // persistent: one CTA per SM, never more CTAs than the class can have items
+    const long long max_items = (long long)f.n_row_blocks * f.nsplit * f.Hkv * f.B;
+    dim3 grid((unsigned)std::max(1LL, std::min<long long>(num_sms, max_items)));
     if (fp8) {
         // e4m3 caches: fp16 MMAs (the widening is exact); output in q's type
         return q16 ? launch_tc<false, false, true>(tp, qmap, kmap, vmap, grid, stream)

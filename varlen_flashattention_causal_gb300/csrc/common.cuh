@@ -39,12 +39,24 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-// two e4m3 values (low byte first) -> two fp16 values in one register; the
-// conversion is exact (every e4m3 value is an fp16 value)
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four e4m3 values (the bytes of w, lowest first) as the fp16 bit patterns
+// of value * 2^-8, two per register (lo: bytes 0, 1; hi: bytes 2, 3).  The
+// e4m3 sign, exponent and mantissa fields drop into the fp16 fields
+// unchanged -- only the exponent bias differs (7 against 15), hence the
+// factor 2^-8, which callers fold into their scales -- and e4m3 subnormals
+// land on fp16 subnormals exactly.  Each byte is sign-extended to 16 bits
+// (prmt with the sign-replicate selector bit), shifted into place, and
+// masked to sign | low 7 bits.  The e4m3 NaN pattern S.1111.111 is not
+// special-cased: it reads as +-480 * 2^-8.
+__device__ __forceinline__ void e4m3x4_to_h2x2_lo8(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));
+    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));
+    lo = (a << 7) & 0xBF80BF80u;
+    hi = (b << 7) & 0xBF80BF80u;
 }
+// 2^8: the factor e4m3x4_to_h2x2_lo8 leaves out
+constexpr float kE4m3Lo8Scale = 256.f;
 
 // ------------------------------------------------------------- PTX helpers
 
@@ -102,6 +114,17 @@ __device__ __forceinline__ int4 ldg_nc16(const void *p) {
 }
 
 // raise bits of the device error word (first writer wins nothing; OR only)
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation, so it may be scheduled while the
+// previous kernel in the stream drains.  pdl_wait() blocks until that
+// kernel has completed and its writes are visible (it returns at once when
+// there is none); every thread calls it before its first global-memory
+// access and before any exit, so a kernel never completes ahead of its
+// predecessor.  pdl_trigger() lets the next kernel be scheduled once every
+// CTA of this one has triggered or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void raise_error(unsigned *err, unsigned bits) {
     if (err) atomicOr(err, bits);
 }

@@ -39,7 +39,7 @@ struct FwdParams {
     float *part_o;               // [T, Hq, part_stride, D] fp32 (used when nsplit > 1)
     float *part_lse;             // [T, Hq, part_stride]
     int rows_lo, rows_hi;
-    int n_row_blocks;            // grid.x = n_row_blocks * nsplit
+    int n_row_blocks;            // row blocks of the largest request of the class
     unsigned *err;
 };
 
@@ -58,6 +58,25 @@ struct CombineParams {
     int small_rows_hi;
     int ns_small, ns_big, part_stride;
 };
+
+// Launch with programmatic stream serialisation (the kernel calls
+// pdl_wait() before touching global memory); stream-ordered like <<< >>>
+// and capturable in a CUDA graph.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
 
 // launchers (return the launch error)
 cudaError_t launch_fwd_mma(const FwdParams &p, int D, int q_dtype, int kv_dtype, int rows_per_cta,
@@ -87,6 +106,8 @@ int mma_rows_per_cta(int max_rows);
 // tcgen05 kernel: whether it handles this shape, rows per CTA, launcher
 bool tc_supported(int D, int q_dtype, int kv_dtype, int G);
 int tc_rows_per_cta();
-cudaError_t launch_fwd_tc(const FwdParams &p, int q_dtype, int kv_dtype, int64_t T, cudaStream_t stream);
+// (persistent: at most num_sms CTAs)
+cudaError_t launch_fwd_tc(const FwdParams &p, int q_dtype, int kv_dtype, int64_t T, int num_sms,
+                          cudaStream_t stream);
 
 }  // namespace attn
