@@ -46,7 +46,8 @@
  *                  in elements; a pointer offset into a row (cascade suffix
  *                  view block_table[:, n:]) is allowed
  *  - Head size D is 64 or 128, Hq % Hkv == 0 (GQA: query head h reads KV
- *    head h / (Hq / Hkv)), block_size is a positive multiple of 16.
+ *    head h / (Hq / Hkv)), block_size is a positive multiple of 16, and
+ *    B and Hq are at most 65535 (ATTN_ERR_SHAPE otherwise).
  *  - Pointers must be 16-byte aligned and token strides multiples of 8
  *    elements (16 bytes for 16-bit types).
  */
@@ -105,7 +106,10 @@ typedef enum {
  *
  * q_dtype: ATTN_BF16 or ATTN_FP16 (out has the same type).
  * kv_dtype: q_dtype, or ATTN_FP8_E4M3 (k/v_descale multiply the stored
- *   values; pass 1.0 for 16-bit caches).
+ *   values; pass 1.0 for 16-bit caches).  The kernels widen e4m3 by placing
+ *   its fields into fp16 (exact for every finite code); the NaN code
+ *   S.1111.111, which kv_cache_write stores only for NaN input, reads as
+ *   +-480.
  * max_seqlen_q / max_seqlen_k: upper bounds of q_len / kv_len over the batch
  *   (host scalars used to size the launch; values larger than the truth are
  *   safe, smaller ones are an error the kernels cannot detect).

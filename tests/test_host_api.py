@@ -73,6 +73,8 @@ def prefill(lib, **kw):
     (dict(Hq=6, Hkv=4), ERR_SHAPE),
     (dict(qs=8 * 128 - 8), ERR_SHAPE),
     (dict(B=-1), ERR_SHAPE),
+    (dict(B=65536), ERR_SHAPE),
+    (dict(Hq=65536 * 2, Hkv=2, qs=65536 * 2 * 128, os=65536 * 2 * 128), ERR_SHAPE),
     (dict(qd=E4M3, kd=E4M3), ERR_DTYPE),
     (dict(qd=BF16, kd=FP16), ERR_DTYPE),
     (dict(qd=FP32, kd=FP32), ERR_DTYPE),

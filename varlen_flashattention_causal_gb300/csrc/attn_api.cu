@@ -144,7 +144,7 @@ attn_status validate_fwd(const FwdArgs &a) {
     if (a.bs <= 0 || a.bs % 16 != 0) return ATTN_ERR_BLOCK_SIZE;
     if (!is16(a.q_dtype)) return ATTN_ERR_DTYPE;
     if (!(a.kv_dtype == a.q_dtype || a.kv_dtype == ATTN_FP8_E4M3)) return ATTN_ERR_DTYPE;
-    if (a.B < 0 || a.B > 65535 || a.T < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0 || a.Hkv > 65535 ||
+    if (a.B < 0 || a.B > 65535 || a.T < 0 || a.Hq <= 0 || a.Hq > 65535 || a.Hkv <= 0 || a.Hq % a.Hkv != 0 ||
         a.num_blocks < 0 || a.max_q < 0 || a.max_k < 0 || a.bt_stride < 0 || a.num_splits < 0)
         return ATTN_ERR_SHAPE;
     if (a.q_stride < (int64_t)a.Hq * a.D || a.out_stride < (int64_t)a.Hq * a.D) return ATTN_ERR_SHAPE;

@@ -137,31 +137,11 @@ __device__ __forceinline__ void store4<__half>(__half *p, float4 v) {
 
 constexpr int kCombineBatch = 8;   // segments whose partial rows a lane loads at once
 
-// One warp per (token, query head).  Segment s contributes with weight
-// exp(lse_s - lse), lse = log sum_s exp(lse_s); segments with lse_s = -inf
-// (no visible key) contribute nothing.  Tokens of requests that ran with a
-// single segment already hold their final output and are skipped.
+// Merge of one (token t, query head h) by one warp.  Segment s contributes
+// with weight exp(lse_s - lse), lse = log sum_s exp(lse_s); segments with
+// lse_s = -inf (no visible key) contribute nothing.
 template <class OT>
-__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
-    pdl_wait();
-    pdl_trigger();
-    const int warp_global = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (warp_global >= p.T * p.Hq) return;
-    const int t = warp_global / p.Hq;
-    const int h = warp_global % p.Hq;
-    int q_len = 1;
-    if (p.cu_seqlens_q) {
-        int lo = 0, hi = p.B - 1;                 // last r with cu[r] <= t
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.cu_seqlens_q[mid] <= t) lo = mid;
-            else hi = mid - 1;
-        }
-        q_len = p.cu_seqlens_q[lo + 1] - p.cu_seqlens_q[lo];
-    }
-    const int ns = (q_len * p.G <= p.small_rows_hi) ? p.ns_small : p.ns_big;
-    if (ns <= 1) return;
+__device__ __forceinline__ void combine_row(const CombineParams &p, int t, int h, int ns, int lane) {
     const int64_t base = ((int64_t)t * p.Hq + h) * (int64_t)p.part_stride;
     const float *ls = p.part_lse + base;
     float mx = -INFINITY;
@@ -206,10 +186,67 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     if (lane == 0 && p.lse) p.lse[(int64_t)t * p.Hq + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
+// General form: one warp per (token, query head); the token's request is
+// found by binary search in cu_seqlens_q, its class gives the segment
+// count, and tokens of requests that ran with one segment are skipped.
+template <class OT>
+__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+    pdl_wait();
+    pdl_trigger();
+    const int warp_global = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp_global >= p.T * p.Hq) return;
+    const int t = warp_global / p.Hq;
+    const int h = warp_global % p.Hq;
+    int q_len = 1;
+    if (p.cu_seqlens_q) {
+        int lo = 0, hi = p.B - 1;                 // last r with cu[r] <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.cu_seqlens_q[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        q_len = p.cu_seqlens_q[lo + 1] - p.cu_seqlens_q[lo];
+    }
+    const int ns = (q_len * p.G <= p.small_rows_hi) ? p.ns_small : p.ns_big;
+    if (ns <= 1) return;
+    combine_row<OT>(p, t, h, ns, lane);
+}
+
+// Rows-light form, for calls in which only rows-light requests were split
+// (the usual case: decode rows next to unsplit prefill chunks).  One CTA
+// per (request, 8 query heads): two loads give the request's class, so the
+// CTAs of rows-heavy requests exit at once instead of one warp per token
+// and head searching for its request.
+constexpr int kCombineHeads = 8;
+template <class OT>
+__global__ void __launch_bounds__(32 * kCombineHeads) combine_light_kernel(const CombineParams p) {
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x;
+    int t0 = r, q_len = 1;
+    if (p.cu_seqlens_q) {
+        t0 = p.cu_seqlens_q[r];
+        q_len = p.cu_seqlens_q[r + 1] - t0;
+    }
+    if (q_len <= 0 || q_len * p.G > p.small_rows_hi) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y * kCombineHeads + warp;
+    if (h >= p.Hq) return;
+    for (int i = 0; i < q_len; ++i) combine_row<OT>(p, t0 + i, h, p.ns_small, lane);
+}
+
 cudaError_t launch_combine(const CombineParams &p, int out_dtype, cudaStream_t stream) {
     const int64_t threads = (int64_t)p.T * p.Hq * 32;
     if (threads == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((threads + 127) / 128);
+    if (p.ns_big <= 1 && p.ns_small > 1) {
+        const dim3 g((unsigned)p.B, (unsigned)((p.Hq + kCombineHeads - 1) / kCombineHeads));
+        const dim3 blk(32 * kCombineHeads);
+        if (out_dtype == DT_BF16) return launch_pdl(combine_light_kernel<__nv_bfloat16>, g, blk, 0, stream, p);
+        if (out_dtype == DT_FP16) return launch_pdl(combine_light_kernel<__half>, g, blk, 0, stream, p);
+        return cudaErrorInvalidValue;
+    }
     if (out_dtype == DT_BF16) return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(128), 0, stream, p);
     if (out_dtype == DT_FP16) return launch_pdl(combine_kernel<__half>, dim3(blocks), dim3(128), 0, stream, p);
     return cudaErrorInvalidValue;

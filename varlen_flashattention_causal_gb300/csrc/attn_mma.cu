@@ -42,11 +42,6 @@ struct MmaCfg {
     static constexpr int TILE16 = BN * ROW16;
     static constexpr int Q_BYTES = ROWS * ROW16;
     static constexpr int STAGE_BYTES = 2 * TILE_RAW;
-    static constexpr int CONV_BYTES = (KVT == DT_E4M3) ? 2 * TILE16 : 0;
-    static constexpr int OSTRIDE = D + 4;                // fp32 epilogue row stride (bank spread)
-    static constexpr int EPI_BYTES = WN * ROWS * OSTRIDE * 4 + 2 * WN * ROWS * 4;
-    static constexpr int MAIN_BYTES = STAGES * STAGE_BYTES + CONV_BYTES;
-    static constexpr int SMEM = Q_BYTES + (MAIN_BYTES > EPI_BYTES ? MAIN_BYTES : EPI_BYTES);
     static constexpr int NW = BN / WN;                   // keys per warp per tile
     static constexpr int NT = NW / 8;                    // n8 tiles of S per warp
     static constexpr int KT = D / 16;                    // k16 steps of Q K^T
@@ -56,6 +51,20 @@ struct MmaCfg {
     // every tile and is also the only warp that reads them (its key slice),
     // so the main loop needs no CTA-wide barrier.
     static constexpr bool WARP_LOCAL = (WM == 1 && RPW == NW);
+    // e4m3 K fragments straight from the staged tile (decode shape, D 128):
+    // the head dimension is read in a permuted order -- k-step kk of lane
+    // quad t covers dims 32t + 4kk .. 32t + 4kk + 3, the same order for the
+    // Q fragments, so Q K^T is unchanged -- which makes a lane's B
+    // fragments of all eight k-steps 32 contiguous bytes of its key row,
+    // widened in registers.  V still goes through shared memory (its
+    // fragments run along keys, which are rows of the cache).
+    static constexpr bool KDIRECT = (KVT == DT_E4M3) && WARP_LOCAL && D == 128;
+    // e4m3: widened fp16 tiles (V only with KDIRECT) after the staging ring
+    static constexpr int CONV_BYTES = (KVT == DT_E4M3) ? (KDIRECT ? TILE16 : 2 * TILE16) : 0;
+    static constexpr int OSTRIDE = D + 4;                // fp32 epilogue row stride (bank spread)
+    static constexpr int EPI_BYTES = WN * ROWS * OSTRIDE * 4 + 2 * WN * ROWS * 4;
+    static constexpr int MAIN_BYTES = STAGES * STAGE_BYTES + CONV_BYTES;
+    static constexpr int SMEM = Q_BYTES + (MAIN_BYTES > EPI_BYTES ? MAIN_BYTES : EPI_BYTES);
     static_assert(WM * WN == 4, "4 warps");
     static_assert(NT % 2 == 0, "n-tile pairs");
     static_assert((RPW * CH) % 32 == 0, "whole warp copy rounds");
@@ -147,6 +156,12 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     const int64_t bt_base = (int64_t)r * p.bt_stride;
     const uint8_t *kbase = reinterpret_cast<const uint8_t *>(p.k_cache);
     const uint8_t *vbase = reinterpret_cast<const uint8_t *>(p.v_cache);
+    // byte offset of 16-byte chunk ch of row `row` in a staged e4m3 tile:
+    // chunks XOR-swizzled by row & 7 with KDIRECT (the direct K fragment
+    // loads of eight rows then hit eight different bank groups), plain otherwise
+    auto stage8 = [](int row, int ch) -> uint32_t {
+        return (uint32_t)(row * C::KV_ROW + ((C::KDIRECT ? (ch ^ (row & 7)) : ch) << 4));
+    };
     auto load_tile = [&](int t, int stage) {
         const int n0 = kv_lo + t * BN;
         int64_t off = 0;
@@ -172,8 +187,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
             const int64_t o = __shfl_sync(0xffffffffu, off, lr);
             const int v = __shfl_sync(0xffffffffu, ok, lr);
             const int row = warp * C::RPW + lr;
-            const uint32_t dst = (C::KVT == DT_E4M3) ? (uint32_t)(row * C::KV_ROW + ch * 16)
-                                                     : swz(row, ch, C::KV_ROW);
+            const uint32_t dst = (C::KVT == DT_E4M3) ? stage8(row, ch) : swz(row, ch, C::KV_ROW);
             const int64_t so = v ? o + ch * 16 : 0;
             cp_async16(smem_u32(sK + dst), kbase + so, v ? 16 : 0);
             cp_async16(smem_u32(sV + dst), vbase + so, v ? 16 : 0);
@@ -183,7 +197,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     // e4m3 tiles are widened to fp16 (exact) into a swizzled tile for
     // ldmatrix.  Warp-local mode: each warp widens only its own rows.
     uint8_t *cK = sMain + STAGES * C::STAGE_BYTES;
-    uint8_t *cV = cK + C::TILE16;
+    uint8_t *cV = C::KDIRECT ? cK : cK + C::TILE16;
     auto convert_tile = [&](int stage) {
         const uint8_t *sK = sMain + stage * C::STAGE_BYTES;
         const uint8_t *sV = sK + C::TILE_RAW;
@@ -193,20 +207,23 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         const int rbase = C::WARP_LOCAL ? warp * C::RPW : 0;
         for (int c = c0; c < kChunks; c += cstep) {
             const int row = rbase + c / (D / 16), ch = c % (D / 16);
-            const int4 rk = *reinterpret_cast<const int4 *>(sK + row * D + ch * 16);
-            const int4 rv = *reinterpret_cast<const int4 *>(sV + row * D + ch * 16);
             // fp16 patterns of value * 2^-8 (the 2^8 is in the scales)
-            int4 k0, k1, v0, v1;
-            e4m3x4_to_h2x2_lo8((uint32_t)rk.x, reinterpret_cast<uint32_t &>(k0.x), reinterpret_cast<uint32_t &>(k0.y));
-            e4m3x4_to_h2x2_lo8((uint32_t)rk.y, reinterpret_cast<uint32_t &>(k0.z), reinterpret_cast<uint32_t &>(k0.w));
-            e4m3x4_to_h2x2_lo8((uint32_t)rk.z, reinterpret_cast<uint32_t &>(k1.x), reinterpret_cast<uint32_t &>(k1.y));
-            e4m3x4_to_h2x2_lo8((uint32_t)rk.w, reinterpret_cast<uint32_t &>(k1.z), reinterpret_cast<uint32_t &>(k1.w));
+            if constexpr (!C::KDIRECT) {
+                const int4 rk = *reinterpret_cast<const int4 *>(sK + stage8(row, ch));
+                int4 k0, k1;
+                e4m3x4_to_h2x2_lo8((uint32_t)rk.x, reinterpret_cast<uint32_t &>(k0.x), reinterpret_cast<uint32_t &>(k0.y));
+                e4m3x4_to_h2x2_lo8((uint32_t)rk.y, reinterpret_cast<uint32_t &>(k0.z), reinterpret_cast<uint32_t &>(k0.w));
+                e4m3x4_to_h2x2_lo8((uint32_t)rk.z, reinterpret_cast<uint32_t &>(k1.x), reinterpret_cast<uint32_t &>(k1.y));
+                e4m3x4_to_h2x2_lo8((uint32_t)rk.w, reinterpret_cast<uint32_t &>(k1.z), reinterpret_cast<uint32_t &>(k1.w));
+                *reinterpret_cast<int4 *>(cK + swz(row, 2 * ch, C::ROW16)) = k0;
+                *reinterpret_cast<int4 *>(cK + swz(row, 2 * ch + 1, C::ROW16)) = k1;
+            }
+            const int4 rv = *reinterpret_cast<const int4 *>(sV + stage8(row, ch));
+            int4 v0, v1;
             e4m3x4_to_h2x2_lo8((uint32_t)rv.x, reinterpret_cast<uint32_t &>(v0.x), reinterpret_cast<uint32_t &>(v0.y));
             e4m3x4_to_h2x2_lo8((uint32_t)rv.y, reinterpret_cast<uint32_t &>(v0.z), reinterpret_cast<uint32_t &>(v0.w));
             e4m3x4_to_h2x2_lo8((uint32_t)rv.z, reinterpret_cast<uint32_t &>(v1.x), reinterpret_cast<uint32_t &>(v1.y));
             e4m3x4_to_h2x2_lo8((uint32_t)rv.w, reinterpret_cast<uint32_t &>(v1.z), reinterpret_cast<uint32_t &>(v1.w));
-            *reinterpret_cast<int4 *>(cK + swz(row, 2 * ch, C::ROW16)) = k0;
-            *reinterpret_cast<int4 *>(cK + swz(row, 2 * ch + 1, C::ROW16)) = k1;
             *reinterpret_cast<int4 *>(cV + swz(row, 2 * ch, C::ROW16)) = v0;
             *reinterpret_cast<int4 *>(cV + swz(row, 2 * ch + 1, C::ROW16)) = v1;
         }
@@ -221,11 +238,30 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     __syncthreads();   // Q visible to every warp
 
     uint32_t qf[C::KT][4];
+    if constexpr (C::KDIRECT) {
+        // permuted head dimension (see KDIRECT): lane (g, t) takes, for
+        // k-step kk, dims 32t + 4kk .. 32t + 4kk + 3 of rows g and g + 8
+        const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
-    for (int kk = 0; kk < C::KT; ++kk) {
-        const int row = wm * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int ch = kk * 2 + (lane >> 4);
-        ldmatrix_x4(qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], smem_u32(sQ + swz(row, ch, C::ROW16)));
+        for (int c = 0; c < 4; ++c) {
+            const uint4 r0 = *reinterpret_cast<const uint4 *>(sQ + swz(wm * 16 + g, 4 * t4 + c, C::ROW16));
+            const uint4 r1 = *reinterpret_cast<const uint4 *>(sQ + swz(wm * 16 + g + 8, 4 * t4 + c, C::ROW16));
+            qf[2 * c][0] = r0.x;       // row g, dims 32t + 8c + 0, 1
+            qf[2 * c][2] = r0.y;       // row g, dims 32t + 8c + 2, 3
+            qf[2 * c][1] = r1.x;       // row g + 8
+            qf[2 * c][3] = r1.y;
+            qf[2 * c + 1][0] = r0.z;   // k-step 2c + 1: dims 32t + 8c + 4 .. 7
+            qf[2 * c + 1][2] = r0.w;
+            qf[2 * c + 1][1] = r1.z;
+            qf[2 * c + 1][3] = r1.w;
+        }
+    } else {
+#pragma unroll
+        for (int kk = 0; kk < C::KT; ++kk) {
+            const int row = wm * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int ch = kk * 2 + (lane >> 4);
+            ldmatrix_x4(qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], smem_u32(sQ + swz(row, ch, C::ROW16)));
+        }
     }
 
     // query token (local index) of the two rows this thread owns in C frags
@@ -266,16 +302,36 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         float s[C::NT][4];
 #pragma unroll
         for (int i = 0; i < C::NT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+        if constexpr (C::KDIRECT) {
+            // n-tile j: lane (g, t) holds key row wn * NW + 8j + g, bytes
+            // [32t, 32t + 32) = its B fragments of all eight k-steps
+            const uint8_t *raw = sMain + (t % STAGES) * C::STAGE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < C::KT; ++kk) {
+            for (int j = 0; j < C::NT; ++j) {
+                const int key = wn * C::NW + 8 * j + (lane >> 2);
+                const int c0 = 2 * (lane & 3);
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(raw + stage8(key, c0));
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(raw + stage8(key, c0 + 1));
+                const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-            for (int j = 0; j < C::NT / 2; ++j) {
-                const int key = wn * C::NW + j * 16 + (lane & 7) + (lane >> 4) * 8;
-                const int ch = kk * 2 + ((lane >> 3) & 1);
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(b0, b1, b2, b3, smem_u32(tK + swz(key, ch, C::ROW16)));
-                mma16816<C::MMA_BF16>(s[2 * j], qf[kk], b0, b1);
-                mma16816<C::MMA_BF16>(s[2 * j + 1], qf[kk], b2, b3);
+                for (int kk = 0; kk < C::KT; ++kk) {
+                    uint32_t b0, b1;
+                    e4m3x4_to_h2x2_lo8(w[kk], b0, b1);
+                    mma16816<false>(s[j], qf[kk], b0, b1);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < C::KT; ++kk) {
+#pragma unroll
+                for (int j = 0; j < C::NT / 2; ++j) {
+                    const int key = wn * C::NW + j * 16 + (lane & 7) + (lane >> 4) * 8;
+                    const int ch = kk * 2 + ((lane >> 3) & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(b0, b1, b2, b3, smem_u32(tK + swz(key, ch, C::ROW16)));
+                    mma16816<C::MMA_BF16>(s[2 * j], qf[kk], b0, b1);
+                    mma16816<C::MMA_BF16>(s[2 * j + 1], qf[kk], b2, b3);
+                }
             }
         }
 
@@ -447,7 +503,9 @@ static cudaError_t launch_cfg(const FwdParams &p, cudaStream_t stream) {
 
 template <int D, int QT, int KVT>
 static cudaError_t launch_rows(const FwdParams &p, int rows_per_cta, cudaStream_t stream) {
-    constexpr int STAGES = (KVT == DT_E4M3) ? 4 : (D == 128 ? 3 : 4);
+    // e4m3, D 128: three stages and one widened tile keep a CTA at 68 KB
+    // of shared memory, three CTAs per SM
+    constexpr int STAGES = (KVT == DT_E4M3) ? (D == 128 ? 3 : 4) : (D == 128 ? 3 : 4);
     switch (rows_per_cta) {
     case 16: return launch_cfg<MmaCfg<D, 1, 4, 64, STAGES, QT, KVT>>(p, stream);
     case 32: return launch_cfg<MmaCfg<D, 2, 2, 64, STAGES, QT, KVT>>(p, stream);
