@@ -16,6 +16,7 @@ reported as TFLOP/s under "prefill".
 deliberately slow reference arm.
 """
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -34,6 +35,34 @@ from varlen_flashattention_causal_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged-decode KV GB/s + varlen-prefill TFLOP/s, % of 1×GB300 roofline"
 L2_BYTES = 129 * 1024 * 1024
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the decode split kernel on this workload, from one `ncu --set full` capture
+# (profiles/decode_llama8b_fwd_mma.md gives the command).  It is reported only
+# while the kernel's sources hash to the value recorded with the capture.
+DECODE_TRAFFIC = {
+    "bytes": None,
+    "sources": ["varlen_flashattention_causal_gb300/csrc/attn_mma.cu",
+                "varlen_flashattention_causal_gb300/csrc/common.cuh",
+                "varlen_flashattention_causal_gb300/csrc/internal.h"],
+    "sha256": None,
+}
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def decode_traffic():
+    t = DECODE_TRAFFIC
+    if t["bytes"] is None or source_hash(t["sources"]) != t["sha256"]:
+        return None
+    return t["bytes"]
 
 
 def peaks():
@@ -256,9 +285,10 @@ def run_ours(args):
                    "l2": "inputs larger than L2: %.0f MB of K/V read per step vs %d MB L2"
                          % (sum(b.kv_lens) * b.Hkv * b.D * 4 / 1e6, L2_BYTES >> 20),
                    "parallelism": "replicas x%d (independent batches, no collective)" % ws},
-        "roofline": {"kernel": "attn_paged_decode (fwd_mma_kernel + combine_kernel)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "peak_source": peak_kind, "traffic": None,
+        "roofline": {"kernel": "attn_paged_decode (fwd_mma_kernel + combine_light_kernel; time of the whole call)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": peak_kind, "traffic": decode_traffic(),
+                     "traffic_kernel": "fwd_mma_kernel (ncu, one launch)",
                      "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(attn_ms, 5)},
         "prefill": pf,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": bi,
