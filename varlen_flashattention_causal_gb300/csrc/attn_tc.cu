@@ -150,6 +150,13 @@ struct TcParams {
 constexpr int kSchedSlots = 64;
 __device__ unsigned long long g_tc_sched[kSchedSlots][2];
 
+// max of three (one instruction on this architecture)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // whole-warp wait: lane 0 polls, the result is broadcast, so every lane
 // takes the same path into the warp-collective tcgen05 instructions after it
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
@@ -591,22 +598,24 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                     }
                     // masked keys: this row sees keys n0 .. n0 + nv - 1 of the tile
                     const int nv = need_mask ? max(0, min(kBN, nlim - n0 + 1)) : kBN;
-                    float mx8[8];
+                    if (nv < kBN) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-                    if (nv == kBN) {
-#pragma unroll
-                        for (int e = 0; e < kBN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(v[e]));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < kBN; ++e) {
-                            const float s = e < nv ? __uint_as_float(v[e]) : -INFINITY;
-                            v[e] = __float_as_uint(s);
-                            mx8[e & 7] = fmaxf(mx8[e & 7], s);
-                        }
+                        for (int e = 0; e < kBN; ++e)
+                            if (e >= nv) v[e] = __float_as_uint(-INFINITY);
                     }
-                    float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                    // row maximum: three-input max in four independent chains
+                    // (the softmax is issue bound: fewer instructions per element
+                    // is what speeds it up)
+                    float mx4[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) mx4[c] = fmaxf(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
+#pragma unroll
+                    for (int b8 = 8; b8 < kBN; b8 += 8) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            mx4[c] = fmax3(mx4[c], __uint_as_float(v[b8 + 2 * c]), __uint_as_float(v[b8 + 2 * c + 1]));
+                    }
+                    float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
                     mx *= sl2;
                     // rescale only when the maximum grows past the threshold
                     const bool bump = mx > m_ref + kRescaleThreshold;
@@ -615,19 +624,25 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                     const float alpha = corr ? ex2(m_ref - m_new) : 1.f;
                     const float base = (m_new == -INFINITY) ? 0.f : m_new;
                     m_ref = m_new;
+                    // P = 2^(s * scale - m): scale-and-shift and the row sum on
+                    // packed fp32 pairs (one instruction per two elements)
                     uint32_t pk[32];
-                    float rs8[8];
+                    float2 rs2[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
+                    for (int c = 0; c < 4; ++c) rs2[c] = make_float2(0.f, 0.f);
+                    const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(-base, -base);
 #pragma unroll
                     for (int e = 0; e < kBN; e += 2) {
-                        const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -base));
-                        const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -base));
-                        rs8[(e >> 1) & 7] += p0 + p1;
+                        const float2 x2 =
+                            __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nb2);
+                        const float p0 = ex2(x2.x);
+                        const float p1 = ex2(x2.y);
+                        rs2[(e >> 1) & 3] = __fadd2_rn(rs2[(e >> 1) & 3], make_float2(p0, p1));
                         pk[e / 2] = pack2<MMA_BF16>(p0, p1);
                     }
-                    const float rs =
-                        ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                    const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
+                    const float2 r03 = __fadd2_rn(r01, r23);
+                    const float rs = r03.x + r03.y;
                     l = l * alpha + rs;
                     if (__any_sync(0xffffffffu, corr)) {
                         // O_X must hold P_X(j-1) V before it is rescaled (corr implies j > 0)
