@@ -44,6 +44,14 @@ def _load():
             c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
             c.c_double, c.c_int, c.c_void_p, c.c_int64,
             c.c_void_p, c.c_void_p, c.c_int]
+        lib.oracle_attention_ext.restype = c.c_int
+        lib.oracle_attention_ext.argtypes = [
+            c.c_void_p, c.c_int, c.c_int64,
+            c.c_void_p, c.c_void_p, c.c_int, c.c_double, c.c_double,
+            c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64,
+            c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
+            c.c_double, c.c_int, c.c_int64, c.c_int64, c.c_double, c.c_void_p,
+            c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p, c.c_int]
         lib.oracle_merge_states.restype = None
         lib.oracle_merge_states.argtypes = [
             c.c_int64, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,
@@ -86,13 +94,17 @@ def _host(t, dtype=None):
 
 def attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
               softmax_scale, causal=True, k_scale=1.0, v_scale=1.0,
-              rows=None, nthreads=0):
+              rows=None, nthreads=0, window=(-1, -1), softcap=0.0, sinks=None):
     """fp64 attention over a paged cache.
 
     q: [T, Hq, D] (bf16/fp16); k_cache, v_cache: [num_blocks, bs, Hkv, D]
     (bf16/fp16/e4m3); cu_seqlens_q: [B+1]; seqused_k: [B]; block_table:
     [B, max_blocks] (int32).  rows: optional packed token indices to
-    evaluate.  Returns (out [n, Hq, D] float64, lse [n, Hq] float64).
+    evaluate.  window = (left, right) keys around the query's absolute
+    position (-1 unlimited), softcap (0 = none), sinks [Hq] (one logit per
+    query head, or None): the variants of "FlashAttention deep dive",
+    flash_attn_varlen_func (window_size, softcap, s_aux) as read in
+    attn_oracle.c.  Returns (out [n, Hq, D] float64, lse [n, Hq] float64).
     """
     lib = _load()
     q = _host(q)
@@ -108,13 +120,26 @@ def attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
     n = T if rws is None else rws.numel()
     out = torch.empty((n, Hq, D), dtype=torch.float64)
     lse = torch.empty((n, Hq), dtype=torch.float64)
-    st = lib.oracle_attention(
-        q.data_ptr(), _code(q), Hq * D,
-        k_cache.data_ptr(), v_cache.data_ptr(), _code(k_cache),
-        float(k_scale), float(v_scale),
-        cu.data_ptr(), su.data_ptr(), bt.data_ptr(), bt.shape[1],
-        B, Hq, Hkv, D, bs, nb, float(softmax_scale), int(bool(causal)),
-        _ptr(rws), n, out.data_ptr(), lse.data_ptr(), int(nthreads))
+    plain = tuple(window) == (-1, -1) and not softcap and sinks is None
+    if plain:
+        st = lib.oracle_attention(
+            q.data_ptr(), _code(q), Hq * D,
+            k_cache.data_ptr(), v_cache.data_ptr(), _code(k_cache),
+            float(k_scale), float(v_scale),
+            cu.data_ptr(), su.data_ptr(), bt.data_ptr(), bt.shape[1],
+            B, Hq, Hkv, D, bs, nb, float(softmax_scale), int(bool(causal)),
+            _ptr(rws), n, out.data_ptr(), lse.data_ptr(), int(nthreads))
+    else:
+        sk = None if sinks is None else _host(torch.as_tensor(sinks), torch.float64)
+        assert sk is None or sk.numel() == Hq
+        st = lib.oracle_attention_ext(
+            q.data_ptr(), _code(q), Hq * D,
+            k_cache.data_ptr(), v_cache.data_ptr(), _code(k_cache),
+            float(k_scale), float(v_scale),
+            cu.data_ptr(), su.data_ptr(), bt.data_ptr(), bt.shape[1],
+            B, Hq, Hkv, D, bs, nb, float(softmax_scale), int(bool(causal)),
+            int(window[0]), int(window[1]), float(softcap), _ptr(sk),
+            _ptr(rws), n, out.data_ptr(), lse.data_ptr(), int(nthreads))
     if st != 0:
         raise ValueError("oracle_attention failed with status %d" % st)
     return out, lse
@@ -165,14 +190,17 @@ def e4m3_to_double(code: int) -> float:
 
 
 def dense_masked_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale,
-                           causal=True):
+                           causal=True, window=(-1, -1), softcap=0.0, sinks=None):
     """Brute force over the whole packed problem (tiny cases only).
 
     q: [T, Hq, D]; k, v: [Tk, Hkv, D] hold every request's keys back to back
     (request r owns key rows [cu_seqlens_k[r], cu_seqlens_k[r+1])), no
     paging.  One T x Tk score matrix per head is built, entries between
     different requests are set to -inf, and, when causal, so are keys after
-    the query's absolute position ctx + i (ctx = kv_len - q_len).  Then a
+    the query's absolute position ctx + i (ctx = kv_len - q_len); a window
+    (left, right) masks keys outside [pos - left, pos + right].  softcap
+    maps the scaled scores through c * tanh(s / c).  sinks append one extra
+    score column per head (the sink logit) whose value row is zero.  Then a
     dense row softmax and P @ V.  Returns float64 numpy (out, lse, mask).
     """
     q = np.asarray(q, dtype=np.float64)
@@ -196,20 +224,31 @@ def dense_masked_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale,
         req_k[ck[r]:ck[r + 1]] = r
         loc_k[ck[r]:ck[r + 1]] = np.arange(ck[r + 1] - ck[r])
     mask = req_q[:, None] == req_k[None, :]
+    pos = (ctx_q + loc_q)[:, None]
     if causal:
-        mask &= loc_k[None, :] <= (ctx_q + loc_q)[:, None]
+        mask &= loc_k[None, :] <= pos
+    if window[0] >= 0:
+        mask &= loc_k[None, :] >= pos - window[0]
+    if window[1] >= 0:
+        mask &= loc_k[None, :] <= pos + window[1]
     out = np.zeros((T, Hq, D))
     lse = np.full((T, Hq), -np.inf)
     for h in range(Hq):
         g = h // G
         s = softmax_scale * (q[:, h, :] @ k[:, g, :].T)
+        if softcap:
+            s = softcap * np.tanh(s / softcap)
         s = np.where(mask, s, -np.inf)
+        vg = v[:, g, :]
+        if sinks is not None:
+            s = np.concatenate([s, np.full((T, 1), float(sinks[h]))], axis=1)
+            vg = np.concatenate([vg, np.zeros((1, D))], axis=0)
         m = s.max(axis=1, keepdims=True)
         live = np.isfinite(m[:, 0])
         m = np.where(np.isfinite(m), m, 0.0)
         e = np.exp(s - m)
         l = e.sum(axis=1)
         p = e / np.where(l > 0, l, 1.0)[:, None]
-        out[:, h, :] = p @ v[:, g, :]
+        out[:, h, :] = p @ vg
         lse[:, h] = np.where(live, m[:, 0] + np.log(np.where(l > 0, l, 1.0)), -np.inf)
     return out, lse, mask

@@ -150,15 +150,32 @@ static int elem_bytes(int dtype) {
  * is [n, Hq] (natural log), n = number of evaluated tokens.  A query with
  * no visible key gets out = 0 and lse = -inf.
  */
-int oracle_attention(const void *q, int q_dtype, int64_t q_stride_tok,
-                     const void *k_cache, const void *v_cache, int kv_dtype,
-                     double k_scale, double v_scale,
-                     const int32_t *cu_seqlens_q, const int32_t *seqused_k,
-                     const int32_t *block_table, int64_t bt_stride,
-                     int B, int Hq, int Hkv, int D, int bs, int num_blocks,
-                     double softmax_scale, int causal,
-                     const int64_t *rows, int64_t n_rows,
-                     double *out, double *lse, int nthreads) {
+/*
+ * Variants named in the argument table of "FlashAttention deep dive"
+ * (flash_attn_varlen_func: window_size, softcap, s_aux) and in its table of
+ * supported variants (sliding window = local attention, soft cap on the
+ * logits, attention sinks).  The page names them without formulas; this
+ * oracle takes the plain readings:
+ *   window (left, right): query i of a request sits at p = ctx + i and sees
+ *     keys j with p - left <= j <= p + right (a negative bound is
+ *     unlimited), on top of the causal rule j <= p and of j < kv_len;
+ *   softcap c > 0: each scaled logit s becomes c * tanh(s / c);
+ *   sinks: query head h has a logit z_h that joins the softmax
+ *     normalisation with a zero value vector:
+ *       out = sum_j e^{s_j} V_j / (e^{z_h} + sum_j e^{s_j}),
+ *       lse = log(e^{z_h} + sum_j e^{s_j}).
+ */
+int oracle_attention_ext(const void *q, int q_dtype, int64_t q_stride_tok,
+                         const void *k_cache, const void *v_cache, int kv_dtype,
+                         double k_scale, double v_scale,
+                         const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                         const int32_t *block_table, int64_t bt_stride,
+                         int B, int Hq, int Hkv, int D, int bs, int num_blocks,
+                         double softmax_scale, int causal,
+                         int64_t window_left, int64_t window_right, double softcap,
+                         const double *sinks,
+                         const int64_t *rows, int64_t n_rows,
+                         double *out, double *lse, int nthreads) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || bs <= 0 ||
         num_blocks < 0 || elem_bytes(q_dtype) == 0 || elem_bytes(kv_dtype) == 0)
         return ORC_EINVAL;
@@ -201,7 +218,12 @@ int oracle_attention(const void *q, int q_dtype, int64_t q_stride_tok,
             int64_t last = kv_len - 1;                  /* last visible key */
             if (causal && ctx + i < last)
                 last = ctx + i;
-            const int64_t nvis = last + 1 > 0 ? last + 1 : 0;
+            if (window_right >= 0 && ctx + i + window_right < last)
+                last = ctx + i + window_right;
+            int64_t first = 0;                          /* first visible key */
+            if (window_left >= 0 && ctx + i - window_left > first)
+                first = ctx + i - window_left;
+            const int64_t nvis = last + 1 > 0 ? last + 1 : 0;   /* keys 0 .. last: s[] indexed by j */
             if (nvis > cap) {
                 free(s);
                 cap = nvis;
@@ -212,7 +234,7 @@ int oracle_attention(const void *q, int q_dtype, int64_t q_stride_tok,
                 qv[d] = load_elem(q, q_off + d, q_dtype);
             int bad = 0;
             double M = -INFINITY;
-            for (int64_t j = 0; j < nvis; ++j) {
+            for (int64_t j = first; j < nvis; ++j) {
                 const int32_t phys = block_table[r * bt_stride + j / bs];
                 if (phys < 0 || phys >= num_blocks) { bad = 1; break; }
                 const int64_t k_off = (((int64_t)phys * bs + j % bs) * Hkv + g) * D;
@@ -220,6 +242,8 @@ int oracle_attention(const void *q, int q_dtype, int64_t q_stride_tok,
                 for (int d = 0; d < D; ++d)
                     dot += qv[d] * (load_elem(k_cache, k_off + d, kv_dtype) * k_scale);
                 s[j] = softmax_scale * dot;
+                if (softcap > 0.0)
+                    s[j] = softcap * tanh(s[j] / softcap);
                 if (s[j] > M) M = s[j];
             }
             if (bad) {
@@ -227,13 +251,15 @@ int oracle_attention(const void *q, int q_dtype, int64_t q_stride_tok,
                 status = ORC_EBLOCK;
                 continue;
             }
+            const double z = sinks ? sinks[h] : -INFINITY;     /* sink logit */
             for (int d = 0; d < D; ++d) o[d] = 0.0;
-            if (nvis == 0) {
+            if (nvis <= first && z == -INFINITY) {      /* no visible key and no sink */
                 lse[oi * Hq + h] = -INFINITY;
                 continue;
             }
-            double L = 0.0;
-            for (int64_t j = 0; j < nvis; ++j) {
+            if (z > M) M = z;
+            double L = z == -INFINITY ? 0.0 : exp(z - M);      /* the sink's share, value 0 */
+            for (int64_t j = first; j < nvis; ++j) {
                 const double e = exp(s[j] - M);
                 L += e;
                 const int32_t phys = block_table[r * bt_stride + j / bs];
@@ -248,6 +274,22 @@ int oracle_attention(const void *q, int q_dtype, int64_t q_stride_tok,
         free(qv);
     }
     return status;
+}
+
+/* Plain attention: no window, no soft cap, no sink. */
+int oracle_attention(const void *q, int q_dtype, int64_t q_stride_tok,
+                     const void *k_cache, const void *v_cache, int kv_dtype,
+                     double k_scale, double v_scale,
+                     const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                     const int32_t *block_table, int64_t bt_stride,
+                     int B, int Hq, int Hkv, int D, int bs, int num_blocks,
+                     double softmax_scale, int causal,
+                     const int64_t *rows, int64_t n_rows,
+                     double *out, double *lse, int nthreads) {
+    return oracle_attention_ext(q, q_dtype, q_stride_tok, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                                cu_seqlens_q, seqused_k, block_table, bt_stride, B, Hq, Hkv, D, bs,
+                                num_blocks, softmax_scale, causal, -1, -1, 0.0, NULL, rows, n_rows, out,
+                                lse, nthreads);
 }
 
 /* ------------------------------------------------------------------ merge */

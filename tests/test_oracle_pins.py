@@ -514,3 +514,108 @@ def test_kv_write_skips_negative_slots_and_rejects_out_of_range():
     assert int(torch.count_nonzero(kc.float())) == 32
     with pytest.raises(ValueError):
         oracle.kv_write(k, k, kc, vc, torch.tensor([0, 1, 32]))
+
+
+# ------------------------------------------ variants: window, soft cap, sinks
+# "FlashAttention deep dive", flash_attn_varlen_func arguments window_size,
+# softcap and s_aux, and its table of supported variants (sliding window,
+# soft cap, attention sinks); readings in oracle/attn_oracle.c.
+
+def _dense(b, **kw):
+    cuk = [0] + np.cumsum(b.kv_lens).tolist()
+    return oracle.dense_masked_attention(b.q.double(), b.k_tok.double(), b.v_tok.double(),
+                                         b.cu_seqlens_q.tolist(), cuk, b.softmax_scale,
+                                         causal=b.causal, **kw)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("window,softcap,with_sinks", [
+    ((3, -1), 0.0, False), ((0, -1), 0.0, False), ((5, 2), 0.0, False), ((-1, 1), 0.0, False),
+    ((-1, -1), 2.5, False), ((-1, -1), 0.0, True), ((4, 0), 1.5, True), ((2, 3), 0.7, True)])
+def test_variants_equal_dense_brute_force(causal, window, softcap, with_sinks):
+    """The paged per-row oracle with a window, a soft cap and sinks equals
+    the dense whole-matrix formulation (mask matrix, np.tanh on the score
+    matrix, the sink as an extra score column with a zero value row)."""
+    rng = np.random.default_rng(30 + int(causal))
+    q_lens = [5, 1, 9, 3]
+    kv = [12, 7, 9, 20]
+    b = W.make_batch(q_lens, kv, Hq=6, Hkv=2, D=32, bs=16, seed=31, causal=causal)
+    sinks = rng.normal(0.0, 1.5, 6) if with_sinks else None
+    out, lse = run(b, window=window, softcap=softcap, sinks=sinks)
+    ref, ref_lse, _ = _dense(b, window=window, softcap=softcap, sinks=sinks)
+    np.testing.assert_allclose(out.numpy(), ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse.numpy(), ref_lse, rtol=0, atol=1e-12)
+
+
+def test_window_zero_left_returns_the_diagonal_value():
+    """Causal with a window of no keys to the left: query i sees only its
+    own position ctx + i, so out = V_{ctx+i} exactly and lse = its score."""
+    b = W.make_batch([4, 2], [10, 2], Hq=2, Hkv=1, D=16, bs=16, seed=32)
+    out, lse = run(b, window=(0, -1))
+    t = 0
+    for r, (ql, kl) in enumerate(zip(b.q_lens, b.kv_lens)):
+        k, v = key_rows(b, r)
+        for i in range(ql):
+            j = kl - ql + i
+            for h in range(2):
+                assert torch.equal(out[t, h], v[j, 0].double())
+                s = b.softmax_scale * float((b.q[t, h].double() * k[j, 0].double()).sum())
+                assert abs(float(lse[t, h]) - s) < 1e-12
+            t += 1
+
+
+def test_wide_window_and_minus_inf_sink_change_nothing():
+    """A window wider than every request, and sinks of -inf, select the
+    same keys and weights as plain attention: results are identical."""
+    b = W.make_batch([6, 1, 3], [9, 30, 3], Hq=4, Hkv=2, D=16, bs=16, seed=33)
+    kc, vc = cache_of(b)
+    out0, lse0 = run(b, kc, vc)
+    out1, lse1 = run(b, kc, vc, window=(64, 64))
+    out2, lse2 = run(b, kc, vc, sinks=[-math.inf] * 4)
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    assert torch.equal(out0, out2) and torch.equal(lse0, lse2)
+
+
+def test_huge_softcap_is_no_cap():
+    """c * tanh(s / c) -> s as c grows (the error is about s^3 / (3 c^2))."""
+    b = W.make_batch([5], [11], Hq=2, Hkv=1, D=32, bs=16, seed=34)
+    out0, lse0 = run(b)
+    out1, lse1 = run(b, softcap=1e6)
+    assert float((out0 - out1).abs().max()) < 1e-9
+    assert float((lse0 - lse1).abs().max()) < 1e-9
+
+
+def test_softcap_bounds_every_logit():
+    """With cap c every logit lies in (-c, c), so lse <= c + log(#keys)
+    however large the raw scores are."""
+    b = W.make_batch([3], [40], Hq=2, Hkv=1, D=32, bs=16, seed=35)
+    b.q = (b.q.float() * 50).to(torch.bfloat16)       # raw scores in the hundreds
+    out, lse = run(b, softcap=2.0)
+    for i in range(3):
+        nk = 40 - 3 + i + 1
+        assert float(lse[i].max()) <= 2.0 + math.log(nk) + 1e-12
+
+
+def test_sink_is_a_merge_with_an_empty_value_state():
+    """A sink z joins the normalisation with value 0: the result equals the
+    log-sum-exp merge ("FlashAttention deep dive", 合并算法) of the plain
+    state with the state (out 0, lse z)."""
+    b = W.make_batch([4, 2], [13, 2], Hq=4, Hkv=2, D=16, bs=16, seed=36)
+    kc, vc = cache_of(b)
+    z = [0.5, -2.0, 3.0, 1.0]
+    out, lse = run(b, kc, vc, sinks=z)
+    po, pl = run(b, kc, vc)
+    T = b.q.shape[0]
+    zl = torch.tensor(z, dtype=torch.float64).repeat(T)
+    mo, ml = oracle.merge_states(po.reshape(-1, 16), pl.reshape(-1), torch.zeros(T * 4, 16,
+                                 dtype=torch.float64), zl)
+    assert float((out.reshape(-1, 16) - mo).abs().max()) < 1e-12
+    assert float((lse.reshape(-1) - ml).abs().max()) < 1e-12
+
+
+def test_sink_without_keys_gives_zero_and_the_sink():
+    """No visible key but a sink: out = 0 and lse = z."""
+    b = W.make_batch([2, 1], [2, 0], Hq=2, Hkv=1, D=16, bs=16, seed=37, causal=False)
+    out, lse = run(b, sinks=[0.25, -1.0])
+    assert torch.equal(out[2], torch.zeros(2, 16, dtype=torch.float64))
+    assert lse[2].tolist() == [0.25, -1.0]
