@@ -137,6 +137,39 @@ attn_status attn_varlen_prefill(
     int num_splits, void *workspace, size_t ws_bytes, attn_stream_t stream);
 
 /*
+ * attn_varlen_prefill_ext -- attn_varlen_prefill with the attention
+ * variants of [vLLM-FA]'s argument table and variant list (window_size,
+ * softcap, s_aux: sliding window, soft cap on the logits, attention sinks).
+ * The page names them without formulas; the readings are:
+ *   window_left, window_right: query i at absolute position p = ctx + i
+ *     sees keys j with p - window_left <= j <= p + window_right, on top of
+ *     the causal rule and j < kv_len; -1 leaves that side unlimited.
+ *   softcap > 0: each logit s = softmax_scale * k_descale * q . K_j
+ *     becomes softcap * tanh(s / softcap) before the softmax; 0 = off.
+ *   sinks: NULL, or a DEVICE array of Hq fp32 logits (natural-log units);
+ *     the sink z_h of query head h joins the normalisation with a zero
+ *     value vector:
+ *       out = sum_j e^{s_j} V_j / (e^{z_h} + sum_j e^{s_j}),
+ *       lse = log(e^{z_h} + sum_j e^{s_j})
+ *     (a query with no visible key then gets out = 0, lse = z_h).
+ * Errors as attn_varlen_prefill, plus ATTN_ERR_SHAPE for a window bound
+ * below -1 or a negative or NaN softcap.  attn_varlen_prefill is this call
+ * with window (-1, -1), softcap 0 and no sinks.
+ */
+attn_status attn_varlen_prefill_ext(
+    const void *q, int64_t q_stride_tok,
+    const void *k_cache, const void *v_cache,
+    void *out, int64_t out_stride_tok, float *lse_out,
+    const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+    const int32_t *block_table, int64_t bt_row_stride,
+    int B, int total_q, int max_seqlen_q, int max_seqlen_k,
+    int Hq, int Hkv, int D, int block_size, int num_blocks,
+    attn_dtype q_dtype, attn_dtype kv_dtype,
+    float softmax_scale, int causal, float k_descale, float v_descale,
+    int window_left, int window_right, float softcap, const float *sinks,
+    int num_splits, void *workspace, size_t ws_bytes, attn_stream_t stream);
+
+/*
  * attn_paged_decode -- one query token per request ([MR] sec. 9: the decode
  * row is the last row of the causal matrix, so all kv_len = seq_lens[r]
  * keys are visible).  q and out are [B, Hq, D] contiguous, lse_out [B, Hq].

@@ -171,3 +171,30 @@ def test_workspace_and_split_rules(lib):
     for B, L in ((64, 4096), (4, 32768), (128, 16384), (1, 2048)):
         s = va.attn_num_splits(B, 1, L, 32, 8, 152)
         assert 1 <= s <= 256 and (L // 64) >= s or s == 1
+
+
+def prefill_ext(lib, wl=-1, wr=-1, cap=0.0, sinks=None, **kw):
+    a = dict(q=FAKE, qs=8 * 128, k=FAKE, v=FAKE, out=FAKE, os=8 * 128, lse=None, cu=FAKE, su=FAKE,
+             bt=FAKE, bts=4, B=2, T=10, mq=6, mk=6, Hq=8, Hkv=2, D=128, bs=16, nb=4, qd=BF16,
+             kd=BF16, scale=0.125, causal=1, kds=1.0, vds=1.0, ns=1, ws=None, wsb=0)
+    a.update(kw)
+    return lib.attn_varlen_prefill_ext(a["q"], a["qs"], a["k"], a["v"], a["out"], a["os"], a["lse"], a["cu"],
+                                       a["su"], a["bt"], a["bts"], a["B"], a["T"], a["mq"], a["mk"], a["Hq"],
+                                       a["Hkv"], a["D"], a["bs"], a["nb"], a["qd"], a["kd"], a["scale"],
+                                       a["causal"], a["kds"], a["vds"], wl, wr, cap, sinks, a["ns"], a["ws"],
+                                       a["wsb"], None)
+
+
+@pytest.mark.parametrize("wl,wr,cap,status", [
+    (-2, -1, 0.0, ERR_SHAPE), (-1, -3, 0.0, ERR_SHAPE), (-1, -1, -1.0, ERR_SHAPE),
+    (-1, -1, float("nan"), ERR_SHAPE), (-1, -1, float("inf"), ERR_SHAPE),
+    (0, 0, 0.0, None), (16, -1, 30.0, None)])
+def test_variant_validation(lib, wl, wr, cap, status):
+    """attn_varlen_prefill_ext: window bounds below -1 and negative, NaN or
+    infinite soft caps are refused before any launch; valid ones get past
+    validation (here they then fail for want of a device)."""
+    st = prefill_ext(lib, wl=wl, wr=wr, cap=cap)
+    if status is None:
+        assert st in (ERR_CUDA, ERR_DEV, OK)
+    else:
+        assert st == status

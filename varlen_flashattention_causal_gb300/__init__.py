@@ -53,6 +53,11 @@ def _load():
         vp, i64, vp, vp, vp, i64, vp, vp, vp, vp, i64,
         i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
         f32, i32, f32, f32, i32, vp, sz, vp]
+    lib.attn_varlen_prefill_ext.restype = i32
+    lib.attn_varlen_prefill_ext.argtypes = [
+        vp, i64, vp, vp, vp, i64, vp, vp, vp, vp, i64,
+        i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+        f32, i32, f32, f32, i32, i32, f32, vp, i32, vp, sz, vp]
     lib.attn_paged_decode.restype = i32
     lib.attn_paged_decode.argtypes = [
         vp, vp, vp, vp, vp, vp, vp, i64,
@@ -124,14 +129,18 @@ def _sms(device):
 
 def attn_varlen_prefill(q, k_cache, v_cache, out, cu_seqlens_q, seqused_k, block_table,
                         max_seqlen_q, max_seqlen_k, softmax_scale, causal=True, lse_out=None,
-                        k_descale=1.0, v_descale=1.0, num_splits=0, workspace=None, stream=None):
+                        k_descale=1.0, v_descale=1.0, num_splits=0, workspace=None, stream=None,
+                        window=(-1, -1), softcap=0.0, sinks=None):
     """flash_attn_varlen_func over a paged cache (see include/attn.h).
 
     q, out: [T, Hq, D] (token stride may exceed Hq * D); k_cache, v_cache:
     [num_blocks, block_size, Hkv, D]; cu_seqlens_q [B+1], seqused_k [B],
     block_table [B, >=max_blocks] int32 (row stride taken from the tensor);
     lse_out: optional [T, Hq] fp32.  num_splits 0 = automatic; the
-    workspace is allocated here when not given.
+    workspace is allocated here when not given.  Variants
+    (attn_varlen_prefill_ext): window = (left, right) keys around each
+    query's position (-1 unlimited), softcap (0 = off), sinks: optional
+    [Hq] fp32 CUDA tensor of per-head sink logits.
     """
     lib = _load()
     T, Hq, D = q.shape
@@ -146,12 +155,16 @@ def attn_varlen_prefill(q, k_cache, v_cache, out, cu_seqlens_q, seqused_k, block
     ns = num_splits if num_splits > 0 else attn_num_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv,
                                                            _sms(q.device))
     ws, ws_bytes = _workspace(T, Hq, D, ns, q.device, workspace)
-    st = lib.attn_varlen_prefill(
+    if sinks is not None and (sinks.dtype != torch.float32 or sinks.numel() != Hq or not sinks.is_contiguous()
+                              or not sinks.is_cuda):
+        raise TypeError("sinks must be a contiguous CUDA float32 tensor of Hq elements")
+    st = lib.attn_varlen_prefill_ext(
         _p(q), q.stride(0), _p(k_cache), _p(v_cache), _p(out), out.stride(0), _p(lse_out),
         _p(cu_seqlens_q), _p(seqused_k), _p(block_table), block_table.stride(0),
         B, T, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, bs, nb,
         _dt(q), _dt(k_cache), float(softmax_scale), int(bool(causal)),
-        float(k_descale), float(v_descale), int(num_splits), _p(ws), ws_bytes, _stream(stream))
+        float(k_descale), float(v_descale), int(window[0]), int(window[1]), float(softcap), _p(sinks),
+        int(num_splits), _p(ws), ws_bytes, _stream(stream))
     _check("attn_varlen_prefill", st)
     return out
 

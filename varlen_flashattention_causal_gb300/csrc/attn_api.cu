@@ -135,6 +135,9 @@ struct FwdArgs {
     void *ws;
     size_t ws_bytes;
     cudaStream_t stream;
+    int window_left = -1, window_right = -1;
+    float softcap = 0.f;
+    const float *sinks = nullptr;
 };
 
 attn_status validate_fwd(const FwdArgs &a) {
@@ -154,6 +157,7 @@ attn_status validate_fwd(const FwdArgs &a) {
         return ATTN_ERR_ALIGN;
     if (!(a.scale == a.scale) || !(a.k_descale == a.k_descale) || !(a.v_descale == a.v_descale))
         return ATTN_ERR_SHAPE;
+    if (a.window_left < -1 || a.window_right < -1 || !(a.softcap >= 0.f) || isinf(a.softcap)) return ATTN_ERR_SHAPE;
     return ATTN_OK;
 }
 
@@ -167,7 +171,17 @@ attn_status run_fwd(const FwdArgs &a) {
 
     const int G = a.Hq / a.Hkv;
     const bool uniform = (long long)a.T == (long long)a.B * a.max_q;
-    const Plan pl = make_plan(a.B, a.max_q, a.max_k, uniform, a.Hq, a.Hkv, a.D, a.q_dtype, a.kv_dtype, dev->sms);
+    // a window bound at least max_seqlen_k long excludes nothing
+    const int wl = (a.window_left >= a.max_k) ? -1 : a.window_left;
+    const int wr = (a.window_right >= a.max_k) ? -1 : a.window_right;
+    // keys one CTA can see: with a left window bound, at most the window
+    // plus the CTA's query span (and the right bound), from a tile-aligned
+    // start; this sizes the split segments
+    long long span_k = a.max_k;
+    if (wl >= 0 && (a.causal || wr >= 0))
+        span_k = std::min<long long>(span_k, (long long)wl + a.max_q + std::max(wr, 0) + kTileN);
+    const int max_k_eff = (int)span_k;
+    const Plan pl = make_plan(a.B, a.max_q, max_k_eff, uniform, a.Hq, a.Hkv, a.D, a.q_dtype, a.kv_dtype, dev->sms);
     int ns_s = pl.small ? pl.ns_small : 1, ns_b = pl.big ? pl.ns_big : 1;
     if (a.num_splits > 0) {
         ns_s = pl.small ? std::min(a.num_splits, kMaxSplits) : 1;
@@ -210,6 +224,13 @@ attn_status run_fwd(const FwdArgs &a) {
     p.scale_log2 = a.scale * a.k_descale * 1.4426950408889634f;
     p.v_descale = a.v_descale;
     p.err = dev->err;
+    p.window_left = wl;
+    p.window_right = wr;
+    if (a.softcap > 0.f) {
+        p.cap_in = a.scale * a.k_descale / a.softcap;
+        p.cap_out = a.softcap * 1.4426950408889634f;
+    }
+    p.sinks = a.sinks;
     p.part_stride = stride;
     if (stride > 1) {
         p.part_o = static_cast<float *>(a.ws);
@@ -218,7 +239,7 @@ attn_status run_fwd(const FwdArgs &a) {
     // every segment spans a whole number of K/V tiles
     auto chunk_for = [&](int ns) {
         if (ns <= 1) return 1 << 30;
-        const int per = (a.max_k + ns - 1) / ns;
+        const int per = (max_k_eff + ns - 1) / ns;
         return ((per + kTileN - 1) / kTileN) * kTileN;
     };
 
@@ -327,6 +348,21 @@ attn_status attn_varlen_prefill(const void *q, int64_t q_stride_tok, const void 
                                 int block_size, int num_blocks, attn_dtype q_dtype, attn_dtype kv_dtype,
                                 float softmax_scale, int causal, float k_descale, float v_descale, int num_splits,
                                 void *workspace, size_t ws_bytes, attn_stream_t stream) {
+    return attn_varlen_prefill_ext(q, q_stride_tok, k_cache, v_cache, out, out_stride_tok, lse_out, cu_seqlens_q,
+                                   seqused_k, block_table, bt_row_stride, B, total_q, max_seqlen_q, max_seqlen_k, Hq,
+                                   Hkv, D, block_size, num_blocks, q_dtype, kv_dtype, softmax_scale, causal,
+                                   k_descale, v_descale, -1, -1, 0.f, nullptr, num_splits, workspace, ws_bytes,
+                                   stream);
+}
+
+attn_status attn_varlen_prefill_ext(const void *q, int64_t q_stride_tok, const void *k_cache, const void *v_cache,
+                                    void *out, int64_t out_stride_tok, float *lse_out, const int32_t *cu_seqlens_q,
+                                    const int32_t *seqused_k, const int32_t *block_table, int64_t bt_row_stride,
+                                    int B, int total_q, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                                    int block_size, int num_blocks, attn_dtype q_dtype, attn_dtype kv_dtype,
+                                    float softmax_scale, int causal, float k_descale, float v_descale,
+                                    int window_left, int window_right, float softcap, const float *sinks,
+                                    int num_splits, void *workspace, size_t ws_bytes, attn_stream_t stream) {
     FwdArgs a{};
     a.q = q;
     a.q_stride = q_stride_tok;
@@ -358,6 +394,10 @@ attn_status attn_varlen_prefill(const void *q, int64_t q_stride_tok, const void 
     a.ws = workspace;
     a.ws_bytes = ws_bytes;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
+    a.window_left = window_left;
+    a.window_right = window_right;
+    a.softcap = softcap;
+    a.sinks = sinks;
     if (B > 0 && !cu_seqlens_q) return ATTN_ERR_NULL;
     return run_fwd(a);
 }

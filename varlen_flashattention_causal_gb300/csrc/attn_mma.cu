@@ -101,20 +101,31 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     const int row_end = min(row0 + ROWS, rows);
     const int ctx = kv_len - q_len;                  // cached context before the queries
     const int i_min = row0 / G, i_max = (row_end - 1) / G;
+    // keys any row of the block may see: up to the last row's causal /
+    // right-window bound, from the first row's left-window bound (rounded
+    // down to a tile); segments cut that range into whole tiles
     int kv_end = kv_len;
     if (p.causal) kv_end = min(kv_len, ctx + i_max + 1);
-    const int kv_lo = s_idx * p.split_chunk;
-    const int kv_hi = min(kv_end, kv_lo + p.split_chunk);
+    if (p.window_right >= 0) kv_end = (int)min((long long)kv_end, (long long)ctx + i_max + p.window_right + 1);
+    const int kv_beg = (p.window_left >= 0) ? (max(0, ctx + i_min - p.window_left) & ~(BN - 1)) : 0;
+    const long long kv_lo_ll = (long long)kv_beg + (long long)s_idx * p.split_chunk;
+    const int kv_lo = (int)min(kv_lo_ll, (long long)INT_MAX);
+    const int kv_hi = (int)min((long long)kv_end, kv_lo_ll + p.split_chunk);
 
     if (kv_lo >= kv_hi) {
-        // no key in this segment for any row of the block: empty state
+        // no key in this segment for any row of the block: empty state (a
+        // sink alone, in segment 0)
         for (int pr = row0 + tid; pr < row_end; pr += blockDim.x) {
             const int64_t tok = q_start + pr / G;
             const int h = kvh * G + pr % G;
+            const float zl = (p.sinks && s_idx == 0) ? p.sinks[h] : -INFINITY;
             if (p.nsplit > 1) {
-                p.part_lse[(tok * p.Hq + h) * p.part_stride + s_idx] = -INFINITY;
+                const int64_t slot = (tok * p.Hq + h) * p.part_stride + s_idx;
+                p.part_lse[slot] = zl;
+                if (zl != -INFINITY)
+                    for (int d = 0; d < D; ++d) p.part_o[slot * D + d] = 0.f;
             } else {
-                if (p.lse) p.lse[tok * p.Hq + h] = -INFINITY;
+                if (p.lse) p.lse[tok * p.Hq + h] = zl;
                 using OT = typename Elem<C::QT>::T;
                 OT *o = reinterpret_cast<OT *>(p.out) + tok * p.out_stride + (int64_t)h * D;
                 for (int d = 0; d < D; ++d) o[d] = OT(0.f);
@@ -267,8 +278,18 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     // query token (local index) of the two rows this thread owns in C frags
     const int ir0 = (row0 + wm * 16 + (lane >> 2)) / G;
     const int ir1 = (row0 + wm * 16 + (lane >> 2) + 8) / G;
-    const int lim0 = p.causal ? ctx + ir0 : INT_MAX;   // last visible key of row 0
-    const int lim1 = p.causal ? ctx + ir1 : INT_MAX;
+    // visible keys of the two rows: [lo, lim]
+    auto last_key = [&](int ir) -> int {
+        long long l = p.causal ? (long long)ctx + ir : (long long)INT_MAX;
+        if (p.window_right >= 0) l = min(l, (long long)ctx + ir + p.window_right);
+        return (int)l;
+    };
+    const int lim0 = last_key(ir0), lim1 = last_key(ir1);
+    const int lo0 = (p.window_left >= 0) ? ctx + ir0 - p.window_left : INT_MIN;
+    const int lo1 = (p.window_left >= 0) ? ctx + ir1 - p.window_left : INT_MIN;
+    // soft cap: raw score -> cap * log2(e) * tanh(score * scale * k_descale / cap)
+    const bool capped = p.cap_in > 0.f;
+    const float cap_in = (C::KVT == DT_E4M3) ? p.cap_in * kE4m3Lo8Scale : p.cap_in;
 
     float o[D / 8][4];
 #pragma unroll
@@ -338,18 +359,30 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         // scale to log2 units; mask only tiles crossing the sequence end or
         // the causal diagonal ("full" tiles skip this, sec. 4)
         const bool need_mask =
-            (n0 + BN > kv_hi) || (p.causal && tile_kind(i_min, i_max + 1, n0, n0 + BN, ctx) != 1);
+            (n0 + BN > kv_hi) || (p.causal && tile_kind(i_min, i_max + 1, n0, n0 + BN, ctx) != 1) ||
+            (p.window_left >= 0 && n0 < ctx + i_max - p.window_left) ||
+            (p.window_right >= 0 && (long long)n0 + BN - 1 > (long long)ctx + i_min + p.window_right);
+        if (capped) {
 #pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt) {
+            for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float v = s[nt][e] * sl2;
-                if (need_mask) {
+                for (int e = 0; e < 4; ++e) s[nt][e] = p.cap_out * tanh_ex2(s[nt][e] * cap_in);
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] *= sl2;
+        }
+        if (need_mask) {
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
                     const int key = n0 + wn * C::NW + nt * 8 + 2 * (lane & 3) + (e & 1);
                     const int lim = (e >> 1) ? lim1 : lim0;
-                    if (key >= kv_hi || key > lim) v = -INFINITY;
+                    const int lo = (e >> 1) ? lo1 : lo0;
+                    if (key >= kv_hi || key > lim || key < lo) s[nt][e] = -INFINITY;
                 }
-                s[nt][e] = v;
             }
         }
 
@@ -463,14 +496,23 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
                 acc.w += sc * v.w;
             }
         }
-        const float inv = lf > 0.f ? vds / lf : 0.f;
+        const int64_t tok = q_start + pr / G;
+        const int h = kvh * G + pr % G;
+        float sink_scale = 1.f;
+        if (p.sinks && s_idx == 0 && p.sinks[h] > -INFINITY) {
+            // the sink joins segment 0's state: a virtual key with logit z, value 0
+            const float z2 = p.sinks[h] * 1.4426950408889634f;
+            const float mn = fmaxf(mf, z2);
+            sink_scale = (mf == -INFINITY) ? 0.f : ex2(mf - mn);
+            lf = lf * sink_scale + ex2(z2 - mn);
+            mf = mn;
+        }
+        const float inv = lf > 0.f ? vds * sink_scale / lf : 0.f;
         acc.x *= inv;
         acc.y *= inv;
         acc.z *= inv;
         acc.w *= inv;
         const float lse_v = lf > 0.f ? (mf + __log2f(lf)) * 0.6931471805599453f : -INFINITY;
-        const int64_t tok = q_start + pr / G;
-        const int h = kvh * G + pr % G;
         if (p.nsplit == 1) {
             using OT = typename Elem<C::QT>::T;
             OT *dst = reinterpret_cast<OT *>(p.out) + tok * p.out_stride + (int64_t)h * D + c4 * 4;

@@ -128,11 +128,17 @@ __device__ __forceinline__ void derive(const FwdParams &p, Item &it) {
     it.row_end = min(it.row0 + 2 * kBM, rows);
     it.ntiles_q = (it.row_end - it.row0 + kBM - 1) / kBM;
     it.ctx = it.kv_len - it.q_len;
-    const int i_max = (it.row_end - 1) / p.G;
+    const int i_min = it.row0 / p.G, i_max = (it.row_end - 1) / p.G;
+    // keys any row of the item may see: up to the last row's causal /
+    // right-window bound, from the first row's left-window bound rounded
+    // down to a tile (a multiple of every page-load height)
     int kv_end = it.kv_len;
     if (p.causal) kv_end = min(it.kv_len, it.ctx + i_max + 1);
-    it.kv_lo = it.s * p.split_chunk;
-    it.kv_hi = min(kv_end, it.kv_lo + p.split_chunk);
+    if (p.window_right >= 0) kv_end = (int)min((long long)kv_end, (long long)it.ctx + i_max + p.window_right + 1);
+    const int kv_beg = (p.window_left >= 0) ? (max(0, it.ctx + i_min - p.window_left) & ~(kBN - 1)) : 0;
+    const long long lo = (long long)kv_beg + (long long)it.s * p.split_chunk;
+    it.kv_lo = (int)min(lo, (long long)INT_MAX);
+    it.kv_hi = (int)min((long long)kv_end, lo + p.split_chunk);
     it.n_kv = it.kv_hi > it.kv_lo ? (it.kv_hi - it.kv_lo + kBN - 1) / kBN : 0;
 }
 
@@ -542,8 +548,12 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const uint32_t tO = tmem + lane_base + col_o(x);
         // e4m3 tiles hold value * 2^-8 (see e4m3x4_to_h2x2_lo8): scale S and O back
-        const float sl2 = FP8 ? p.scale_log2 * kE4m3Lo8Scale : p.scale_log2;
         const float vds = FP8 ? p.v_descale * kE4m3Lo8Scale : p.v_descale;
+        // soft cap: S -> cap * log2(e) * tanh(S * scale * k_descale / cap),
+        // already in log2 units; else S * scale * k_descale * log2(e)
+        const bool capped = p.cap_in > 0.f;
+        const float cap_in = FP8 ? p.cap_in * kE4m3Lo8Scale : p.cap_in;
+        const float sl2 = capped ? 1.f : (FP8 ? p.scale_log2 * kE4m3Lo8Scale : p.scale_log2);
         int Lbase = 0, jx = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -551,14 +561,19 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
             ok = read_item(k, it);
             if (!ok || it.r < 0) break;
             if (it.n_kv == 0) {
-                // no key for any row in this segment: empty state, no pipeline work
+                // no key for any row in this segment: empty state (a sink
+                // alone, in segment 0), no pipeline work
                 for (int pr = it.row0 + (tid - 64); pr < it.row_end; pr += 256) {
                     const int64_t tok = it.q_start + pr / G;
                     const int h = it.kvh * G + pr % G;
+                    const float zl = (p.sinks && it.s == 0) ? p.sinks[h] : -INFINITY;
                     if (p.nsplit > 1) {
-                        p.part_lse[(tok * p.Hq + h) * p.part_stride + it.s] = -INFINITY;
+                        const int64_t slot = (tok * p.Hq + h) * p.part_stride + it.s;
+                        p.part_lse[slot] = zl;
+                        if (zl != -INFINITY)
+                            for (int d = 0; d < kD; ++d) p.part_o[slot * kD + d] = 0.f;
                     } else {
-                        if (p.lse) p.lse[tok * p.Hq + h] = -INFINITY;
+                        if (p.lse) p.lse[tok * p.Hq + h] = zl;
                         uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
                                                              (tok * p.out_stride + (int64_t)h * kD) * 2);
                         for (int c = 0; c < kD / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
@@ -571,7 +586,10 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                 const int prow = it.row0 + x * kBM + trow;  // packed row within the request
                 const bool row_ok = prow < it.row_end;
                 const int qi = prow / G;                    // local query index
-                const int lim = p.causal ? it.ctx + qi : INT_MAX;
+                long long lim_ll = p.causal ? (long long)it.ctx + qi : (long long)INT_MAX;
+                if (p.window_right >= 0) lim_ll = min(lim_ll, (long long)it.ctx + qi + p.window_right);
+                const int lim = (int)lim_ll;                // last visible key of this row
+                const int lo_key = (p.window_left >= 0) ? it.ctx + qi - p.window_left : INT_MIN;
                 float m_ref = -INFINITY;                    // reference maximum (log2 units)
                 float l = 0.f;
                 // query range of this Q tile, for the tile classification
@@ -584,7 +602,9 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                     const int b = jg & 1;
                     const uint32_t tS = tmem + lane_base + col_s(x, b);
                     const bool need_mask =
-                        (n0 + kBN > kv_hi) || (p.causal && tile_kind(tq_lo, tq_hi, n0, n0 + kBN, it.ctx) != 1);
+                        (n0 + kBN > kv_hi) || (p.causal && tile_kind(tq_lo, tq_hi, n0, n0 + kBN, it.ctx) != 1) ||
+                        (p.window_left >= 0 && n0 < it.ctx + tq_hi - 1 - p.window_left) ||
+                        (p.window_right >= 0 && (long long)n0 + kBN - 1 > (long long)it.ctx + tq_lo + p.window_right);
                     ok = warp_wait(bar(B_SFULL(x, b)), (jg >> 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
@@ -596,12 +616,21 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                         tmem_ld32(tS + 32, v1);
                         tmem_wait_ld();
                     }
-                    // masked keys: this row sees keys n0 .. n0 + nv - 1 of the tile
-                    const int nv = need_mask ? max(0, min(kBN, nlim - n0 + 1)) : kBN;
-                    if (nv < kBN) {
+                    if (capped) {
 #pragma unroll
                         for (int e = 0; e < kBN; ++e)
-                            if (e >= nv) v[e] = __float_as_uint(-INFINITY);
+                            v[e] = __float_as_uint(p.cap_out * tanh_ex2(__uint_as_float(v[e]) * cap_in));
+                    }
+                    // masked keys: this row sees keys n0 + e_lo .. n0 + nv - 1 of the tile
+                    int nv = kBN, e_lo = 0;
+                    if (need_mask) {
+                        nv = max(0, min(kBN, nlim - n0 + 1));
+                        if (p.window_left >= 0) e_lo = min(kBN, max(0, lo_key - n0));
+                    }
+                    if (nv < kBN || e_lo > 0) {
+#pragma unroll
+                        for (int e = 0; e < kBN; ++e)
+                            if (e >= nv || e < e_lo) v[e] = __float_as_uint(-INFINITY);
                     }
                     // row maximum: three-input max in four independent chains
                     // (the softmax is issue bound: fewer instructions per element
@@ -693,10 +722,19 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                 }
                 if (ok) {
                     tc_fence_after();
-                    const float inv = l > 0.f ? vds / l : 0.f;
-                    const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
                     const int64_t tok = it.q_start + qi;
                     const int h = it.kvh * G + prow % G;
+                    float sink_scale = 1.f;
+                    if (row_ok && p.sinks && it.s == 0 && p.sinks[h] > -INFINITY) {
+                        // the sink joins segment 0's state: a virtual key with logit z, value 0
+                        const float z2 = p.sinks[h] * 1.4426950408889634f;
+                        const float mn = fmaxf(m_ref, z2);
+                        sink_scale = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mn);
+                        l = l * sink_scale + ex2(z2 - mn);
+                        m_ref = mn;
+                    }
+                    const float inv = l > 0.f ? vds * sink_scale / l : 0.f;
+                    const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
 #pragma unroll
                     for (int c = 0; c < kD / 32; ++c) {
                         uint32_t o[32];

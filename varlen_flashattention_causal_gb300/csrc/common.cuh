@@ -114,6 +114,14 @@ __device__ __forceinline__ int4 ldg_nc16(const void *p) {
 }
 
 // raise bits of the device error word (first writer wins nothing; OR only)
+// tanh(y) = 1 - 2 / (1 + e^(2y)), e^(2y) = 2^(2 y log2 e) by ex2; the
+// exponent is clamped to +-60, where the result is +-1 in fp32 anyway.
+// Absolute error about 1e-7 (the soft cap multiplies it by the cap).
+__device__ __forceinline__ float tanh_ex2(float y) {
+    const float t = fminf(fmaxf(2.8853900817779268f * y, -60.f), 60.f);
+    return 1.f - __fdividef(2.f, 1.f + ex2(t));
+}
+
 // Programmatic dependent launch.  Every kernel of the library is launched
 // with programmatic stream serialisation, so it may be scheduled while the
 // previous kernel in the stream drains.  pdl_wait() blocks until that

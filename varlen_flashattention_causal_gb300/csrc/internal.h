@@ -41,6 +41,14 @@ struct FwdParams {
     int rows_lo, rows_hi;
     int n_row_blocks;            // row blocks of the largest request of the class
     unsigned *err;
+    // variants: keys p - window_left .. p + window_right around the query's
+    // absolute position p (-1 = unlimited side); soft cap (cap_in =
+    // scale * k_descale / softcap applied to the raw dot product, cap_out =
+    // softcap * log2(e); cap_in = 0: off); per-query-head sink logits
+    // (natural log; nullptr: none), taken into the state of segment 0
+    int window_left, window_right;
+    float cap_in, cap_out;
+    const float *sinks;
 };
 
 // Split-KV reduction over the partial states of every token whose request
