@@ -540,6 +540,37 @@ def run_workload(args):
                    unit="GB/s", ms_per_step=round(med, 4), eager_ms_per_step=round(eager, 4), timing="cuda graph",
                    bytes=by, splits=[ns1, ns2],
                    roofline={"bound": "hbm", "peak": hbm, "frac": round(by / (med * 1e-3) / 1e9 / hbm, 4)})
+    elif args.workload == "swa":
+        b = W.swa_decode(gen_kv=False)
+        kc, vc = _device_cache(b, dev)
+        q, out = b.q.to(dev), torch.empty(b.q.shape, dtype=torch.bfloat16, device=dev)
+        cu, su, bt = b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev)
+        win, sinks = b.extra["window"], b.extra["sinks"].to(dev)
+        span = min(b.max_seqlen_k, win[0] + 1)
+        ns = va.attn_num_splits(b.B, 1, span, b.Hq, b.Hkv, sms)
+        wsp = torch.empty(max(1, va.attn_workspace_size(b.T, b.Hq, b.D, ns)), dtype=torch.uint8, device=dev)
+        fn = lambda: va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt, 1, b.max_seqlen_k, b.softmax_scale,
+                                            causal=True, window=win, sinks=sinks, num_splits=0, workspace=wsp)
+        med, mean = _time(fn, args.steps, args.warmup)
+        # algorithmic bytes: the keys inside each query's window, K and V once per KV head
+        by = sum(min(L, win[0] + 1) for L in b.kv_lens) * b.Hkv * b.D * 2 * 2 + 2 * b.T * b.Hq * b.D * 2
+        res.update(metric="sliding-window decode GB/s (window keys)", value=round(by / (med * 1e-3) / 1e9, 1),
+                   unit="GB/s", ms_per_step=round(med, 4), bytes=by, window=list(win), sinks=True,
+                   roofline={"bound": "hbm", "peak": hbm, "frac": round(by / (med * 1e-3) / 1e9 / hbm, 4)})
+    elif args.workload == "verify":
+        b = W.verify_decode(gen_kv=False)
+        kc, vc = _device_cache(b, dev)
+        q, out = b.q.to(dev), torch.empty(b.q.shape, dtype=torch.bfloat16, device=dev)
+        cu, su, bt = b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev)
+        ns = va.attn_num_splits(b.B, b.max_seqlen_q, b.max_seqlen_k, b.Hq, b.Hkv, sms)
+        wsp = torch.empty(max(1, va.attn_workspace_size(b.T, b.Hq, b.D, ns)), dtype=torch.uint8, device=dev)
+        fn = lambda: va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt, b.max_seqlen_q, b.max_seqlen_k,
+                                            b.softmax_scale, causal=True, num_splits=0, workspace=wsp)
+        med, mean = _time(fn, args.steps, args.warmup)
+        by = decode_bytes(b)
+        res.update(metric="multi-token verify GB/s", value=round(by / (med * 1e-3) / 1e9, 1), unit="GB/s",
+                   ms_per_step=round(med, 4), bytes=by, q_lens=[min(b.q_lens), max(b.q_lens)],
+                   roofline={"bound": "hbm", "peak": hbm, "frac": round(by / (med * 1e-3) / 1e9 / hbm, 4)})
     elif args.workload == "fp8mixed":
         b = W.fp8_mixed(gen_kv=False)
         ks, vs = 4.5 / 448.0, 4.5 / 448.0           # |N(0,1)| max over ~1e8 draws is about 4.5-6
@@ -569,7 +600,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "longctx-bs16", "longctx-bs64", "longctx-bs256", "cascade",
+                    choices=["decode", "prefill", "longctx-bs16", "longctx-bs64", "longctx-bs256", "cascade", "swa",
+                             "verify",
                              "fp8mixed"],
                     help="decode is the benchmark line; the others time one more workload each")
     args = ap.parse_args()

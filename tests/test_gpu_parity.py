@@ -602,3 +602,36 @@ def test_variants_other_paths(D, kv_dtype):
                                       sinks=sinks.double() if use_sinks else None)
             check(out, lse, ro, rl, TOL_FP8 if fp8 else TOL)
     assert_no_device_error()
+
+
+def test_workload_swa_decode_with_sinks():
+    """Sliding-window decode with sinks (the swa bench workload, smaller):
+    window of 1000 keys over contexts of 2k-8k, split-KV over the window."""
+    b = W.swa_decode(B=8, lo=2048, hi=8192, window=1000)
+    kc, vc = gpu_cache(b)
+    win, sinks = b.extra["window"], b.extra["sinks"]
+    dev = torch.device("cuda")
+    q = b.q.to(dev)
+    for ns in (0, 1):
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        va.attn_varlen_prefill(q, kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev),
+                               1, b.max_seqlen_k, b.softmax_scale, lse_out=lse, num_splits=ns, window=win,
+                               sinks=sinks.to(dev))
+        ro, rl = oracle.attention(b.q, *cpu_cache(b), b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                                  window=win, sinks=sinks.double())
+        check(out, lse, ro, rl, TOL)
+    assert_no_device_error()
+
+
+def test_workload_verify_full():
+    """Multi-token verification (the verify bench workload, smaller): 2-8
+    query tokens per request over paged contexts; requests of up to 16
+    packed rows run on the rows-light kernel, longer ones on the
+    tensor-core kernel, all in one call."""
+    b = W.verify_decode(B=32, hi=4096)
+    kc, vc = gpu_cache(b)
+    out, lse = gpu_attn(b, kc, vc)
+    ro, rl = ref_attn(b, *cpu_cache(b))
+    check(out, lse, ro, rl, TOL)
+    assert_no_device_error()

@@ -58,11 +58,17 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t part_o_bytes(int T, int Hq, int D, int ns) { return align256((size_t)T * Hq * ns * D * sizeof(float)); }
 
-// packed rows (q_len * G) up to which a request runs in the rows-light
-// class: the mma.sync kernel with 16-row CTAs (decode: one token x up to 16
-// heads of a group).  Larger requests run on the tcgen05 kernel when it
-// supports the shape, else on the mma.sync kernel sized for the largest one.
-constexpr int kSmallRows = 16;
+// Request classes by packed row count (q_len * G):
+//   0  rows <= 16: decode and short verify rows, mma.sync kernel with 16-row
+//      CTAs (one token x up to 16 heads of a group);
+//   1  17 .. 64 rows: longer verify rows and short chunks, mma.sync kernel
+//      with 32- or 64-row CTAs (memory-bound work, where a 128-row
+//      tensor-core tile would mostly be padding);
+//   2  more than 64 rows: prefill and chunks, tcgen05 kernel.  When the
+//      tcgen05 kernel does not take the shape (head size 64, G not dividing
+//      128) class 1 extends to every request above 16 rows instead.
+constexpr int kLightRows = 16;
+constexpr int kMidRows = 64;
 
 // Split rule.  `base` CTAs run without splitting; `target` is the CTA count
 // that fills every SM twice.  Too few CTAs: cut each request's keys into
@@ -80,12 +86,15 @@ int split_rule(long long base, int max_seqlen_k, long long target, int min_tiles
     return (int)std::max<long long>(s, 1);
 }
 
+struct ClassPlan {
+    bool on;       // launched
+    int lo, hi;    // packed-row range of the class
+    bool tc;       // tcgen05 kernel (else mma.sync with rpc rows per CTA)
+    int rpc;       // rows per CTA
+    int ns;        // segments (automatic choice)
+};
 struct Plan {
-    bool small, big;      // launch the rows-light class (packed rows <= small_rows_hi) / rows-heavy class
-    bool big_tc;          // rows-heavy class on the tcgen05 kernel (else the mma.sync kernel)
-    int rpc;              // rows per CTA of the rows-light mma kernel
-    int small_rows_hi;    // largest packed row count of the rows-light class
-    int ns_small, ns_big; // segments per class (automatic choice)
+    ClassPlan c[3];
 };
 
 // uniform: every request has exactly max_q query tokens (so all requests
@@ -95,22 +104,29 @@ Plan make_plan(int B, int max_q, int max_k, bool uniform, int Hq, int Hkv, int D
     Plan pl{};
     const int G = Hq / Hkv;
     const int max_rows = std::max(1, max_q) * G;
-    pl.big = max_rows > kSmallRows;
-    pl.big_tc = pl.big && tc_supported(D, q_dtype, kv_dtype, G);
-    // a group wider than the class bound leaves the rows-light class empty
-    pl.small = !pl.big || (!uniform && G <= kSmallRows);
-    pl.small_rows_hi = pl.big ? kSmallRows : INT32_MAX;
-    pl.rpc = mma_rows_per_cta(std::min(max_rows, kSmallRows));
-    pl.ns_small = pl.ns_big = 1;
-    if (pl.small) {
-        const long long rb = (std::min(max_rows, kSmallRows) + pl.rpc - 1) / pl.rpc;
-        // decode-like rows: also bound the keys per segment (32 tiles)
-        pl.ns_small = split_rule((long long)B * Hkv * rb, max_k, 6LL * sms, 2, rb == 1 ? 32 : 0);
-    }
-    if (pl.big) {
-        const int rpc_big = pl.big_tc ? tc_rows_per_cta() : mma_rows_per_cta(max_rows);
-        const long long rb = (max_rows + rpc_big - 1) / rpc_big;
-        pl.ns_big = split_rule((long long)B * Hkv * rb, max_k, (pl.big_tc ? 2LL : 4LL) * sms, 4, 0);
+    const bool heavy_tc = tc_supported(D, q_dtype, kv_dtype, G);
+    const int hi[3] = {kLightRows, heavy_tc ? kMidRows : INT32_MAX, INT32_MAX};
+    for (int k = 0; k < 3; ++k) {
+        ClassPlan &c = pl.c[k];
+        c.lo = k == 0 ? 0 : hi[k - 1] + 1;
+        c.hi = hi[k];
+        if (k == 2 && !heavy_tc) continue;                 // folded into class 1
+        // uniform lengths: only max_rows's class; otherwise every class from
+        // the smallest request (one token: G rows) to the largest
+        c.on = uniform ? (max_rows >= c.lo && max_rows <= c.hi) : (max_rows >= c.lo && G <= c.hi);
+        if (!c.on) continue;
+        c.tc = (k == 2);
+        const int rows_cap = std::min(max_rows, c.hi);
+        // (class 1 on 16-row CTAs, each row block re-reading K/V from L2,
+        // measured slower than one CTA for all of a request's rows)
+        c.rpc = c.tc ? tc_rows_per_cta() : (k == 0 ? kLightRows : mma_rows_per_cta(rows_cap));
+        const long long rb = (rows_cap + c.rpc - 1) / c.rpc;
+        if (k == 0)        // decode-like rows: also bound the keys per segment (32 tiles)
+            c.ns = split_rule((long long)B * Hkv * rb, max_k, 4LL * sms, 2, rb == 1 ? 32 : 0);
+        else if (!c.tc)
+            c.ns = split_rule((long long)B * Hkv * rb, max_k, 4LL * sms, 2, rb == 1 ? 32 : 0);
+        else
+            c.ns = split_rule((long long)B * Hkv * rb, max_k, 2LL * sms, 4, 0);
     }
     return pl;
 }
@@ -182,20 +198,22 @@ attn_status run_fwd(const FwdArgs &a) {
         span_k = std::min<long long>(span_k, (long long)wl + a.max_q + std::max(wr, 0) + kTileN);
     const int max_k_eff = (int)span_k;
     const Plan pl = make_plan(a.B, a.max_q, max_k_eff, uniform, a.Hq, a.Hkv, a.D, a.q_dtype, a.kv_dtype, dev->sms);
-    int ns_s = pl.small ? pl.ns_small : 1, ns_b = pl.big ? pl.ns_big : 1;
-    if (a.num_splits > 0) {
-        ns_s = pl.small ? std::min(a.num_splits, kMaxSplits) : 1;
-        ns_b = pl.big ? std::min(a.num_splits, kMaxSplits) : 1;
-    } else {
-        // automatic: cap to what the workspace holds (the layout is sized
-        // by the larger of the two counts)
+    int ns[3];
+    for (int k = 0; k < 3; ++k)
+        ns[k] = !pl.c[k].on ? 1 : (a.num_splits > 0 ? std::min(a.num_splits, kMaxSplits) : pl.c[k].ns);
+    auto ns_max = [&]() { return std::max(ns[0], std::max(ns[1], ns[2])); };
+    if (a.num_splits <= 0) {
+        // automatic: cap to what the workspace holds (its layout is sized by
+        // the largest count)
         auto fits = [&](int n) { return n <= 1 || (a.ws && a.ws_bytes >= attn_workspace_size(a.T, a.Hq, a.D, n)); };
-        while (!fits(std::max(ns_s, ns_b))) {
-            if (ns_s >= ns_b) --ns_s;
-            else --ns_b;
+        while (!fits(ns_max())) {
+            int k = 0;
+            for (int j = 1; j < 3; ++j)
+                if (ns[j] > ns[k]) k = j;
+            --ns[k];
         }
     }
-    const int stride = std::max(ns_s, ns_b);
+    const int stride = ns_max();
     if (stride > 1) {
         if (!a.ws) return ATTN_ERR_WORKSPACE;
         if (a.ws_bytes < attn_workspace_size(a.T, a.Hq, a.D, stride)) return ATTN_ERR_WORKSPACE;
@@ -237,41 +255,27 @@ attn_status run_fwd(const FwdArgs &a) {
         p.part_lse = reinterpret_cast<float *>(static_cast<char *>(a.ws) + part_o_bytes(a.T, a.Hq, a.D, stride));
     }
     // every segment spans a whole number of K/V tiles
-    auto chunk_for = [&](int ns) {
-        if (ns <= 1) return 1 << 30;
-        const int per = (max_k_eff + ns - 1) / ns;
+    auto chunk_for = [&](int n) {
+        if (n <= 1) return 1 << 30;
+        const int per = (max_k_eff + n - 1) / n;
         return ((per + kTileN - 1) / kTileN) * kTileN;
     };
 
     const int max_rows = std::max(1, a.max_q) * G;
-    if (pl.small) {
-        // rows-light requests: mma.sync kernel
-        FwdParams m = p;
-        m.nsplit = ns_s;
-        m.split_chunk = chunk_for(ns_s);
-        m.rows_lo = 0;
-        m.rows_hi = pl.small_rows_hi;
-        m.n_row_blocks = (std::min(max_rows, pl.small_rows_hi) + pl.rpc - 1) / pl.rpc;
-        if ((long long)m.n_row_blocks * ns_s > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-        st = check_cuda(launch_fwd_mma(m, a.D, a.q_dtype, a.kv_dtype, pl.rpc, a.stream));
-        if (st != ATTN_OK) return st;
-    }
-    if (pl.big) {
-        // rows-heavy requests: tcgen05 kernel, or, for shapes it does not
-        // take (head size 64, G not dividing 128), the mma.sync kernel sized
-        // for the largest request
+    for (int k = 0; k < 3; ++k) {
+        const ClassPlan &c = pl.c[k];
+        if (!c.on) continue;
         FwdParams t = p;
-        t.nsplit = ns_b;
-        t.split_chunk = chunk_for(ns_b);
-        t.rows_lo = kSmallRows + 1;
-        t.rows_hi = INT32_MAX;
-        const int rpc_big = pl.big_tc ? tc_rows_per_cta() : mma_rows_per_cta(max_rows);
-        t.n_row_blocks = (max_rows + rpc_big - 1) / rpc_big;
-        if ((long long)t.n_row_blocks * ns_b > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-        if (pl.big_tc)
+        t.nsplit = ns[k];
+        t.split_chunk = chunk_for(ns[k]);
+        t.rows_lo = c.lo;
+        t.rows_hi = c.hi;
+        t.n_row_blocks = (std::min(max_rows, c.hi) + c.rpc - 1) / c.rpc;
+        if ((long long)t.n_row_blocks * ns[k] > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+        if (c.tc)
             st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.kv_dtype, a.T, dev->sms, a.stream));
         else
-            st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, rpc_big, a.stream));
+            st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, c.rpc, a.stream));
         if (st != ATTN_OK) return st;
     }
     if (stride > 1) {
@@ -287,9 +291,12 @@ attn_status run_fwd(const FwdArgs &a) {
         c.Hq = a.Hq;
         c.D = a.D;
         c.G = G;
-        c.small_rows_hi = pl.small ? pl.small_rows_hi : 0;
-        c.ns_small = ns_s;
-        c.ns_big = ns_b;
+        c.max_q = a.max_q;
+        c.rows_hi0 = pl.c[0].hi;
+        c.rows_hi1 = pl.c[1].hi;
+        c.ns0 = ns[0];
+        c.ns1 = ns[1];
+        c.ns2 = ns[2];
         c.part_stride = stride;
         st = check_cuda(launch_combine(c, a.q_dtype, a.stream));
     }
@@ -309,7 +316,10 @@ int attn_num_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, 
     if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || B <= 0) return 1;
     // both request classes may be present: the larger count sizes the workspace
     const Plan pl = make_plan(B, max_seqlen_q, max_seqlen_k, false, Hq, Hkv, 128, ATTN_BF16, ATTN_BF16, num_sms);
-    return std::max(pl.small ? pl.ns_small : 1, pl.big ? pl.ns_big : 1);
+    int n = 1;
+    for (int k = 0; k < 3; ++k)
+        if (pl.c[k].on) n = std::max(n, pl.c[k].ns);
+    return n;
 }
 
 int attn_tile_kind(int q_lo, int q_hi, int k_lo, int k_hi, int ctx) { return tile_kind(q_lo, q_hi, k_lo, k_hi, ctx); }

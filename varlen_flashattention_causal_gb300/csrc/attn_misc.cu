@@ -5,6 +5,7 @@
 //   * combine_kernel    split-KV reduction ("vLLM 中 Attention Kernel 如何并行
 //                       处理多个请求", sec. 12): merge the per-segment states
 //   * merge_kernel      merge_attn_states (cascade attention, stage 3)
+#include <algorithm>
 #include <climits>
 
 #include "common.cuh"
@@ -208,16 +209,17 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
         }
         q_len = p.cu_seqlens_q[lo + 1] - p.cu_seqlens_q[lo];
     }
-    const int ns = (q_len * p.G <= p.small_rows_hi) ? p.ns_small : p.ns_big;
+    const int rows = q_len * p.G;
+    const int ns = rows <= p.rows_hi0 ? p.ns0 : (rows <= p.rows_hi1 ? p.ns1 : p.ns2);
     if (ns <= 1) return;
     combine_row<OT>(p, t, h, ns, lane);
 }
 
-// Rows-light form, for calls in which only rows-light requests were split
-// (the usual case: decode rows next to unsplit prefill chunks).  One CTA
-// per (request, 8 query heads): two loads give the request's class, so the
-// CTAs of rows-heavy requests exit at once instead of one warp per token
-// and head searching for its request.
+// Per-request form, for calls in which no request above 64 packed rows was
+// split (the usual case: decode and verify rows next to unsplit prefill
+// chunks).  One CTA per (request, 8 query heads, query token): two loads
+// give the request's class, so the CTAs of unsplit requests exit at once
+// instead of one warp per token and head searching for its request.
 constexpr int kCombineHeads = 8;
 template <class OT>
 __global__ void __launch_bounds__(32 * kCombineHeads) combine_light_kernel(const CombineParams p) {
@@ -229,19 +231,26 @@ __global__ void __launch_bounds__(32 * kCombineHeads) combine_light_kernel(const
         t0 = p.cu_seqlens_q[r];
         q_len = p.cu_seqlens_q[r + 1] - t0;
     }
-    if (q_len <= 0 || q_len * p.G > p.small_rows_hi) return;
+    const int rows = q_len * p.G;
+    const int ns = rows <= p.rows_hi0 ? p.ns0 : (rows <= p.rows_hi1 ? p.ns1 : p.ns2);
+    if (q_len <= 0 || ns <= 1) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * kCombineHeads + warp;
     if (h >= p.Hq) return;
-    for (int i = 0; i < q_len; ++i) combine_row<OT>(p, t0 + i, h, p.ns_small, lane);
+    for (int i = blockIdx.z; i < q_len; i += gridDim.z) combine_row<OT>(p, t0 + i, h, ns, lane);
 }
 
 cudaError_t launch_combine(const CombineParams &p, int out_dtype, cudaStream_t stream) {
     const int64_t threads = (int64_t)p.T * p.Hq * 32;
     if (threads == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((threads + 127) / 128);
-    if (p.ns_big <= 1 && p.ns_small > 1) {
-        const dim3 g((unsigned)p.B, (unsigned)((p.Hq + kCombineHeads - 1) / kCombineHeads));
+    // per-request form when every split request has at most 64 packed rows
+    // (so at most 64 tokens for a CTA to walk)
+    const bool light = (p.ns2 <= 1) && (p.ns1 <= 1 || p.rows_hi1 <= 64);
+    if (light) {
+        // tokens of a split request: at most 64 packed rows, so at most 64 / G
+        const int zt = std::max(1, std::min(p.max_q, std::max(1, std::max(p.rows_hi0, std::min(p.rows_hi1, 64)) / p.G)));
+        const dim3 g((unsigned)p.B, (unsigned)((p.Hq + kCombineHeads - 1) / kCombineHeads), (unsigned)std::min(zt, 64));
         const dim3 blk(32 * kCombineHeads);
         if (out_dtype == DT_BF16) return launch_pdl(combine_light_kernel<__nv_bfloat16>, g, blk, 0, stream, p);
         if (out_dtype == DT_FP16) return launch_pdl(combine_light_kernel<__half>, g, blk, 0, stream, p);

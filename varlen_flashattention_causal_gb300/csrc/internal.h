@@ -54,7 +54,8 @@ struct FwdParams {
 // Split-KV reduction over the partial states of every token whose request
 // ran with more than one segment.  A token's request is found from
 // cu_seqlens_q (nullptr: token t is request t); its class -- packed rows
-// q_len * G up to small_rows_hi, or above -- gives its segment count.
+// q_len * G up to rows_hi0, up to rows_hi1, or above -- gives its segment
+// count ns0, ns1 or ns2.
 struct CombineParams {
     const float *part_o;
     const float *part_lse;
@@ -62,9 +63,9 @@ struct CombineParams {
     int64_t out_stride;
     float *lse;
     const int32_t *cu_seqlens_q;
-    int B, T, Hq, D, G;
-    int small_rows_hi;
-    int ns_small, ns_big, part_stride;
+    int B, T, Hq, D, G, max_q;
+    int rows_hi0, rows_hi1;
+    int ns0, ns1, ns2, part_stride;
 };
 
 // Launch with programmatic stream serialisation (the kernel calls

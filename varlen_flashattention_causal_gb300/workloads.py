@@ -244,6 +244,38 @@ def fp8_mixed(device="cpu", n_dec=128, n_pre=4, pre_len=2048, lo=128, hi=16384, 
     return _finish(b, g, device, [range(L) for L in kv], gen_kv=gen_kv)
 
 
+def swa_decode(device="cpu", B=64, lo=4096, hi=32768, window=4096, gen_kv=True):
+    """Sliding-window decode with attention sinks: each query sees its last
+    `window` keys (window_left = window - 1); Hq 32 / Hkv 8, D 128, bs 16,
+    contexts U[lo, hi]; one N(0, 1) sink logit per query head."""
+    g = generator(5)
+    ctx = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+    Hq, Hkv, D, bs = 32, 8, 128, 16
+    used = sum((L + bs - 1) // bs for L in ctx)
+    pool = (used * 5 + 3) // 4
+    bt = block_tables(ctx, bs, pool, g)
+    b = Batch("swa-decode", Hq, Hkv, D, bs, pool, [1] * B, ctx, block_table=bt)
+    b.extra["window"] = (window - 1, -1)
+    b.extra["sinks"] = torch.randn((Hq,), generator=g, dtype=torch.float32)
+    return _finish(b, g, device, [range(L) for L in ctx], gen_kv=gen_kv)
+
+
+def verify_decode(device="cpu", B=64, q_lo=2, q_hi=8, lo=512, hi=8192, gen_kv=True):
+    """Multi-token verification (speculative decoding): q_len U[q_lo, q_hi]
+    new tokens per request at the end of a paged context U[lo, hi] (the
+    new tokens' keys included), Hq 32 / Hkv 8, D 128, bs 16, causal."""
+    g = generator(6)
+    ql = torch.randint(q_lo, q_hi + 1, (B,), generator=g).tolist()
+    ctx = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+    kv = [c + q for c, q in zip(ctx, ql)]
+    Hq, Hkv, D, bs = 32, 8, 128, 16
+    used = sum((L + bs - 1) // bs for L in kv)
+    pool = (used * 5 + 3) // 4
+    bt = block_tables(kv, bs, pool, g)
+    b = Batch("verify-decode", Hq, Hkv, D, bs, pool, ql, kv, block_table=bt)
+    return _finish(b, g, device, [range(L) for L in kv], gen_kv=gen_kv)
+
+
 def make_batch(q_lens, kv_lens, Hq, Hkv, D, bs, seed, pool=None, causal=True,
                kv_dtype="bf16", device="cpu", name="custom", q_dtype=torch.bfloat16):
     """A seeded batch of any shape (tests).  All kv_lens tokens of every
