@@ -50,7 +50,7 @@ def _load():
             c.c_void_p, c.c_void_p, c.c_int, c.c_double, c.c_double,
             c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64,
             c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
-            c.c_double, c.c_int, c.c_int64, c.c_int64, c.c_double, c.c_void_p,
+            c.c_double, c.c_int, c.c_int64, c.c_int64, c.c_double, c.c_void_p, c.c_double,
             c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p, c.c_int]
         lib.oracle_merge_states.restype = None
         lib.oracle_merge_states.argtypes = [
@@ -94,7 +94,7 @@ def _host(t, dtype=None):
 
 def attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
               softmax_scale, causal=True, k_scale=1.0, v_scale=1.0,
-              rows=None, nthreads=0, window=(-1, -1), softcap=0.0, sinks=None):
+              rows=None, nthreads=0, window=(-1, -1), softcap=0.0, sinks=None, q_scale=1.0):
     """fp64 attention over a paged cache.
 
     q: [T, Hq, D] (bf16/fp16); k_cache, v_cache: [num_blocks, bs, Hkv, D]
@@ -104,7 +104,8 @@ def attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
     position (-1 unlimited), softcap (0 = none), sinks [Hq] (one logit per
     query head, or None): the variants of "FlashAttention deep dive",
     flash_attn_varlen_func (window_size, softcap, s_aux) as read in
-    attn_oracle.c.  Returns (out [n, Hq, D] float64, lse [n, Hq] float64).
+    attn_oracle.c.  q may be e4m3 with q_scale (its value is code *
+    q_scale).  Returns (out [n, Hq, D] float64, lse [n, Hq] float64).
     """
     lib = _load()
     q = _host(q)
@@ -120,7 +121,7 @@ def attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
     n = T if rws is None else rws.numel()
     out = torch.empty((n, Hq, D), dtype=torch.float64)
     lse = torch.empty((n, Hq), dtype=torch.float64)
-    plain = tuple(window) == (-1, -1) and not softcap and sinks is None
+    plain = tuple(window) == (-1, -1) and not softcap and sinks is None and q_scale == 1.0
     if plain:
         st = lib.oracle_attention(
             q.data_ptr(), _code(q), Hq * D,
@@ -138,7 +139,7 @@ def attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
             float(k_scale), float(v_scale),
             cu.data_ptr(), su.data_ptr(), bt.data_ptr(), bt.shape[1],
             B, Hq, Hkv, D, bs, nb, float(softmax_scale), int(bool(causal)),
-            int(window[0]), int(window[1]), float(softcap), _ptr(sk),
+            int(window[0]), int(window[1]), float(softcap), _ptr(sk), float(q_scale),
             _ptr(rws), n, out.data_ptr(), lse.data_ptr(), int(nthreads))
     if st != 0:
         raise ValueError("oracle_attention failed with status %d" % st)

@@ -160,6 +160,8 @@ static int elem_bytes(int dtype) {
  *     keys j with p - left <= j <= p + right (a negative bound is
  *     unlimited), on top of the causal rule j <= p and of j < kv_len;
  *   softcap c > 0: each scaled logit s becomes c * tanh(s / c);
+ *   q_scale: q is stored scaled ("FlashAttention deep dive", FA3 FP8
+ *     support: q_descale beside k/v_descale), its value is code * q_scale;
  *   sinks: query head h has a logit z_h that joins the softmax
  *     normalisation with a zero value vector:
  *       out = sum_j e^{s_j} V_j / (e^{z_h} + sum_j e^{s_j}),
@@ -173,7 +175,7 @@ int oracle_attention_ext(const void *q, int q_dtype, int64_t q_stride_tok,
                          int B, int Hq, int Hkv, int D, int bs, int num_blocks,
                          double softmax_scale, int causal,
                          int64_t window_left, int64_t window_right, double softcap,
-                         const double *sinks,
+                         const double *sinks, double q_scale,
                          const int64_t *rows, int64_t n_rows,
                          double *out, double *lse, int nthreads) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || bs <= 0 ||
@@ -231,7 +233,7 @@ int oracle_attention_ext(const void *q, int q_dtype, int64_t q_stride_tok,
             }
             const int64_t q_off = t * q_stride_tok + (int64_t)h * D;
             for (int d = 0; d < D; ++d)
-                qv[d] = load_elem(q, q_off + d, q_dtype);
+                qv[d] = load_elem(q, q_off + d, q_dtype) * q_scale;
             int bad = 0;
             double M = -INFINITY;
             for (int64_t j = first; j < nvis; ++j) {
@@ -288,7 +290,7 @@ int oracle_attention(const void *q, int q_dtype, int64_t q_stride_tok,
                      double *out, double *lse, int nthreads) {
     return oracle_attention_ext(q, q_dtype, q_stride_tok, k_cache, v_cache, kv_dtype, k_scale, v_scale,
                                 cu_seqlens_q, seqused_k, block_table, bt_stride, B, Hq, Hkv, D, bs,
-                                num_blocks, softmax_scale, causal, -1, -1, 0.0, NULL, rows, n_rows, out,
+                                num_blocks, softmax_scale, causal, -1, -1, 0.0, NULL, 1.0, rows, n_rows, out,
                                 lse, nthreads);
 }
 

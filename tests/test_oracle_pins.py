@@ -619,3 +619,35 @@ def test_sink_without_keys_gives_zero_and_the_sink():
     out, lse = run(b, sinks=[0.25, -1.0])
     assert torch.equal(out[2], torch.zeros(2, 16, dtype=torch.float64))
     assert lse[2].tolist() == [0.25, -1.0]
+
+
+# ------------------------------------------------ fp8 queries with q_scale
+# "FlashAttention deep dive", FA3 FP8 support (q_descale beside the k/v
+# descales); "Making FlashAttention-4 faster for inference", PR 2109 (FP8
+# inputs).  Value of an e4m3 query element = code * q_scale.
+
+def test_fp8_query_with_scale_equals_its_bf16_value():
+    """Scaling e4m3 codes by a power of two is exact in bf16 (4 significant
+    bits into 8), so attention with (e4m3 q, q_scale = 2^-3) equals attention
+    with the bf16 tensor holding code * 2^-3, bit for bit."""
+    b = W.make_batch([5, 1, 9], [12, 30, 9], Hq=4, Hkv=2, D=32, bs=16, seed=38)
+    kc, vc = cache_of(b)
+    q8 = (b.q.float() * 8.0).to(torch.float8_e4m3fn)
+    qv = (q8.float() * 0.125).to(torch.bfloat16)
+    assert torch.equal(qv.float(), q8.float() * 0.125)
+    out8, lse8 = oracle.attention(q8, kc, vc, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                                  q_scale=0.125)
+    b.q = qv
+    outb, lseb = run(b, kc, vc)
+    assert torch.equal(out8, outb) and torch.equal(lse8, lseb)
+
+
+def test_fp8_query_scale_is_a_logit_scale():
+    """q_scale multiplies every logit like softmax_scale does: (q_scale s,
+    softmax_scale t) and (1, s * t) agree to rounding."""
+    b = W.make_batch([4, 2], [20, 7], Hq=2, Hkv=1, D=16, bs=16, seed=39)
+    kc, vc = cache_of(b)
+    q8 = b.q.to(torch.float8_e4m3fn)
+    o1, l1 = oracle.attention(q8, kc, vc, b.cu_seqlens_q, b.seqused_k, b.block_table, 0.25, q_scale=0.7)
+    o2, l2 = oracle.attention(q8, kc, vc, b.cu_seqlens_q, b.seqused_k, b.block_table, 0.25 * 0.7)
+    assert float((o1 - o2).abs().max()) < 1e-12 and float((l1 - l2).abs().max()) < 1e-12
