@@ -571,6 +571,32 @@ def run_workload(args):
         res.update(metric="multi-token verify GB/s", value=round(by / (med * 1e-3) / 1e9, 1), unit="GB/s",
                    ms_per_step=round(med, 4), bytes=by, q_lens=[min(b.q_lens), max(b.q_lens)],
                    roofline={"bound": "hbm", "peak": hbm, "frac": round(by / (med * 1e-3) / 1e9 / hbm, 4)})
+    elif args.workload == "fp8decode":
+        # the decode workload's shape on an e4m3 cache, with bf16 queries and
+        # with e4m3 queries (q_descale; Q K^T on e4m3 operands)
+        b = W.decode_llama8b(gen_kv=False)
+        ks, vs = 4.5 / 448.0, 4.5 / 448.0
+        kc, vc = _device_cache(b, dev, torch.float8_e4m3fn, (ks, vs))
+        su, bt = b.seqused_k.to(dev), b.block_table.to(dev)
+        cu = b.cu_seqlens_q.to(dev)
+        ns = va.attn_num_splits(b.B, 1, b.max_seqlen_k, b.Hq, b.Hkv, sms)
+        wsp = torch.empty(max(1, va.attn_workspace_size(b.B, b.Hq, b.D, ns)), dtype=torch.uint8, device=dev)
+        by = decode_bytes(b, elem=1)
+        q16 = b.q.to(dev)
+        qs = float(b.q.float().abs().max()) / 448.0
+        q8 = (b.q.float() / qs).to(torch.float8_e4m3fn).to(dev)
+        out = torch.empty(b.q.shape, dtype=torch.bfloat16, device=dev)
+        lines = {}
+        for name, q, qd in (("q_bf16", q16, 1.0), ("q_e4m3", q8, qs)):
+            fn = lambda: va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt, 1, b.max_seqlen_k, b.softmax_scale,
+                                                causal=True, q_descale=qd, k_descale=ks, v_descale=vs,
+                                                num_splits=0, workspace=wsp)
+            med, mean = _time(fn, args.steps, args.warmup)
+            lines[name] = {"ms": round(med, 4), "gbs": round(by / (med * 1e-3) / 1e9, 1),
+                           "frac": round(by / (med * 1e-3) / 1e9 / hbm, 4)}
+        best = max(lines.values(), key=lambda x: x["gbs"])
+        res.update(metric="fp8-KV decode GB/s", value=best["gbs"], unit="GB/s", ms_per_step=best["ms"], bytes=by,
+                   variants=lines, roofline={"bound": "hbm", "peak": hbm, "frac": best["frac"]})
     elif args.workload == "fp8mixed":
         b = W.fp8_mixed(gen_kv=False)
         ks, vs = 4.5 / 448.0, 4.5 / 448.0           # |N(0,1)| max over ~1e8 draws is about 4.5-6
@@ -601,7 +627,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "longctx-bs16", "longctx-bs64", "longctx-bs256", "cascade", "swa",
-                             "verify",
+                             "verify", "fp8decode",
                              "fp8mixed"],
                     help="decode is the benchmark line; the others time one more workload each")
     args = ap.parse_args()

@@ -152,9 +152,14 @@ attn_status attn_varlen_prefill(
  *       out = sum_j e^{s_j} V_j / (e^{z_h} + sum_j e^{s_j}),
  *       lse = log(e^{z_h} + sum_j e^{s_j})
  *     (a query with no visible key then gets out = 0, lse = z_h).
+ * fp8 queries ([vLLM-FA] FA3 FP8 support, q_descale): q_dtype may be
+ *   ATTN_FP8_E4M3 when kv_dtype is ATTN_FP8_E4M3 and D is 128; a query
+ *   element's value is then code * q_descale, QK^T runs on e4m3 operands,
+ *   out is bf16, and q_stride_tok must be a multiple of 16 elements.  For
+ *   16-bit queries pass q_descale = 1.
  * Errors as attn_varlen_prefill, plus ATTN_ERR_SHAPE for a window bound
  * below -1 or a negative or NaN softcap.  attn_varlen_prefill is this call
- * with window (-1, -1), softcap 0 and no sinks.
+ * with q_descale 1, window (-1, -1), softcap 0 and no sinks.
  */
 attn_status attn_varlen_prefill_ext(
     const void *q, int64_t q_stride_tok,
@@ -165,7 +170,7 @@ attn_status attn_varlen_prefill_ext(
     int B, int total_q, int max_seqlen_q, int max_seqlen_k,
     int Hq, int Hkv, int D, int block_size, int num_blocks,
     attn_dtype q_dtype, attn_dtype kv_dtype,
-    float softmax_scale, int causal, float k_descale, float v_descale,
+    float softmax_scale, int causal, float q_descale, float k_descale, float v_descale,
     int window_left, int window_right, float softcap, const float *sinks,
     int num_splits, void *workspace, size_t ws_bytes, attn_stream_t stream);
 

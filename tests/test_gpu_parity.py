@@ -635,3 +635,53 @@ def test_workload_verify_full():
     ro, rl = ref_attn(b, *cpu_cache(b))
     check(out, lse, ro, rl, TOL)
     assert_no_device_error()
+
+
+# ------------------------------------------------ e4m3 queries (q_descale)
+
+@pytest.mark.parametrize("bs,num_splits", [(16, 0), (32, 1), (16, 3)])
+def test_fp8_query_against_oracle(bs, num_splits):
+    """e4m3 queries with q_descale over an e4m3 cache ("FlashAttention deep
+    dive", FA3 FP8: q/k/v descales): decode, verify and prefill rows in one
+    call, Q K^T on e4m3 operands, bf16 output; the oracle gets the same
+    e4m3 codes and scales."""
+    b = W.make_batch([1, 7, 300, 1, 129, 20, 3], [500, 7, 600, 2000, 129, 333, 40], 32, 8, 128, bs, seed=60,
+                     kv_dtype="fp8")
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    qs = float(b.q.float().abs().max()) / 448.0
+    q8 = (b.q.float() / qs).to(torch.float8_e4m3fn)
+    dev = torch.device("cuda")
+    out = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(q8.shape[:2], dtype=torch.float32, device=dev)
+    va.attn_varlen_prefill(q8.to(dev), kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev),
+                           b.block_table.to(dev), b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale, lse_out=lse,
+                           q_descale=qs, k_descale=b.k_scale, v_descale=b.v_scale, num_splits=num_splits)
+    ro, rl = oracle.attention(q8, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                              k_scale=b.k_scale, v_scale=b.v_scale, q_scale=qs)
+    check(out, lse, ro, rl, TOL_FP8)
+    assert_no_device_error()
+
+
+def test_fp8_query_with_variants():
+    """e4m3 queries with a sliding window, a soft cap and sinks."""
+    b = W.make_batch([1, 12, 90, 1], [800, 60, 200, 1500], 32, 8, 128, 16, seed=61, kv_dtype="fp8")
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    qs = float(b.q.float().abs().max()) / 448.0
+    q8 = (b.q.float() / qs).to(torch.float8_e4m3fn)
+    g = torch.Generator().manual_seed(W.SEED0 + 760)
+    sinks = (torch.randn(32, generator=g) * 2.0).float()
+    dev = torch.device("cuda")
+    for ns in (1, 0):
+        out = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(q8.shape[:2], dtype=torch.float32, device=dev)
+        va.attn_varlen_prefill(q8.to(dev), kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev),
+                               b.block_table.to(dev), b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale, lse_out=lse,
+                               q_descale=qs, k_descale=b.k_scale, v_descale=b.v_scale, num_splits=ns,
+                               window=(100, -1), softcap=5.0, sinks=sinks.to(dev))
+        ro, rl = oracle.attention(q8, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                                  k_scale=b.k_scale, v_scale=b.v_scale, q_scale=qs, window=(100, -1),
+                                  softcap=5.0, sinks=sinks.double())
+        check(out, lse, ro, rl, TOL_FP8)
+    assert_no_device_error()

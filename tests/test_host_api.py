@@ -75,7 +75,9 @@ def prefill(lib, **kw):
     (dict(B=-1), ERR_SHAPE),
     (dict(B=65536), ERR_SHAPE),
     (dict(Hq=65536 * 2, Hkv=2, qs=65536 * 2 * 128, os=65536 * 2 * 128), ERR_SHAPE),
-    (dict(qd=E4M3, kd=E4M3), ERR_DTYPE),
+    (dict(qd=E4M3, kd=BF16), ERR_DTYPE),
+    (dict(qd=E4M3, kd=E4M3, D=64, qs=8 * 64, os=8 * 64), ERR_DTYPE),
+    (dict(qd=E4M3, kd=E4M3, qs=8 * 128 + 8), ERR_ALIGN),
     (dict(qd=BF16, kd=FP16), ERR_DTYPE),
     (dict(qd=FP32, kd=FP32), ERR_DTYPE),
     (dict(q=ctypes.c_void_p(4104)), ERR_ALIGN),
@@ -181,7 +183,8 @@ def prefill_ext(lib, wl=-1, wr=-1, cap=0.0, sinks=None, **kw):
     return lib.attn_varlen_prefill_ext(a["q"], a["qs"], a["k"], a["v"], a["out"], a["os"], a["lse"], a["cu"],
                                        a["su"], a["bt"], a["bts"], a["B"], a["T"], a["mq"], a["mk"], a["Hq"],
                                        a["Hkv"], a["D"], a["bs"], a["nb"], a["qd"], a["kd"], a["scale"],
-                                       a["causal"], a["kds"], a["vds"], wl, wr, cap, sinks, a["ns"], a["ws"],
+                                       a["causal"], a.get("qds", 1.0), a["kds"], a["vds"], wl, wr, cap, sinks,
+                                       a["ns"], a["ws"],
                                        a["wsb"], None)
 
 

@@ -57,7 +57,7 @@ def _load():
     lib.attn_varlen_prefill_ext.argtypes = [
         vp, i64, vp, vp, vp, i64, vp, vp, vp, vp, i64,
         i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-        f32, i32, f32, f32, i32, i32, f32, vp, i32, vp, sz, vp]
+        f32, i32, f32, f32, f32, i32, i32, f32, vp, i32, vp, sz, vp]
     lib.attn_paged_decode.restype = i32
     lib.attn_paged_decode.argtypes = [
         vp, vp, vp, vp, vp, vp, vp, i64,
@@ -130,7 +130,7 @@ def _sms(device):
 def attn_varlen_prefill(q, k_cache, v_cache, out, cu_seqlens_q, seqused_k, block_table,
                         max_seqlen_q, max_seqlen_k, softmax_scale, causal=True, lse_out=None,
                         k_descale=1.0, v_descale=1.0, num_splits=0, workspace=None, stream=None,
-                        window=(-1, -1), softcap=0.0, sinks=None):
+                        window=(-1, -1), softcap=0.0, sinks=None, q_descale=1.0):
     """flash_attn_varlen_func over a paged cache (see include/attn.h).
 
     q, out: [T, Hq, D] (token stride may exceed Hq * D); k_cache, v_cache:
@@ -140,7 +140,9 @@ def attn_varlen_prefill(q, k_cache, v_cache, out, cu_seqlens_q, seqused_k, block
     workspace is allocated here when not given.  Variants
     (attn_varlen_prefill_ext): window = (left, right) keys around each
     query's position (-1 unlimited), softcap (0 = off), sinks: optional
-    [Hq] fp32 CUDA tensor of per-head sink logits.
+    [Hq] fp32 CUDA tensor of per-head sink logits.  q may be
+    float8_e4m3fn (with an e4m3 cache, head size 128) scaled by q_descale;
+    out is then bf16.
     """
     lib = _load()
     T, Hq, D = q.shape
@@ -162,7 +164,7 @@ def attn_varlen_prefill(q, k_cache, v_cache, out, cu_seqlens_q, seqused_k, block
         _p(q), q.stride(0), _p(k_cache), _p(v_cache), _p(out), out.stride(0), _p(lse_out),
         _p(cu_seqlens_q), _p(seqused_k), _p(block_table), block_table.stride(0),
         B, T, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, bs, nb,
-        _dt(q), _dt(k_cache), float(softmax_scale), int(bool(causal)),
+        _dt(q), _dt(k_cache), float(softmax_scale), int(bool(causal)), float(q_descale),
         float(k_descale), float(v_descale), int(window[0]), int(window[1]), float(softcap), _p(sinks),
         int(num_splits), _p(ws), ws_bytes, _stream(stream))
     _check("attn_varlen_prefill", st)

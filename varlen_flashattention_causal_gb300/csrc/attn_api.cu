@@ -146,7 +146,7 @@ struct FwdArgs {
     attn_dtype q_dtype, kv_dtype;
     float scale;
     int causal;
-    float k_descale, v_descale;
+    float q_descale = 1.f, k_descale, v_descale;
     int num_splits;
     void *ws;
     size_t ws_bytes;
@@ -161,17 +161,22 @@ attn_status validate_fwd(const FwdArgs &a) {
     if (a.B > 0 && a.cu_seqlens_q == nullptr && a.max_q != 1) return ATTN_ERR_NULL;
     if (a.D != 64 && a.D != 128) return ATTN_ERR_HEAD_SIZE;
     if (a.bs <= 0 || a.bs % 16 != 0) return ATTN_ERR_BLOCK_SIZE;
-    if (!is16(a.q_dtype)) return ATTN_ERR_DTYPE;
+    // 16-bit q with a cache of the same type or e4m3; e4m3 q with an e4m3
+    // cache and head size 128 (out is then bf16)
+    const bool q8 = a.q_dtype == ATTN_FP8_E4M3;
+    if (!is16(a.q_dtype) && !q8) return ATTN_ERR_DTYPE;
     if (!(a.kv_dtype == a.q_dtype || a.kv_dtype == ATTN_FP8_E4M3)) return ATTN_ERR_DTYPE;
+    if (q8 && a.D != 128) return ATTN_ERR_DTYPE;
     if (a.B < 0 || a.B > 65535 || a.T < 0 || a.Hq <= 0 || a.Hq > 65535 || a.Hkv <= 0 || a.Hq % a.Hkv != 0 ||
         a.num_blocks < 0 || a.max_q < 0 || a.max_k < 0 || a.bt_stride < 0 || a.num_splits < 0)
         return ATTN_ERR_SHAPE;
     if (a.q_stride < (int64_t)a.Hq * a.D || a.out_stride < (int64_t)a.Hq * a.D) return ATTN_ERR_SHAPE;
     if ((long long)a.max_q * (a.Hq / a.Hkv) > (1LL << 30)) return ATTN_ERR_SHAPE;
     if (!aligned16(a.q) || !aligned16(a.k_cache) || !aligned16(a.v_cache) || !aligned16(a.out) ||
-        (a.q_stride % 8) != 0 || (a.out_stride % 8) != 0)
+        (a.q_stride % (q8 ? 16 : 8)) != 0 || (a.out_stride % 8) != 0)
         return ATTN_ERR_ALIGN;
-    if (!(a.scale == a.scale) || !(a.k_descale == a.k_descale) || !(a.v_descale == a.v_descale))
+    if (!(a.scale == a.scale) || !(a.k_descale == a.k_descale) || !(a.v_descale == a.v_descale) ||
+        !(a.q_descale == a.q_descale))
         return ATTN_ERR_SHAPE;
     if (a.window_left < -1 || a.window_right < -1 || !(a.softcap >= 0.f) || isinf(a.softcap)) return ATTN_ERR_SHAPE;
     return ATTN_OK;
@@ -239,13 +244,13 @@ attn_status run_fwd(const FwdArgs &a) {
     p.bs = a.bs;
     p.num_blocks = a.num_blocks;
     p.causal = a.causal ? 1 : 0;
-    p.scale_log2 = a.scale * a.k_descale * 1.4426950408889634f;
+    p.scale_log2 = a.scale * a.q_descale * a.k_descale * 1.4426950408889634f;
     p.v_descale = a.v_descale;
     p.err = dev->err;
     p.window_left = wl;
     p.window_right = wr;
     if (a.softcap > 0.f) {
-        p.cap_in = a.scale * a.k_descale / a.softcap;
+        p.cap_in = a.scale * a.q_descale * a.k_descale / a.softcap;
         p.cap_out = a.softcap * 1.4426950408889634f;
     }
     p.sinks = a.sinks;
@@ -298,7 +303,7 @@ attn_status run_fwd(const FwdArgs &a) {
         c.ns1 = ns[1];
         c.ns2 = ns[2];
         c.part_stride = stride;
-        st = check_cuda(launch_combine(c, a.q_dtype, a.stream));
+        st = check_cuda(launch_combine(c, a.q_dtype == ATTN_FP8_E4M3 ? ATTN_BF16 : a.q_dtype, a.stream));
     }
     return st;
 }
@@ -360,7 +365,7 @@ attn_status attn_varlen_prefill(const void *q, int64_t q_stride_tok, const void 
                                 void *workspace, size_t ws_bytes, attn_stream_t stream) {
     return attn_varlen_prefill_ext(q, q_stride_tok, k_cache, v_cache, out, out_stride_tok, lse_out, cu_seqlens_q,
                                    seqused_k, block_table, bt_row_stride, B, total_q, max_seqlen_q, max_seqlen_k, Hq,
-                                   Hkv, D, block_size, num_blocks, q_dtype, kv_dtype, softmax_scale, causal,
+                                   Hkv, D, block_size, num_blocks, q_dtype, kv_dtype, softmax_scale, causal, 1.f,
                                    k_descale, v_descale, -1, -1, 0.f, nullptr, num_splits, workspace, ws_bytes,
                                    stream);
 }
@@ -370,8 +375,9 @@ attn_status attn_varlen_prefill_ext(const void *q, int64_t q_stride_tok, const v
                                     const int32_t *seqused_k, const int32_t *block_table, int64_t bt_row_stride,
                                     int B, int total_q, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
                                     int block_size, int num_blocks, attn_dtype q_dtype, attn_dtype kv_dtype,
-                                    float softmax_scale, int causal, float k_descale, float v_descale,
-                                    int window_left, int window_right, float softcap, const float *sinks,
+                                    float softmax_scale, int causal, float q_descale, float k_descale,
+                                    float v_descale, int window_left, int window_right, float softcap,
+                                    const float *sinks,
                                     int num_splits, void *workspace, size_t ws_bytes, attn_stream_t stream) {
     FwdArgs a{};
     a.q = q;
@@ -404,6 +410,7 @@ attn_status attn_varlen_prefill_ext(const void *q, int64_t q_stride_tok, const v
     a.ws = workspace;
     a.ws_bytes = ws_bytes;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
+    a.q_descale = q_descale;
     a.window_left = window_left;
     a.window_right = window_right;
     a.softcap = softcap;

@@ -26,6 +26,8 @@
 // (Q) and at the end (the merge); with
 // nsplit > 1 each CTA writes a normalised partial state that the combine
 // kernel merges by log-sum-exp (sec. 12).
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace attn {
@@ -34,7 +36,8 @@ template <int D_, int WM_, int WN_, int BN_, int STAGES_, int QT_, int KVT_>
 struct MmaCfg {
     static constexpr int D = D_, WM = WM_, WN = WN_, BN = BN_, STAGES = STAGES_, QT = QT_, KVT = KVT_;
     static constexpr int ROWS = 16 * WM;
-    static constexpr bool MMA_BF16 = (KVT == DT_BF16);   // fp16 and e4m3 caches run f16 MMAs
+    static constexpr bool MMA_BF16 = (KVT == DT_BF16);   // fp16 and e4m3 caches run f16 MMAs (P V)
+    using OutT = std::conditional_t<QT == DT_FP16, __half, __nv_bfloat16>;   // e4m3 q: bf16 out
     static constexpr int KV_BYTES = Elem<KVT>::bytes;
     static constexpr int KV_ROW = D * KV_BYTES;          // bytes of one cached row (one KV head)
     static constexpr int TILE_RAW = BN * KV_ROW;         // one K (or V) tile as stored
@@ -58,9 +61,16 @@ struct MmaCfg {
     // fragments of all eight k-steps 32 contiguous bytes of its key row,
     // widened in registers.  V still goes through shared memory (its
     // fragments run along keys, which are rows of the cache).
-    static constexpr bool KDIRECT = (KVT == DT_E4M3) && WARP_LOCAL && D == 128;
+    static constexpr bool KDIRECT = (KVT == DT_E4M3) && WARP_LOCAL && D == 128 && QT != DT_E4M3;
+    // e4m3 queries: Q K^T on e4m3 operands (m16n8k32), the K fragments
+    // read straight from the staged bytes with no widening, in the same
+    // permuted head order (k-step kk of lane quad t covers dims
+    // 32t + 8kk .. 32t + 8kk + 7); output in bf16
+    static constexpr bool Q8 = (QT == DT_E4M3);
+    static constexpr bool STAGE_SWZ = KDIRECT || Q8;   // staged e4m3 rows chunk-swizzled
+    static_assert(!Q8 || (KVT == DT_E4M3 && D == 128), "e4m3 queries need an e4m3 cache and head size 128");
     // e4m3: widened fp16 tiles (V only with KDIRECT) after the staging ring
-    static constexpr int CONV_BYTES = (KVT == DT_E4M3) ? (KDIRECT ? TILE16 : 2 * TILE16) : 0;
+    static constexpr int CONV_BYTES = (KVT == DT_E4M3) ? ((KDIRECT || Q8) ? TILE16 : 2 * TILE16) : 0;
     static constexpr int OSTRIDE = D + 4;                // fp32 epilogue row stride (bank spread)
     static constexpr int EPI_BYTES = WN * ROWS * OSTRIDE * 4 + 2 * WN * ROWS * 4;
     static constexpr int MAIN_BYTES = STAGES * STAGE_BYTES + CONV_BYTES;
@@ -69,6 +79,8 @@ struct MmaCfg {
     static_assert(NT % 2 == 0, "n-tile pairs");
     static_assert((RPW * CH) % 32 == 0, "whole warp copy rounds");
 };
+
+constexpr float kRescaleLog2 = 8.0f;   // reference-maximum threshold (log2 units)
 
 template <class C>
 __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
@@ -126,7 +138,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
                     for (int d = 0; d < D; ++d) p.part_o[slot * D + d] = 0.f;
             } else {
                 if (p.lse) p.lse[tok * p.Hq + h] = zl;
-                using OT = typename Elem<C::QT>::T;
+                using OT = typename C::OutT;
                 OT *o = reinterpret_cast<OT *>(p.out) + tok * p.out_stride + (int64_t)h * D;
                 for (int d = 0; d < D; ++d) o[d] = OT(0.f);
             }
@@ -134,8 +146,21 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         return;
     }
 
-    // ---- Q rows of this block -> shared memory (16-bit MMA form, swizzled)
-    for (int c = tid; c < ROWS * (D / 8); c += blockDim.x) {
+    // ---- Q rows of this block -> shared memory: e4m3 rows of D bytes with
+    // 16-byte chunks swizzled by row & 7 (e4m3 queries), else the 16-bit MMA
+    // form, swizzled
+    if constexpr (C::Q8) {
+        for (int c = tid; c < ROWS * (D / 16); c += blockDim.x) {
+            const int lr = c / (D / 16), ch = c % (D / 16);
+            const int pr = row0 + lr;
+            int4 v = make_int4(0, 0, 0, 0);
+            if (pr < row_end)
+                v = ldg_nc16(reinterpret_cast<const uint8_t *>(p.q) +
+                             (int64_t)(q_start + pr / G) * p.q_stride + (int64_t)(kvh * G + pr % G) * D + ch * 16);
+            *reinterpret_cast<int4 *>(sQ + lr * D + ((ch ^ (lr & 7)) << 4)) = v;
+        }
+    }
+    for (int c = tid; c < (C::Q8 ? 0 : ROWS * (D / 8)); c += blockDim.x) {
         const int lr = c / (D / 8), ch = c % (D / 8);
         const int pr = row0 + lr;
         int4 v = make_int4(0, 0, 0, 0);
@@ -160,7 +185,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     }
 
     // e4m3 tiles hold value * 2^-8 (see e4m3x4_to_h2x2_lo8): scale S and O back
-    const float sl2 = (C::KVT == DT_E4M3) ? p.scale_log2 * kE4m3Lo8Scale : p.scale_log2;
+    const float sl2 = (C::KVT == DT_E4M3 && !C::Q8) ? p.scale_log2 * kE4m3Lo8Scale : p.scale_log2;
     const float vds = (C::KVT == DT_E4M3) ? p.v_descale * kE4m3Lo8Scale : p.v_descale;
 
     // ---- K/V tile gather through the block table
@@ -168,10 +193,10 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     const uint8_t *kbase = reinterpret_cast<const uint8_t *>(p.k_cache);
     const uint8_t *vbase = reinterpret_cast<const uint8_t *>(p.v_cache);
     // byte offset of 16-byte chunk ch of row `row` in a staged e4m3 tile:
-    // chunks XOR-swizzled by row & 7 with KDIRECT (the direct K fragment
+    // chunks XOR-swizzled by row & 7 with STAGE_SWZ (the direct K fragment
     // loads of eight rows then hit eight different bank groups), plain otherwise
     auto stage8 = [](int row, int ch) -> uint32_t {
-        return (uint32_t)(row * C::KV_ROW + ((C::KDIRECT ? (ch ^ (row & 7)) : ch) << 4));
+        return (uint32_t)(row * C::KV_ROW + ((C::STAGE_SWZ ? (ch ^ (row & 7)) : ch) << 4));
     };
     auto load_tile = [&](int t, int stage) {
         const int n0 = kv_lo + t * BN;
@@ -208,7 +233,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     // e4m3 tiles are widened to fp16 (exact) into a swizzled tile for
     // ldmatrix.  Warp-local mode: each warp widens only its own rows.
     uint8_t *cK = sMain + STAGES * C::STAGE_BYTES;
-    uint8_t *cV = C::KDIRECT ? cK : cK + C::TILE16;
+    uint8_t *cV = (C::KDIRECT || C::Q8) ? cK : cK + C::TILE16;
     auto convert_tile = [&](int stage) {
         const uint8_t *sK = sMain + stage * C::STAGE_BYTES;
         const uint8_t *sV = sK + C::TILE_RAW;
@@ -219,7 +244,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         for (int c = c0; c < kChunks; c += cstep) {
             const int row = rbase + c / (D / 16), ch = c % (D / 16);
             // fp16 patterns of value * 2^-8 (the 2^8 is in the scales)
-            if constexpr (!C::KDIRECT) {
+            if constexpr (!C::KDIRECT && !C::Q8) {
                 const int4 rk = *reinterpret_cast<const int4 *>(sK + stage8(row, ch));
                 int4 k0, k1;
                 e4m3x4_to_h2x2_lo8((uint32_t)rk.x, reinterpret_cast<uint32_t &>(k0.x), reinterpret_cast<uint32_t &>(k0.y));
@@ -249,7 +274,23 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     __syncthreads();   // Q visible to every warp
 
     uint32_t qf[C::KT][4];
-    if constexpr (C::KDIRECT) {
+    if constexpr (C::Q8) {
+        // e4m3 A fragments, permuted head order (see Q8): k-step kk (32
+        // dims) of lane (g, t) holds bytes 32t + 8kk .. + 3 (a0, a1) and
+        // 32t + 8kk + 4 .. + 7 (a2, a3) of rows g and g + 8
+        const int g = lane >> 2, t4 = lane & 3;
+        const int r0 = wm * 16 + g, r1 = r0 + 8;
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+            const int ch = 2 * t4 + (kk >> 1), off = (kk & 1) * 8;
+            const uint2 x0 = *reinterpret_cast<const uint2 *>(sQ + r0 * D + ((ch ^ (r0 & 7)) << 4) + off);
+            const uint2 x1 = *reinterpret_cast<const uint2 *>(sQ + r1 * D + ((ch ^ (r1 & 7)) << 4) + off);
+            qf[kk][0] = x0.x;
+            qf[kk][1] = x1.x;
+            qf[kk][2] = x0.y;
+            qf[kk][3] = x1.y;
+        }
+    } else if constexpr (C::KDIRECT) {
         // permuted head dimension (see KDIRECT): lane (g, t) takes, for
         // k-step kk, dims 32t + 4kk .. 32t + 4kk + 3 of rows g and g + 8
         const int g = lane >> 2, t4 = lane & 3;
@@ -289,7 +330,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     const int lo1 = (p.window_left >= 0) ? ctx + ir1 - p.window_left : INT_MIN;
     // soft cap: raw score -> cap * log2(e) * tanh(score * scale * k_descale / cap)
     const bool capped = p.cap_in > 0.f;
-    const float cap_in = (C::KVT == DT_E4M3) ? p.cap_in * kE4m3Lo8Scale : p.cap_in;
+    const float cap_in = (C::KVT == DT_E4M3 && !C::Q8) ? p.cap_in * kE4m3Lo8Scale : p.cap_in;
 
     float o[D / 8][4];
 #pragma unroll
@@ -323,7 +364,22 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         float s[C::NT][4];
 #pragma unroll
         for (int i = 0; i < C::NT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-        if constexpr (C::KDIRECT) {
+        if constexpr (C::Q8) {
+            // n-tile j: lane (g, t) holds key row wn * NW + 8j + g, bytes
+            // [32t, 32t + 32): its B fragments of all four k32 steps, as stored
+            const uint8_t *raw = sMain + (t % STAGES) * C::STAGE_BYTES;
+#pragma unroll
+            for (int j = 0; j < C::NT; ++j) {
+                const int key = wn * C::NW + 8 * j + (lane >> 2);
+                const int c0 = 2 * (lane & 3);
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(raw + stage8(key, c0));
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(raw + stage8(key, c0 + 1));
+                mma16832_e4m3(s[j], qf[0], w0.x, w0.y);
+                mma16832_e4m3(s[j], qf[1], w0.z, w0.w);
+                mma16832_e4m3(s[j], qf[2], w1.x, w1.y);
+                mma16832_e4m3(s[j], qf[3], w1.z, w1.w);
+            }
+        } else if constexpr (C::KDIRECT) {
             // n-tile j: lane (g, t) holds key row wn * NW + 8j + g, bytes
             // [32t, 32t + 32) = its B fragments of all eight k-steps
             const uint8_t *raw = sMain + (t % STAGES) * C::STAGE_BYTES;
@@ -386,8 +442,12 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
             }
         }
 
-        // online softmax (two rows per thread, four lanes per row)
-        float mx[2] = {m[0], m[1]};
+        // online softmax (two rows per thread, four lanes per row).  m is a
+        // reference maximum that moves only when a row's maximum grows by
+        // more than 2^8 (log2 units): P is formed against it (every value
+        // <= 256, exact since l and O share the reference), and O is
+        // rescaled only on the rare tiles that move it
+        float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
             mx[0] = fmaxf(mx[0], fmaxf(s[nt][0], s[nt][1]));
@@ -401,9 +461,10 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         float base[2], alpha[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            base[h] = (mx[h] == -INFINITY) ? 0.f : mx[h];   // fully masked row so far
-            alpha[h] = ex2(m[h] - base[h]);
-            m[h] = mx[h];
+            const bool bump = mx[h] > m[h] + kRescaleLog2;
+            alpha[h] = (bump && m[h] != -INFINITY) ? ex2(m[h] - mx[h]) : 1.f;
+            if (bump) m[h] = mx[h];
+            base[h] = (m[h] == -INFINITY) ? 0.f : m[h];      // fully masked row so far
         }
         float rs[2] = {0.f, 0.f};
 #pragma unroll
@@ -417,12 +478,14 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         }
         l[0] = l[0] * alpha[0] + rs[0];
         l[1] = l[1] * alpha[1] + rs[1];
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            o[i][0] *= alpha[0];
-            o[i][1] *= alpha[0];
-            o[i][2] *= alpha[1];
-            o[i][3] *= alpha[1];
+            for (int i = 0; i < D / 8; ++i) {
+                o[i][0] *= alpha[0];
+                o[i][1] *= alpha[0];
+                o[i][2] *= alpha[1];
+                o[i][3] *= alpha[1];
+            }
         }
 
         // O += P V (P re-used from the S accumulators as A fragments)
@@ -514,10 +577,10 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         acc.w *= inv;
         const float lse_v = lf > 0.f ? (mf + __log2f(lf)) * 0.6931471805599453f : -INFINITY;
         if (p.nsplit == 1) {
-            using OT = typename Elem<C::QT>::T;
+            using OT = typename C::OutT;
             OT *dst = reinterpret_cast<OT *>(p.out) + tok * p.out_stride + (int64_t)h * D + c4 * 4;
             uint2 pk;
-            if constexpr (C::QT == DT_BF16) {
+            if constexpr (C::QT != DT_FP16) {
                 pk.x = pack2<true>(acc.x, acc.y);
                 pk.y = pack2<true>(acc.z, acc.w);
             } else {
@@ -557,6 +620,10 @@ static cudaError_t launch_rows(const FwdParams &p, int rows_per_cta, cudaStream_
 
 template <int D>
 static cudaError_t launch_d(const FwdParams &p, int q_dtype, int kv_dtype, int rows_per_cta, cudaStream_t s) {
+    if (q_dtype == DT_E4M3 && kv_dtype == DT_E4M3) {
+        if constexpr (D == 128) return launch_rows<D, DT_E4M3, DT_E4M3>(p, rows_per_cta, s);
+        return cudaErrorInvalidValue;
+    }
     if (q_dtype == DT_BF16 && kv_dtype == DT_BF16) return launch_rows<D, DT_BF16, DT_BF16>(p, rows_per_cta, s);
     if (q_dtype == DT_FP16 && kv_dtype == DT_FP16) return launch_rows<D, DT_FP16, DT_FP16>(p, rows_per_cta, s);
     if (q_dtype == DT_BF16 && kv_dtype == DT_E4M3) return launch_rows<D, DT_BF16, DT_E4M3>(p, rows_per_cta, s);

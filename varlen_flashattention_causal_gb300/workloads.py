@@ -168,14 +168,14 @@ def tiny(device="cpu"):
     return pre, dec
 
 
-def decode_llama8b(device="cpu", B=64, lo=512, hi=4096, pool=40960):
+def decode_llama8b(device="cpu", B=64, lo=512, hi=4096, pool=40960, gen_kv=True):
     """Workload 1: Llama-3-8B-shaped paged decode (query = last position)."""
     g = generator(1)
     ctx = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
     Hq, Hkv, D, bs = 32, 8, 128, 16
     bt = block_tables(ctx, bs, pool, g)
     b = Batch("decode-llama8b", Hq, Hkv, D, bs, pool, [1] * B, ctx, block_table=bt)
-    return _finish(b, g, device, [range(L) for L in ctx])
+    return _finish(b, g, device, [range(L) for L in ctx], gen_kv=gen_kv)
 
 
 LONGCTX = [32 * 1024, 64 * 1024, 96 * 1024, 128 * 1024]
