@@ -170,6 +170,9 @@ def test_workspace_and_split_rules(lib):
     assert va.attn_num_splits(1, 1, 100, 32, 8, 152) == 1     # too short to split
     # one long request among many short ones is still cut into segments
     assert va.attn_num_splits(1024, 1, 16384, 32, 8, 152) >= 8
+    # the decode benchmark shape (64 requests up to 4060 keys, 8 KV heads):
+    # 4 segments, the flat optimum of a 1-16 sweep on this chip
+    assert va.attn_num_splits(64, 1, 4060, 32, 8, 152) == 4
     for B, L in ((64, 4096), (4, 32768), (128, 16384), (1, 2048)):
         s = va.attn_num_splits(B, 1, L, 32, 8, 152)
         assert 1 <= s <= 256 and (L // 64) >= s or s == 1

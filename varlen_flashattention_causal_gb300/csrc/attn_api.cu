@@ -122,7 +122,7 @@ Plan make_plan(int B, int max_q, int max_k, bool uniform, int Hq, int Hkv, int D
         c.rpc = c.tc ? tc_rows_per_cta() : (k == 0 ? kLightRows : mma_rows_per_cta(rows_cap));
         const long long rb = (rows_cap + c.rpc - 1) / c.rpc;
         if (k == 0)        // decode-like rows: also bound the keys per segment (32 tiles)
-            c.ns = split_rule((long long)B * Hkv * rb, max_k, 4LL * sms, 2, rb == 1 ? 32 : 0);
+            c.ns = split_rule((long long)B * Hkv * rb, max_k, 6LL * sms, 2, 32);
         else if (!c.tc)
             c.ns = split_rule((long long)B * Hkv * rb, max_k, 4LL * sms, 2, rb == 1 ? 32 : 0);
         else
