@@ -250,7 +250,10 @@ cudaError_t launch_combine(const CombineParams &p, int out_dtype, cudaStream_t s
     if (light) {
         // tokens of a split request: at most 64 packed rows, so at most 64 / G
         const int zt = std::max(1, std::min(p.max_q, std::max(1, std::max(p.rows_hi0, std::min(p.rows_hi1, 64)) / p.G)));
-        const dim3 g((unsigned)p.B, (unsigned)((p.Hq + kCombineHeads - 1) / kCombineHeads), (unsigned)std::min(zt, 64));
+        // (at most 4 CTAs along the tokens, each walking every 4th token:
+        // most requests of a mixed batch have one token, and the extra CTAs
+        // of the others would only exit)
+        const dim3 g((unsigned)p.B, (unsigned)((p.Hq + kCombineHeads - 1) / kCombineHeads), (unsigned)std::min(zt, 4));
         const dim3 blk(32 * kCombineHeads);
         if (out_dtype == DT_BF16) return launch_pdl(combine_light_kernel<__nv_bfloat16>, g, blk, 0, stream, p);
         if (out_dtype == DT_FP16) return launch_pdl(combine_light_kernel<__half>, g, blk, 0, stream, p);
