@@ -46,13 +46,26 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or the hint (ns) runs out, instead of spinning on issue
+// slots that the warps sharing its scheduler need.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete; false on timeout
 // or when *abort was raised by another role.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
-        if (mbar_test(bar, parity)) return true;
+        if (mbar_test_sleep(bar, parity)) return true;
         if (*abort) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
             *abort = 1;
