@@ -420,6 +420,47 @@ def test_workload3_cascade_decode_full():
     check(out, lse, ro, rl, TOL)
     assert_no_device_error()
 
+    # the same step captured in a CUDA graph with the prefix call on a second
+    # stream (joined before the merge), as the benchmark times it: with the
+    # automatic split counts the same kernels compute the same items, so the
+    # result is bit-identical; with 4 prefix and 2 suffix segments (the
+    # benchmark's pair) it matches the oracle
+    pre_o2, suf_o2, out2 = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    pre_l2, suf_l2, lse2 = (torch.empty((T, Hq), dtype=torch.float32, device="cuda") for _ in range(3))
+    cu0 = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    su0 = torch.tensor([P], dtype=torch.int32, device="cuda")
+    cu, su = b.cu_seqlens_q.cuda(), (b.seqused_k - P).cuda()
+    side = torch.cuda.Stream()
+    for ns_pre, ns_suf in ((0, 0), (4, 2)):
+        def step():
+            cur = torch.cuda.current_stream()
+            side.wait_stream(cur)
+            with torch.cuda.stream(side):
+                va.attn_varlen_prefill(q, kc, vc, pre_o2, cu0, su0, bt[:1], T, P, b.softmax_scale, causal=False,
+                                       lse_out=pre_l2, num_splits=ns_pre)
+            va.attn_varlen_prefill(q, kc, vc, suf_o2, cu, su, bt[:, nblk:], 1, b.max_seqlen_k - P,
+                                   b.softmax_scale, causal=True, lse_out=suf_l2, num_splits=ns_suf)
+            cur.wait_stream(side)
+            va.attn_merge_states(out2, lse2, pre_o2, pre_l2, suf_o2, suf_l2)
+
+        warm = torch.cuda.Stream()
+        warm.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(warm):
+            step()
+        torch.cuda.current_stream().wait_stream(warm)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            out2.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            if ns_pre == 0:
+                assert torch.equal(out2, out) and torch.equal(lse2, lse)
+            else:
+                check(out2, lse2, ro, rl, TOL)
+        assert_no_device_error()
+
 
 def test_workload4_fp8_mixed_full_sampled():
     b = W.fp8_mixed()
