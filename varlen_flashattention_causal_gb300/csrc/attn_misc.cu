@@ -145,11 +145,52 @@ template <class OT>
 __device__ __forceinline__ void combine_row(const CombineParams &p, int t, int h, int ns, int lane) {
     const int64_t base = ((int64_t)t * p.Hq + h) * (int64_t)p.part_stride;
     const float *ls = p.part_lse + base;
+    const int D = p.D;
+    if (ns <= kCombineBatch) {
+        // one round trip: every lane loads all ns lse values (one address
+        // per segment, broadcast across the warp) with its own O columns,
+        // and takes the maximum itself
+        const int d = lane * 4;
+        const float *po = p.part_o + base * D + d;
+        float l[kCombineBatch];
+        float4 v[kCombineBatch];
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k) {
+            const bool in = k < ns;
+            l[k] = in ? ls[k] : -INFINITY;
+            v[k] = (in && d < D) ? *reinterpret_cast<const float4 *>(po + (int64_t)k * D)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k) mx = fmaxf(mx, l[k]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
+        if (mx != -INFINITY) {
+#pragma unroll
+            for (int k = 0; k < kCombineBatch; ++k) {
+                // an empty segment wrote only its lse: its O slot is not used
+                const float w = l[k] == -INFINITY ? 0.f : expf(l[k] - mx);
+                if (w == 0.f) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                wsum += w;
+                acc.x += w * v[k].x;
+                acc.y += w * v[k].y;
+                acc.z += w * v[k].z;
+                acc.w += w * v[k].w;
+            }
+        }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        if (d < D) {
+            OT *out = reinterpret_cast<OT *>(p.out) + (int64_t)t * p.out_stride + (int64_t)h * D;
+            store4<OT>(out + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        }
+        if (lane == 0 && p.lse) p.lse[(int64_t)t * p.Hq + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+        return;
+    }
     float mx = -INFINITY;
     for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, ls[s]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const int D = p.D;
     const int d = lane * 4;                       // this lane's four columns
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
