@@ -54,6 +54,11 @@ struct MmaCfg {
     // every tile and is also the only warp that reads them (its key slice),
     // so the main loop needs no CTA-wide barrier.
     static constexpr bool WARP_LOCAL = (WM == 1 && RPW == NW);
+    // Two row blocks of 16 rows (2 x 2 warps): warp w = wm + 2 wn fetches
+    // rows [16w, 16w + 16), so the two warps of key slice wn fetch exactly
+    // the 32 rows that only they read, and a barrier of that pair (64
+    // threads) stands in for the CTA-wide one.
+    static constexpr bool PAIR_LOCAL = (WM == 2 && WN == 2 && NW == 2 * RPW);
     // e4m3 K fragments straight from the staged tile (decode shape, D 128):
     // the head dimension is read in a permuted order -- k-step kk of lane
     // quad t covers dims 32t + 4kk .. 32t + 4kk + 3, the same order for the
@@ -237,10 +242,11 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     auto convert_tile = [&](int stage) {
         const uint8_t *sK = sMain + stage * C::STAGE_BYTES;
         const uint8_t *sV = sK + C::TILE_RAW;
-        constexpr int kChunks = (C::WARP_LOCAL ? C::RPW : BN) * (D / 16);
-        const int c0 = C::WARP_LOCAL ? lane : tid;
-        const int cstep = C::WARP_LOCAL ? 32 : (int)blockDim.x;
-        const int rbase = C::WARP_LOCAL ? warp * C::RPW : 0;
+        constexpr bool own_rows = C::WARP_LOCAL || C::PAIR_LOCAL;   // each warp widens the rows it fetched
+        constexpr int kChunks = (own_rows ? C::RPW : BN) * (D / 16);
+        const int c0 = own_rows ? lane : tid;
+        const int cstep = own_rows ? 32 : (int)blockDim.x;
+        const int rbase = own_rows ? warp * C::RPW : 0;
         for (int c = c0; c < kChunks; c += cstep) {
             const int row = rbase + c / (D / 16), ch = c % (D / 16);
             // fp16 patterns of value * 2^-8 (the 2^8 is in the scales)
@@ -338,11 +344,19 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
     float m[2] = {-INFINITY, -INFINITY};
     float l[2] = {0.f, 0.f};
 
+    // the threads that wrote what a warp reads next (and will overwrite what
+    // it has read): the warp, its key-slice pair, or the CTA
+    auto tile_sync = [&]() {
+        if constexpr (C::WARP_LOCAL) __syncwarp();
+        else if constexpr (C::PAIR_LOCAL) {
+            if (wn == 0) named_bar_sync<1, 64>();
+            else named_bar_sync<2, 64>();
+        }
+        else __syncthreads();
+    };
     for (int t = 0; t < n_tiles; ++t) {
         cp_async_wait<STAGES - 2>();
-        // warp-local mode: the stage and the widened rows this warp reads
-        // were written by this warp alone
-        if constexpr (C::WARP_LOCAL) __syncwarp(); else __syncthreads();
+        tile_sync();
         {
             const int tn = t + STAGES - 1;
             if (tn < n_tiles) load_tile(tn, tn % STAGES);
@@ -351,7 +365,7 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
         const uint8_t *tK, *tV;
         if constexpr (C::KVT == DT_E4M3) {
             convert_tile(t % STAGES);
-            if constexpr (C::WARP_LOCAL) __syncwarp(); else __syncthreads();
+            tile_sync();
             tK = cK;
             tV = cV;
         } else {

@@ -142,6 +142,13 @@ __device__ __forceinline__ float tanh_ex2(float y) {
 // access and before any exit, so a kernel never completes ahead of its
 // predecessor.  pdl_trigger() lets the next kernel be scheduled once every
 // CTA of this one has triggered or exited.
+// named barrier ID (1..15; 0 is __syncthreads) of COUNT threads, whole
+// warps; a constant id lets the compiler reserve only the barriers in use
+template <int ID, int COUNT>
+__device__ __forceinline__ void named_bar_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
