@@ -214,16 +214,22 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
         clk.mark("start")
+        # the K timed steps, with nothing between the launches (an event
+        # between two launches would cut their programmatic chaining)
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
+        for i in range(K):
+            step()
+        t1.record()
+        torch.cuda.synchronize()
+        # the attention call alone, for its roofline: events around each call
         for i in range(K):
             va.kv_cache_write(k_new, v_new, kc, vc, slots)
             ev[i][0].record()
             va.attn_paged_decode(q, kc, vc, out, seq_lens, bt, b.max_seqlen_k, b.softmax_scale,
                                  num_splits=ns, workspace=wsp)
             ev[i][1].record()
-        t1.record()
         torch.cuda.synchronize()
         clk.mark("stop")
     if ws > 1:
@@ -241,34 +247,70 @@ def run_ours(args):
     achieved = dbytes / (attn_ms * 1e-3) / 1e9
 
     # ---------------- e2e: host inputs -> device -> result back, per step
-    h_q = q.cpu().pin_memory()
-    h_k, h_v = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-    h_slots, h_lens, h_bt = slots.cpu().pin_memory(), seq_lens.cpu().pin_memory(), bt.cpu().pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-    d_slots, d_lens, d_bt = torch.empty_like(slots), torch.empty_like(seq_lens), torch.empty_like(bt)
-    bi = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_lens, h_bt))
-    bo = h_out.numel() * h_out.element_size()
+    # The step's inputs (q, new K/V rows, slots, lengths, block table) sit
+    # packed in one pinned host buffer and go up in one copy; the result
+    # comes back in one copy.  As a serving loop runs it, both copies run on
+    # a copy stream with two device buffer sets: step k+1's inputs upload
+    # and step k's result downloads while the next step computes.
+    ins = (q, k_new, v_new, slots, seq_lens, bt)
+    offs, total = [], 0
+    for t in ins:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_in = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    for t, o in zip(ins, offs):
+        n = t.numel() * t.element_size()
+        h_in[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+    d_in = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
 
-    def e2e_step():
-        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_lens, h_lens), (d_bt, h_bt)):
-            d.copy_(h, non_blocking=True)
-        va.kv_cache_write(d_k, d_v, kc, vc, d_slots)
-        va.attn_paged_decode(d_q, kc, vc, out, d_lens, d_bt, b.max_seqlen_k, b.softmax_scale,
-                             num_splits=ns, workspace=wsp)
-        h_out.copy_(out, non_blocking=True)
+    def views(buf):
+        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(ins, offs)]
 
-    for _ in range(3):
-        e2e_step()
+    d_views = [views(d) for d in d_in]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    h_outs = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    bi = sum(t.numel() * t.element_size() for t in ins)
+    bo = out.numel() * out.element_size()
+    cur, cp = torch.cuda.current_stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]       # the compute that used buffer set i finished
+    out_free = [torch.cuda.Event() for _ in range(2)]   # the result in outs[i] has been copied back
+
+    def upload(i):
+        with torch.cuda.stream(cp):
+            cp.wait_event(done[i])                       # the step two back has read d_in[i]
+            d_in[i].copy_(h_in, non_blocking=True)
+            in_ready[i].record(cp)
+
+    def e2e_steps(n):
+        upload(0)
+        for k in range(n):
+            i = k & 1
+            if k + 1 < n:
+                upload(1 - i)
+            cur.wait_event(in_ready[i])
+            cur.wait_event(out_free[i])
+            dq, dk, dv, dslots, dlens, dbt = d_views[i]
+            va.kv_cache_write(dk, dv, kc, vc, dslots)
+            va.attn_paged_decode(dq, kc, vc, outs[i], dlens, dbt, b.max_seqlen_k, b.softmax_scale,
+                                 num_splits=ns, workspace=wsp)
+            done[i].record(cur)
+            with torch.cuda.stream(cp):
+                cp.wait_event(done[i])
+                h_outs[i].copy_(outs[i], non_blocking=True)
+                out_free[i].record(cp)
+        cur.wait_stream(cp)
+
+    e2e_steps(3)
     torch.cuda.synchronize()
     Ke = max(10, K // 4)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(Ke):
-        e2e_step()
+    e2e_steps(Ke)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
+    assert torch.equal(h_outs[(Ke - 1) & 1], out.cpu()), "e2e result differs from the device-timed step"
     e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
 
     # ---------------- chunked varlen prefill (TFLOP/s)
@@ -292,7 +334,9 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(attn_ms, 5)},
         "prefill": pf,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 5)},
+                "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 5),
+                "copies": "one packed pinned-host upload and one result download per step, on a copy "
+                          "stream overlapping the neighbouring steps' compute (two buffer sets)"},
         "gpu_launches": 3 * K,
         "clocks": clk.summary(),
     }
