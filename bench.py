@@ -673,6 +673,33 @@ def run_workload(args):
         best = max(lines.values(), key=lambda x: x["gbs"])
         res.update(metric="fp8-KV decode GB/s", value=best["gbs"], unit="GB/s", ms_per_step=best["ms"], bytes=by,
                    variants=lines, roofline={"bound": "hbm", "peak": hbm, "frac": best["frac"]})
+    elif args.workload == "fp8prefill":
+        # the chunked prefill workload's shape on an e4m3 cache: bf16 queries
+        # (K, V and Q widened to fp16 in shared memory, f16 MMAs) and e4m3
+        # queries (q_descale; S = Q K^T on e4m3 operands, kind::f8f6f4, K
+        # read from its staging slot; P V on fp16 with V widened)
+        b = W.chunked_prefill(gen_kv=False)
+        ks, vs = 4.5 / 448.0, 4.5 / 448.0
+        kc, vc = _device_cache(b, dev, torch.float8_e4m3fn, (ks, vs))
+        cu, su, bt = b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev)
+        q16 = b.q.to(dev)
+        qs = float(b.q.float().abs().max()) / 448.0
+        q8 = (b.q.float() / qs).to(torch.float8_e4m3fn).to(dev)
+        out = torch.empty(b.q.shape, dtype=torch.bfloat16, device=dev)
+        fl = prefill_flops(b)
+        lines = {}
+        for name, q, qd in (("q_bf16", q16, 1.0), ("q_e4m3", q8, qs)):
+            fn = lambda: va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt, b.max_seqlen_q, b.max_seqlen_k,
+                                                b.softmax_scale, causal=True, q_descale=qd, k_descale=ks,
+                                                v_descale=vs, num_splits=1)
+            med, mean = _time(fn, args.steps, args.warmup)
+            tf = fl / (med * 1e-3) / 1e12
+            lines[name] = {"ms": round(med, 4), "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / tc, 4)}
+        best = max(lines.values(), key=lambda x: x["tflops"])
+        res.update(metric="fp8-KV chunked prefill TFLOP/s", value=best["tflops"], unit="TFLOP/s",
+                   ms_per_step=best["ms"], flops=fl, variants=lines,
+                   roofline={"bound": "tensor", "peak": tc, "frac": best["frac_of_bf16_peak"],
+                             "note": "P V runs on fp16 MMAs, so the bf16 GEMM peak is the denominator"})
     elif args.workload == "fp8mixed":
         b = W.fp8_mixed(gen_kv=False)
         ks, vs = 4.5 / 448.0, 4.5 / 448.0           # |N(0,1)| max over ~1e8 draws is about 4.5-6
@@ -704,7 +731,7 @@ def main():
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "longctx-bs16", "longctx-bs64", "longctx-bs256", "cascade", "swa",
                              "verify", "fp8decode",
-                             "fp8mixed"],
+                             "fp8prefill", "fp8mixed"],
                     help="decode is the benchmark line; the others time one more workload each")
     args = ap.parse_args()
     if args.warmup < 3:

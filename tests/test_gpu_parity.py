@@ -704,6 +704,52 @@ def test_fp8_query_against_oracle(bs, num_splits):
     assert_no_device_error()
 
 
+def _q8_call(b, q8, qs, kc, vc, num_splits=0):
+    dev = torch.device("cuda")
+    out = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(q8.shape[:2], dtype=torch.float32, device=dev)
+    va.attn_varlen_prefill(q8.to(dev), kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev),
+                           b.block_table.to(dev), b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale, lse_out=lse,
+                           q_descale=qs, k_descale=b.k_scale, v_descale=b.v_scale, num_splits=num_splits)
+    return out, lse
+
+
+@pytest.mark.parametrize("bs", [64, 256])
+def test_fp8_query_tensor_core_page_sizes(bs):
+    """e4m3 queries on requests above 64 packed rows (the tensor-core
+    kernel: S = Q K^T as kind::f8f6f4 MMAs, K read from its 128-byte-
+    swizzled staging slot, page loads of gcd(bs, 64) rows), ragged lengths,
+    against the oracle with the same e4m3 codes and scales."""
+    b = W.make_batch([130, 17, 300, 64], [130, 400, 1000, 700], 32, 8, 128, bs, seed=62, kv_dtype="fp8")
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    qs = float(b.q.float().abs().max()) / 448.0
+    q8 = (b.q.float() / qs).to(torch.float8_e4m3fn)
+    for ns in (1, 0):
+        out, lse = _q8_call(b, q8, qs, kc, vc, ns)
+        ro, rl = oracle.attention(q8, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                                  k_scale=b.k_scale, v_scale=b.v_scale, q_scale=qs)
+        check(out, lse, ro, rl, TOL_FP8)
+    assert_no_device_error()
+
+
+def test_fp8_query_mixed_workload_sampled():
+    """The fp8 mixed batch (128 decode rows + four 2048-token prefill chunks,
+    e4m3 cache, bs 32) with e4m3 queries: every decode row and sampled
+    prefill rows against the oracle."""
+    b = W.fp8_mixed()
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    qs = float(b.q.float().abs().max()) / 448.0
+    q8 = (b.q.float() / qs).to(torch.float8_e4m3fn)
+    out, lse = _q8_call(b, q8, qs, kc, vc)
+    rows = sorted(set(range(128)) | set(_rows_sample(b, 40, seed=5)))
+    ro, rl = oracle.attention(q8, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                              k_scale=b.k_scale, v_scale=b.v_scale, q_scale=qs, rows=rows)
+    check(out, lse, ro, rl, TOL_FP8, rows=rows)
+    assert_no_device_error()
+
+
 def test_fp8_query_with_variants():
     """e4m3 queries with a sliding window, a soft cap and sinks."""
     b = W.make_batch([1, 12, 90, 1], [800, 60, 200, 1500], 32, 8, 128, 16, seed=61, kv_dtype="fp8")

@@ -18,7 +18,7 @@
 // the next item's Q and K/V loads overlap the current item's last tiles
 // and epilogue.
 //
-// Roles (11 warps, 13 with e4m3 caches):
+// Roles (11 warps; 13 with e4m3 caches, 12 with e4m3 queries):
 //   warp 0      scheduler and TMA producer: finds the CTA's next item,
 //               publishes it in a two-entry ring in shared memory, then
 //               loads Q once per item and the K_j and V_j tiles of 64 keys,
@@ -39,6 +39,12 @@
 //   warps 6-9   softmax warpgroup of Q tile B
 //   warps 11-12 (e4m3 caches only) converters: Q to fp16 in place, then
 //               every staged e4m3 tile to fp16 in a ring slot
+//   e4m3 queries (with an e4m3 cache): Q stays e4m3 and S = Q K^T runs as
+//               kind::f8f6f4 MMAs (K = 32 a step) with K read straight from
+//               its 128-byte-swizzled staging slot (released by the issuers'
+//               commits); warp 11 alone widens only the V tiles, into a ring
+//               indexed by V tile; P V stays on fp16
+//               ("FlashAttention deep dive", FA3 FP8 path)
 // TMEM columns: S_A double buffer [0,64) [64,128), S_B [128,192) [192,256),
 // O_A [256,384), O_B [384,512).  P_X(j) (bf16/fp16, two per column) is
 // written over the first 32 columns of the S buffer it was computed from and
@@ -80,10 +86,10 @@ constexpr int kBN = 64;                                // keys per K/V tile
 constexpr int kD = 128;                                // head size handled here
 constexpr uint32_t kQBytes = kBM * kD * 2;             // one Q tile, 32 KB
 constexpr uint32_t kQHalf = kBM * 128;                 // 64 columns of a Q tile
+constexpr uint32_t kQBytes8 = kBM * kD;                // one e4m3 Q tile, 16 KB (128-byte rows)
 constexpr uint32_t kTileBytes = kBN * kD * 2;          // one 16-bit K or V tile, 16 KB
 constexpr uint32_t kKVHalf = kBN * 128;                // 64 columns of a K/V tile
 constexpr uint32_t kStageBytes = kBN * kD;             // one e4m3 K or V tile, 8 KB
-constexpr int kConvChunks = kBN * kD / 16 / 64;        // 16-byte chunks of a staged tile per converter thread
 constexpr float kRescaleThreshold = 8.0f;              // log2 units
 
 // Shared memory map (offsets from a 1024-aligned base).  16-bit caches:
@@ -93,14 +99,22 @@ constexpr float kRescaleThreshold = 8.0f;              // log2 units
 // warps widen each staged tile into the fp16 ring (exact: every e4m3
 // value is an fp16 value).  The misc area holds the abort flag, the TMEM
 // address and the two-entry work-item ring.
-template <bool FP8>
+// e4m3 queries (Q8, with an e4m3 cache): Q_A, Q_B as e4m3 (16 KB each), a
+// ring of eight 16 KB fp16 slots that holds only V (K is read by the tensor
+// core straight from its staging slot), and the staging ring.
+template <bool FP8, bool Q8 = false>
 struct TcLayout {
-    static constexpr int kSlots = FP8 ? 7 : 10;
+    static_assert(!Q8 || FP8, "e4m3 queries need an e4m3 cache");
+    static constexpr uint32_t kQTile = Q8 ? kQBytes8 : kQBytes;
+    static constexpr int kSlots = FP8 ? (Q8 ? 8 : 7) : 10;
     static constexpr int kStages = FP8 ? 6 : 0;
-    static constexpr int kThreads = FP8 ? 416 : 352;
+    // converter warps: two for e4m3 caches, one with e4m3 q (V only), which
+    // keeps the CTA at 12 warps and so 168 registers a thread, not 128
+    static constexpr int kConvWarps = FP8 ? (Q8 ? 1 : 2) : 0;
+    static constexpr int kThreads = 352 + 32 * kConvWarps;
     static constexpr int kConsumerWarps = kThreads / 32 - 1;   // every warp but the producer
     static constexpr uint32_t kOffQ = 0;
-    static constexpr uint32_t kOffKV = kOffQ + 2 * kQBytes;
+    static constexpr uint32_t kOffKV = kOffQ + 2 * kQTile;
     static constexpr uint32_t kOffStage = kOffKV + kSlots * kTileBytes;
     static constexpr uint32_t kOffBar = kOffStage + kStages * kStageBytes;
     static constexpr int kNumBars = 23 + 2 * kSlots + 2 * kStages;
@@ -173,11 +187,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 // MMA_BF16: tensor-core operand type (bf16, else fp16); OUT_BF16: output
 // type (that of q); FP8: e4m3 caches, widened to fp16 in shared memory.
-template <bool MMA_BF16, bool OUT_BF16, bool FP8>
-__global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
+template <bool MMA_BF16, bool OUT_BF16, bool FP8, bool Q8 = false>
+__global__ void __launch_bounds__(TcLayout<FP8, Q8>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap qmap,
                   const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
-    using Lay = TcLayout<FP8>;
+    using Lay = TcLayout<FP8, Q8>;
+    constexpr uint32_t kQTile = Lay::kQTile;
     constexpr int kSlots = Lay::kSlots, kStages = Lay::kStages;
     constexpr uint32_t kOffQ = Lay::kOffQ, kOffKV = Lay::kOffKV, kOffStage = Lay::kOffStage;
     constexpr uint32_t kOffBar = Lay::kOffBar, kOffMisc = Lay::kOffMisc;
@@ -219,14 +234,16 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
         *never = 0;
         mbar_init(bar(B_Q), 1);
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(bar(B_FULL(s)), FP8 ? 2u : 1u);          // TMA bytes, or the two converter warps
+            mbar_init(bar(B_FULL(s)), FP8 ? (uint32_t)Lay::kConvWarps : 1u);   // TMA bytes, or the converter warps
             mbar_init(bar(B_EMPTY(s)), 2u);                    // one release per chain
         }
         for (int t = 0; t < kStages; ++t) {
             mbar_init(bar(B_STFULL(t)), 1);
-            mbar_init(bar(B_STEMPTY(t)), 2);
+            // released by the converter warps, or (e4m3 q, K stages: even t)
+            // by the two MMA issuers
+            mbar_init(bar(B_STEMPTY(t)), (Q8 && (t & 1) == 0) ? 2u : (uint32_t)Lay::kConvWarps);
         }
-        if (FP8) mbar_init(bar(B_QREADY), 2);
+        if (FP8) mbar_init(bar(B_QREADY), (uint32_t)Lay::kConvWarps);
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(B_SFULL(x, 0)), 1);
             mbar_init(bar(B_SFULL(x, 1)), 1);
@@ -370,12 +387,13 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
             if (npipe > 0) ok = warp_wait(bar(B_QFREE), (npipe - 1) & 1, abort_flag);
             if (!ok) break;
             if (lane == 0) {
-                mbar_expect_tx(bar(B_Q), (uint32_t)it.ntiles_q * kQBytes);
+                mbar_expect_tx(bar(B_Q), (uint32_t)it.ntiles_q * kQTile);
                 const int tok0 = it.q_start + it.row0 / G;
                 const int toks_per_tile = kBM / G;
+                // 16-bit q: two boxes of 64 columns; e4m3 q: one box of 128 bytes
                 for (int x = 0; x < it.ntiles_q; ++x)
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_3d(sbase + kOffQ + x * kQBytes + h * kQHalf, &qmap, h * 64, it.kvh * G,
+                    for (int h = 0; h < (Q8 ? 1 : 2); ++h)
+                        tma_load_3d(sbase + kOffQ + x * kQTile + h * kQHalf, &qmap, h * 64, it.kvh * G,
                                     tok0 + x * toks_per_tile, bar(B_Q));
             }
             __syncwarp();
@@ -462,8 +480,9 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
         // descriptors of every operand base, built once; a K slice or a
         // ring slot only adds a small offset to the start-address field
         // (addresses stay below 2^18, so the 14-bit field never carries)
-        const uint64_t dQ = sdesc_sw128(sbase + kOffQ + x * kQBytes, 16, 1024);
+        const uint64_t dQ = sdesc_sw128(sbase + kOffQ + x * kQTile, 16, 1024);
         const uint64_t dK = sdesc_sw128(sbase + kOffKV, 16, 1024);
+        const uint64_t dK8 = sdesc_sw128(sbase + kOffStage, 16, 1024);   // e4m3 q: K in its staging slot
         const uint64_t dV = sdesc_sw128(sbase + kOffKV, kKVHalf, 1024);
         const uint32_t tOx = tmem + col_o(x);
         int npipe = 0, Lbase = 0;
@@ -484,8 +503,21 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                     // every slot in order (the other chain's MMAs gate the reuse)
                     mbar_arrive(bar(B_QFREE));
                     for (int L = Lbase; L < Lbase + 2 * n_kv && ok; ++L) {
-                        ok = mbar_wait(bar(B_FULL(L % kSlots)), (L / kSlots) & 1, abort_flag);
-                        if (ok) mbar_arrive(bar(B_EMPTY(L % kSlots)));
+                        if constexpr (Q8) {
+                            if ((L & 1) == 0) {
+                                // K_j is read from its staging slot
+                                const int st = L % kStages;
+                                ok = mbar_wait(bar(B_STFULL(st)), (L / kStages) & 1, abort_flag);
+                                if (ok) mbar_arrive(bar(B_STEMPTY(st)));
+                            } else {
+                                const int v = L >> 1;           // fp16 ring position (V only)
+                                ok = mbar_wait(bar(B_FULL(v % kSlots)), (v / kSlots) & 1, abort_flag);
+                                if (ok) mbar_arrive(bar(B_EMPTY(v % kSlots)));
+                            }
+                        } else {
+                            ok = mbar_wait(bar(B_FULL(L % kSlots)), (L / kSlots) & 1, abort_flag);
+                            if (ok) mbar_arrive(bar(B_EMPTY(L % kSlots)));
+                        }
                     }
                 }
                 for (int j = 0; active && j <= n_kv && ok; ++j) {
@@ -493,23 +525,39 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                     const int LV = LK - 1;                 // load index of V_(j-1)
                     const int jg = jx + j;                 // chain tile index of K_j
                     if (j < n_kv) {
-                        const int sk = LK % kSlots;
-                        ok = mbar_wait(bar(B_FULL(sk)), (LK / kSlots) & 1, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint64_t b0 = dK + ((sk * kTileBytes) >> 4);
                         const uint32_t d = tmem + col_s(x, jg & 1);
+                        if constexpr (Q8) {
+                            // S = Q K^T on e4m3 operands (K = 32 a step), K read
+                            // straight from its 128-byte-swizzled staging slot
+                            const int st = LK % kStages;
+                            ok = mbar_wait(bar(B_STFULL(st)), (LK / kStages) & 1, abort_flag);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint64_t b0 = dK8 + ((st * kStageBytes) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < kD / 16; ++kk)
-                            umma_ss(d, dQ + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
-                                    b0 + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
-                        umma_commit(bar(B_SFULL(x, jg & 1)));
-                        umma_commit(bar(B_EMPTY(sk)));
+                            for (int kk = 0; kk < kD / 32; ++kk)
+                                umma_ss_f8(d, dQ + ((kk * 32) >> 4), b0 + ((kk * 32) >> 4), idS, kk > 0 ? 1u : 0u);
+                            umma_commit(bar(B_SFULL(x, jg & 1)));
+                            umma_commit(bar(B_STEMPTY(st)));
+                        } else {
+                            const int sk = LK % kSlots;
+                            ok = mbar_wait(bar(B_FULL(sk)), (LK / kSlots) & 1, abort_flag);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint64_t b0 = dK + ((sk * kTileBytes) >> 4);
+#pragma unroll
+                            for (int kk = 0; kk < kD / 16; ++kk)
+                                umma_ss(d, dQ + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
+                                        b0 + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
+                            umma_commit(bar(B_SFULL(x, jg & 1)));
+                            umma_commit(bar(B_EMPTY(sk)));
+                        }
                         if (j == n_kv - 1) umma_commit(bar(B_QFREE));
                     }
                     if (j > 0) {
-                        const int sv = LV % kSlots;
-                        ok = mbar_wait(bar(B_FULL(sv)), (LV / kSlots) & 1, abort_flag);
+                        const int vpos = Q8 ? (LV >> 1) : LV;    // fp16 ring position of V_(j-1)
+                        const int sv = vpos % kSlots;
+                        ok = mbar_wait(bar(B_FULL(sv)), (vpos / kSlots) & 1, abort_flag);
                         if (ok) ok = mbar_wait(bar(B_PFULL(x, (jg - 1) & 1)), ((jg - 1) >> 1) & 1, abort_flag);
                         // the item's first P V overwrites O_X: the previous
                         // item's epilogue must have read it out
@@ -552,8 +600,10 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
         // soft cap: S -> cap * log2(e) * tanh(S * scale * k_descale / cap),
         // already in log2 units; else S * scale * k_descale * log2(e)
         const bool capped = p.cap_in > 0.f;
-        const float cap_in = FP8 ? p.cap_in * kE4m3Lo8Scale : p.cap_in;
-        const float sl2 = capped ? 1.f : (FP8 ? p.scale_log2 * kE4m3Lo8Scale : p.scale_log2);
+        // (with e4m3 q, K is not widened: S carries no 2^-8)
+        constexpr bool kWideK = FP8 && !Q8;
+        const float cap_in = kWideK ? p.cap_in * kE4m3Lo8Scale : p.cap_in;
+        const float sl2 = capped ? 1.f : (kWideK ? p.scale_log2 * kE4m3Lo8Scale : p.scale_log2);
         int Lbase = 0, jx = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -694,8 +744,10 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                         // not loaded) -- zero them so 0 * V cannot produce NaN.  Both
                         // warpgroups write the same zeros, each before publishing its
                         // own P, because either issuer may read the tile first.
-                        const int Lv = Lbase + 2 * j + 1, sv = Lv % kSlots;
-                        ok = warp_wait(bar(B_FULL(sv)), (Lv / kSlots) & 1, abort_flag);
+                        const int Lv = Lbase + 2 * j + 1;
+                        const int vpos = Q8 ? (Lv >> 1) : Lv;   // fp16 ring position of V_j
+                        const int sv = vpos % kSlots;
+                        ok = warp_wait(bar(B_FULL(sv)), (vpos / kSlots) & 1, abort_flag);
                         if (!ok) break;
                         __syncwarp();
                         if (trow < kBN && trow >= kv_hi - n0) {
@@ -785,8 +837,10 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
             Lbase += 2 * n_kv;
         }
     } else if constexpr (FP8) {
-        // ============================== e4m3 -> fp16 converters (warps 11, 12)
-        const int cid = tid - 352;                 // 0 .. 63
+        // ================ e4m3 -> fp16 converters (warps 11, 12; 11 alone with e4m3 q)
+        constexpr int kConvThreads = 32 * Lay::kConvWarps;
+        constexpr int kConvChunks = kBN * kD / 16 / kConvThreads;   // 16-byte chunks of a staged tile a thread
+        const int cid = tid - 352;                 // 0 .. kConvThreads - 1
         int npipe = 0, Lbase = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -797,10 +851,10 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
             ok = warp_wait(bar(B_Q), npipe & 1, abort_flag);
             if (!ok) break;
             __syncwarp();
-            if constexpr (OUT_BF16) {
+            if constexpr (OUT_BF16 && !Q8) {
                 // q arrived as bf16; the MMAs run on fp16 operands: convert in place
                 uint4 *qv = reinterpret_cast<uint4 *>(sm + kOffQ);
-                for (int c = cid; c < it.ntiles_q * (int)(kQBytes / 16); c += 64) {
+                for (int c = cid; c < it.ntiles_q * (int)(kQBytes / 16); c += kConvThreads) {
                     const uint4 raw4 = qv[c];
                     const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw4);
                     uint4 w;
@@ -816,8 +870,11 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_QREADY));
-            for (int L = Lbase; L < Lbase + 2 * it.n_kv && ok; ++L) {
-                const int st = L % kStages, sl = L % kSlots;
+            // every staged tile, or with e4m3 q only the V tiles (odd L; the
+            // tensor core reads K in its staging slot), at ring position v
+            for (int L = Lbase + (Q8 ? 1 : 0); L < Lbase + 2 * it.n_kv && ok; L += (Q8 ? 2 : 1)) {
+                const int v = Q8 ? (L >> 1) : L;
+                const int st = L % kStages, sl = v % kSlots;
                 ok = warp_wait(bar(B_STFULL(st)), (L / kStages) & 1, abort_flag);
                 if (!ok) break;
                 __syncwarp();
@@ -828,17 +885,17 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                 uint4 raw8[kConvChunks];
 #pragma unroll
                 for (int u = 0; u < kConvChunks; ++u) {
-                    const int i = cid + 64 * u;
+                    const int i = cid + kConvThreads * u;
                     raw8[u] = *reinterpret_cast<const uint4 *>(src + (i >> 3) * 128 + (i & 7) * 16);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_STEMPTY(st)));
-                if (L >= kSlots) ok = warp_wait(bar(B_EMPTY(sl)), ((L / kSlots) - 1) & 1, abort_flag);
+                if (v >= kSlots) ok = warp_wait(bar(B_EMPTY(sl)), ((v / kSlots) - 1) & 1, abort_flag);
                 if (!ok) break;
                 uint8_t *dst = sm + kOffKV + sl * kTileBytes;
 #pragma unroll
                 for (int u = 0; u < kConvChunks; ++u) {
-                    const int i = cid + 64 * u;
+                    const int i = cid + kConvThreads * u;
                     const int row = i >> 3, c = i & 7;          // e4m3 columns 16c .. 16c + 15 of one key
                     const uint4 raw4 = raw8[u];
                     uint4 lo, hi;                                // fp16 patterns of value * 2^-8
@@ -896,7 +953,7 @@ static int gcd_int(int a, int b) {
 bool tc_supported(int D, int q_dtype, int kv_dtype, int G) {
     if (D != kD) return false;
     const bool ok_types = (q_dtype == DT_BF16 && kv_dtype == DT_BF16) || (q_dtype == DT_FP16 && kv_dtype == DT_FP16) ||
-                          ((q_dtype == DT_BF16 || q_dtype == DT_FP16) && kv_dtype == DT_E4M3);
+                          ((q_dtype == DT_BF16 || q_dtype == DT_FP16 || q_dtype == DT_E4M3) && kv_dtype == DT_E4M3);
     if (!ok_types) return false;
     if (G <= 0 || G > 128 || (128 % G) != 0) return false;
     return true;
@@ -904,11 +961,11 @@ bool tc_supported(int D, int q_dtype, int kv_dtype, int G) {
 
 int tc_rows_per_cta() { return 2 * kBM; }
 
-template <bool MMA_BF16, bool OUT_BF16, bool FP8>
+template <bool MMA_BF16, bool OUT_BF16, bool FP8, bool Q8 = false>
 static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &qmap, const CUtensorMap &kmap,
                              const CUtensorMap &vmap, dim3 grid, cudaStream_t stream) {
-    using Lay = TcLayout<FP8>;
-    auto kern = fwd_tc_kernel<MMA_BF16, OUT_BF16, FP8>;
+    using Lay = TcLayout<FP8, Q8>;
+    auto kern = fwd_tc_kernel<MMA_BF16, OUT_BF16, FP8, Q8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, dim3(Lay::kThreads), Lay::kSmemBytes, stream, tp, qmap, kmap, vmap);
@@ -935,18 +992,24 @@ cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int kv_dtype, int64_t
         tp.sched = slots[dev] + 2 * (next[dev].fetch_add(1u) % kSchedSlots);
     }
     const bool q16 = q_dtype == DT_FP16;
+    const bool q8 = q_dtype == DT_E4M3;
     const bool fp8 = kv_dtype == DT_E4M3;
     CUtensorMap qmap, kmap, vmap;
-    // Q viewed as [T][Hq][D]: box = 64 columns x G heads x (128 / G) tokens
-    if (!encode_3d_bf16(&qmap, f.q, q16, kD, (uint64_t)f.Hq, (uint64_t)T, (uint64_t)kD * 2,
-                        (uint64_t)f.q_stride * 2, 64, (uint32_t)f.G, (uint32_t)(kBM / f.G)))
+    // Q viewed as [T][Hq][D]: box = 64 columns (16-bit) or all 128 bytes
+    // (e4m3) x G heads x (128 / G) tokens, 128-byte swizzle
+    if (q8 ? !encode_3d_u8(&qmap, f.q, kD, (uint64_t)f.Hq, (uint64_t)T, (uint64_t)kD, (uint64_t)f.q_stride, kD,
+                           (uint32_t)f.G, (uint32_t)(kBM / f.G), true)
+           : !encode_3d_bf16(&qmap, f.q, q16, kD, (uint64_t)f.Hq, (uint64_t)T, (uint64_t)kD * 2,
+                             (uint64_t)f.q_stride * 2, 64, (uint32_t)f.G, (uint32_t)(kBM / f.G)))
         return cudaErrorInvalidValue;
     // caches viewed as [num_blocks * bs][Hkv][D]: box = 1 head x R rows and
     // 64 columns (16-bit, swizzled) or all 128 bytes of a row (e4m3)
     const uint64_t nslots = (uint64_t)f.num_blocks * f.bs;
     const uint32_t R = (uint32_t)tp.kv_rows;
     if (fp8) {
-        if (!encode_3d_u8(&kmap, f.k_cache, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD, (uint64_t)f.Hkv * kD, kD, 1, R) ||
+        // (e4m3 q: K swizzled for the tensor core, which reads it staged)
+        if (!encode_3d_u8(&kmap, f.k_cache, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD, (uint64_t)f.Hkv * kD, kD, 1, R,
+                          q8) ||
             !encode_3d_u8(&vmap, f.v_cache, kD, (uint64_t)f.Hkv, nslots, (uint64_t)kD, (uint64_t)f.Hkv * kD, kD, 1, R))
             return cudaErrorInvalidValue;
     } else {
@@ -959,6 +1022,8 @@ cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int kv_dtype, int64_t
     // persistent: one CTA per SM, never more CTAs than the class can have items
     const long long max_items = (long long)f.n_row_blocks * f.nsplit * f.Hkv * f.B;
     dim3 grid((unsigned)std::max(1LL, std::min<long long>(num_sms, max_items)));
+    if (q8)   // e4m3 q and cache: S on e4m3 MMAs, P V on fp16 (V widened); bf16 output
+        return launch_tc<false, true, true, true>(tp, qmap, kmap, vmap, grid, stream);
     if (fp8) {
         // e4m3 caches: fp16 MMAs (the widening is exact); output in q's type
         return q16 ? launch_tc<false, false, true>(tp, qmap, kmap, vmap, grid, stream)

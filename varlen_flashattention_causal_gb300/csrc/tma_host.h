@@ -43,10 +43,12 @@ inline bool encode_3d_bf16(CUtensorMap *map, const void *base, bool fp16, uint64
     return r == CUDA_SUCCESS;
 }
 
-// 3-D map over bytes (e4m3 caches): same shape rules, no swizzle (the
-// converter warps read the staged rows and write the swizzled fp16 tile).
+// 3-D map over bytes (e4m3): same shape rules.  No swizzle where converter
+// warps read the staged rows; the 128-byte swizzle (sw128) where the tensor
+// core reads the tile directly (e4m3 Q and K of the e4m3-query kernel).
 inline bool encode_3d_u8(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                         bool sw128 = false) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -54,8 +56,8 @@ inline bool encode_3d_u8(CUtensorMap *map, const void *base, uint64_t d0, uint64
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
