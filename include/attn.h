@@ -154,9 +154,10 @@ attn_status attn_varlen_prefill(
  *     (a query with no visible key then gets out = 0, lse = z_h).
  * fp8 queries ([vLLM-FA] FA3 FP8 support, q_descale): q_dtype may be
  *   ATTN_FP8_E4M3 when kv_dtype is ATTN_FP8_E4M3 and D is 128; a query
- *   element's value is then code * q_descale, QK^T runs on e4m3 operands,
- *   out is bf16, and q_stride_tok must be a multiple of 16 elements.  For
- *   16-bit queries pass q_descale = 1.
+ *   element's value is then code * q_descale, QK^T runs on e4m3 operands
+ *   (K codes as stored: a NaN code in K or q gives NaN scores, unlike the
+ *   widened +-480 above), out is bf16, and q_stride_tok must be a multiple
+ *   of 16 elements.  For 16-bit queries pass q_descale = 1.
  * Errors as attn_varlen_prefill, plus ATTN_ERR_SHAPE for a window bound
  * below -1 or a negative or NaN softcap.  attn_varlen_prefill is this call
  * with q_descale 1, window (-1, -1), softcap 0 and no sinks.
