@@ -18,7 +18,7 @@
 // the next item's Q and K/V loads overlap the current item's last tiles
 // and epilogue.
 //
-// Roles (11 warps; 13 with e4m3 caches, 12 with e4m3 queries):
+// Roles (11 warps; 15 with e4m3 caches, 12 with e4m3 queries):
 //   warp 0      scheduler and TMA producer: finds the CTA's next item,
 //               publishes it in a two-entry ring in shared memory, then
 //               loads Q once per item and the K_j and V_j tiles of 64 keys,
@@ -37,7 +37,7 @@
 //               rows) still waits for every slot of the item and releases it.
 //   warps 2-5   softmax warpgroup of Q tile A, one thread per row
 //   warps 6-9   softmax warpgroup of Q tile B
-//   warps 11-12 (e4m3 caches only) converters: Q to fp16 in place, then
+//   warps 11-14 (e4m3 caches only) converters: Q to fp16 in place, then
 //               every staged e4m3 tile to fp16 in a ring slot
 //   e4m3 queries (with an e4m3 cache): Q stays e4m3 and S = Q K^T runs as
 //               kind::f8f6f4 MMAs (K = 32 a step) with K read straight from
@@ -95,7 +95,7 @@ constexpr float kRescaleThreshold = 8.0f;              // log2 units
 // Shared memory map (offsets from a 1024-aligned base).  16-bit caches:
 // Q_A, Q_B, then a ring of ten 16 KB K/V slots the TMA fills directly.
 // e4m3 caches: Q_A, Q_B, a ring of seven 16 KB fp16 slots, and a ring of
-// six 8 KB staging slots the TMA fills with e4m3 pages; two converter
+// six 8 KB staging slots the TMA fills with e4m3 pages; the converter
 // warps widen each staged tile into the fp16 ring (exact: every e4m3
 // value is an fp16 value).  The misc area holds the abort flag, the TMEM
 // address and the two-entry work-item ring.
@@ -108,9 +108,10 @@ struct TcLayout {
     static constexpr uint32_t kQTile = Q8 ? kQBytes8 : kQBytes;
     static constexpr int kSlots = FP8 ? (Q8 ? 8 : 7) : 10;
     static constexpr int kStages = FP8 ? 6 : 0;
-    // converter warps: two for e4m3 caches, one with e4m3 q (V only), which
-    // keeps the CTA at 12 warps and so 168 registers a thread, not 128
-    static constexpr int kConvWarps = FP8 ? (Q8 ? 1 : 2) : 0;
+    // converter warps: four for e4m3 caches with 16-bit q (K, V and Q to
+    // widen; 13 to 15 warps all leave 128 registers a thread), one with
+    // e4m3 q (V only), which keeps the CTA at 12 warps and 168 registers
+    static constexpr int kConvWarps = FP8 ? (Q8 ? 1 : 4) : 0;
     static constexpr int kThreads = 352 + 32 * kConvWarps;
     static constexpr int kConsumerWarps = kThreads / 32 - 1;   // every warp but the producer
     static constexpr uint32_t kOffQ = 0;
@@ -837,7 +838,7 @@ __global__ void __launch_bounds__(TcLayout<FP8, Q8>::kThreads, 1)
             Lbase += 2 * n_kv;
         }
     } else if constexpr (FP8) {
-        // ================ e4m3 -> fp16 converters (warps 11, 12; 11 alone with e4m3 q)
+        // =========== e4m3 -> fp16 converters (warps 11-14; 11 alone with e4m3 q)
         constexpr int kConvThreads = 32 * Lay::kConvWarps;
         constexpr int kConvChunks = kBN * kD / 16 / kConvThreads;   // 16-byte chunks of a staged tile a thread
         const int cid = tid - 352;                 // 0 .. kConvThreads - 1
