@@ -280,7 +280,7 @@ attn_status run_fwd(const FwdArgs &a) {
         if (c.tc)
             st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.kv_dtype, a.T, dev->sms, a.stream));
         else
-            st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, c.rpc, a.stream));
+            st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, c.rpc, a.max_q <= 1, a.stream));
         if (st != ATTN_OK) return st;
     }
     if (stride > 1) {

@@ -80,6 +80,11 @@ struct MmaCfg {
     static constexpr int EPI_BYTES = WN * ROWS * OSTRIDE * 4 + 2 * WN * ROWS * 4;
     static constexpr int MAIN_BYTES = STAGES * STAGE_BYTES + CONV_BYTES;
     static constexpr int SMEM = Q_BYTES + (MAIN_BYTES > EPI_BYTES ? MAIN_BYTES : EPI_BYTES);
+    // decode shape with two stages: more CTAs per SM instead of a deeper
+    // ring -- e4m3 cache: 52 KB and at most 128 registers a thread, four CTAs
+    // (three with three stages); 16-bit cache: 68 KB and at most 168
+    // registers, three CTAs (two with three stages, at 100 KB)
+    static constexpr int MIN_BLOCKS = (WARP_LOCAL && STAGES == 2) ? (KVT == DT_E4M3 ? 4 : 3) : 1;
     static_assert(WM * WN == 4, "4 warps");
     static_assert(NT % 2 == 0, "n-tile pairs");
     static_assert((RPW * CH) % 32 == 0, "whole warp copy rounds");
@@ -88,7 +93,7 @@ struct MmaCfg {
 constexpr float kRescaleLog2 = 8.0f;   // reference-maximum threshold (log2 units)
 
 template <class C>
-__global__ void __launch_bounds__(128) fwd_mma_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(128, C::MIN_BLOCKS) fwd_mma_kernel(const FwdParams p) {
     constexpr int D = C::D, ROWS = C::ROWS, BN = C::BN, STAGES = C::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *sQ = smem;
@@ -621,36 +626,42 @@ static cudaError_t launch_cfg(const FwdParams &p, cudaStream_t stream) {
 }
 
 template <int D, int QT, int KVT>
-static cudaError_t launch_rows(const FwdParams &p, int rows_per_cta, cudaStream_t stream) {
-    // e4m3, D 128: three stages and one widened tile keep a CTA at 68 KB
-    // of shared memory, three CTAs per SM
-    constexpr int STAGES = (KVT == DT_E4M3) ? (D == 128 ? 3 : 4) : (D == 128 ? 3 : 4);
+static cudaError_t launch_rows(const FwdParams &p, int rows_per_cta, bool single_token, cudaStream_t stream) {
+    // D 128: three stages (e4m3: plus one widened tile, 68 KB).  16-row CTAs
+    // run two, for more CTAs per SM (see MmaCfg::MIN_BLOCKS), on e4m3 caches
+    // (faster on the fp8 decode and mixed batches) and on 16-bit caches when
+    // every request of the call has one query token (16-bit verify rows of
+    // several tokens measured faster with the deeper ring)
+    constexpr int STAGES = (D == 128) ? 3 : 4;
     switch (rows_per_cta) {
-    case 16: return launch_cfg<MmaCfg<D, 1, 4, 64, STAGES, QT, KVT>>(p, stream);
+    case 16:
+        if (D == 128 && (KVT == DT_E4M3 || single_token)) return launch_cfg<MmaCfg<D, 1, 4, 64, 2, QT, KVT>>(p, stream);
+        return launch_cfg<MmaCfg<D, 1, 4, 64, STAGES, QT, KVT>>(p, stream);
     case 32: return launch_cfg<MmaCfg<D, 2, 2, 64, STAGES, QT, KVT>>(p, stream);
     default: return launch_cfg<MmaCfg<D, 4, 1, 64, STAGES, QT, KVT>>(p, stream);
     }
 }
 
 template <int D>
-static cudaError_t launch_d(const FwdParams &p, int q_dtype, int kv_dtype, int rows_per_cta, cudaStream_t s) {
+static cudaError_t launch_d(const FwdParams &p, int q_dtype, int kv_dtype, int rows_per_cta, bool single_token,
+                            cudaStream_t s) {
     if (q_dtype == DT_E4M3 && kv_dtype == DT_E4M3) {
-        if constexpr (D == 128) return launch_rows<D, DT_E4M3, DT_E4M3>(p, rows_per_cta, s);
+        if constexpr (D == 128) return launch_rows<D, DT_E4M3, DT_E4M3>(p, rows_per_cta, single_token, s);
         return cudaErrorInvalidValue;
     }
-    if (q_dtype == DT_BF16 && kv_dtype == DT_BF16) return launch_rows<D, DT_BF16, DT_BF16>(p, rows_per_cta, s);
-    if (q_dtype == DT_FP16 && kv_dtype == DT_FP16) return launch_rows<D, DT_FP16, DT_FP16>(p, rows_per_cta, s);
-    if (q_dtype == DT_BF16 && kv_dtype == DT_E4M3) return launch_rows<D, DT_BF16, DT_E4M3>(p, rows_per_cta, s);
-    if (q_dtype == DT_FP16 && kv_dtype == DT_E4M3) return launch_rows<D, DT_FP16, DT_E4M3>(p, rows_per_cta, s);
+    if (q_dtype == DT_BF16 && kv_dtype == DT_BF16) return launch_rows<D, DT_BF16, DT_BF16>(p, rows_per_cta, single_token, s);
+    if (q_dtype == DT_FP16 && kv_dtype == DT_FP16) return launch_rows<D, DT_FP16, DT_FP16>(p, rows_per_cta, single_token, s);
+    if (q_dtype == DT_BF16 && kv_dtype == DT_E4M3) return launch_rows<D, DT_BF16, DT_E4M3>(p, rows_per_cta, single_token, s);
+    if (q_dtype == DT_FP16 && kv_dtype == DT_E4M3) return launch_rows<D, DT_FP16, DT_E4M3>(p, rows_per_cta, single_token, s);
     return cudaErrorInvalidValue;
 }
 
 int mma_rows_per_cta(int max_rows) { return max_rows <= 16 ? 16 : (max_rows <= 32 ? 32 : 64); }
 
-cudaError_t launch_fwd_mma(const FwdParams &p, int D, int q_dtype, int kv_dtype, int rows_per_cta,
+cudaError_t launch_fwd_mma(const FwdParams &p, int D, int q_dtype, int kv_dtype, int rows_per_cta, bool single_token,
                            cudaStream_t stream) {
-    if (D == 64) return launch_d<64>(p, q_dtype, kv_dtype, rows_per_cta, stream);
-    if (D == 128) return launch_d<128>(p, q_dtype, kv_dtype, rows_per_cta, stream);
+    if (D == 64) return launch_d<64>(p, q_dtype, kv_dtype, rows_per_cta, single_token, stream);
+    if (D == 128) return launch_d<128>(p, q_dtype, kv_dtype, rows_per_cta, single_token, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -88,7 +88,8 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // launchers (return the launch error)
-cudaError_t launch_fwd_mma(const FwdParams &p, int D, int q_dtype, int kv_dtype, int rows_per_cta,
+// single_token: every request of the call has one query token (max_q 1)
+cudaError_t launch_fwd_mma(const FwdParams &p, int D, int q_dtype, int kv_dtype, int rows_per_cta, bool single_token,
                            cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, int out_dtype, cudaStream_t stream);
 cudaError_t launch_merge(void *out, float *lse_out, const void *o1, const float *lse1, const void *o2,
