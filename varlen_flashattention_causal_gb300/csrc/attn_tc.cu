@@ -122,6 +122,9 @@ struct TcLayout {
     static constexpr uint32_t kOffMisc = kOffBar + 8 * 64;
     static constexpr uint32_t kSmemBytes = kOffMisc + 128 + 1024;   // + alignment slack
     static_assert(kNumBars <= 64, "barrier area");
+    // e4m3 q: K loads (even load index) must always land in even stages, whose
+    // release count (the two issuers) differs from the V stages' (converters)
+    static_assert(!Q8 || kStages % 2 == 0, "K and V keep their stage parity");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
