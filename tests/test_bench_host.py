@@ -1,0 +1,66 @@
+"""Host-side checks of the benchmark's measurement arithmetic: the algorithmic
+bytes and flops the roofline fractions divide by, recounted by brute force
+from their definitions, and the gate that attaches the recorded DRAM traffic
+only to the kernel sources it was captured from.  No GPU."""
+import os
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from varlen_flashattention_causal_gb300 import workloads as W  # noqa: E402
+
+
+def _visible_pairs(q_len, kv_len):
+    """(query, key) pairs a causal, bottom-right-aligned request attends to,
+    counted one by one."""
+    ctx = kv_len - q_len
+    return sum(1 for i in range(q_len) for j in range(kv_len) if j <= ctx + i)
+
+
+@pytest.mark.parametrize("q_lens,kv_lens", [([6, 4, 17, 33], [6, 4, 17, 33]),
+                                             ([1, 5, 9], [40, 5, 30]),
+                                             ([3], [3])])
+def test_prefill_flops_counts_visible_pairs(q_lens, kv_lens):
+    b = W.make_batch(q_lens, kv_lens, 8, 2, 64, 16, seed=3)
+    pairs = sum(_visible_pairs(q, k) for q, k in zip(q_lens, kv_lens))
+    # Q K^T and P V: 2 flops per multiply-add, D of each per pair and head
+    assert bench.prefill_flops(b) == 4 * b.D * b.Hq * pairs
+
+
+def test_decode_bytes_counts_each_cached_row_once_per_kv_head():
+    b = W.make_batch([1, 1, 1], [17, 40, 3], 8, 2, 64, 16, seed=4)
+    kv = 0
+    for L in b.kv_lens:
+        for _tok in range(L):
+            kv += b.Hkv * b.D * 2 * 2          # K and V rows of every KV head, bf16
+    qo = 2 * b.T * b.Hq * b.D * 2              # q read, out written
+    pages = sum(-(-L // b.bs) for L in b.kv_lens)
+    assert bench.decode_bytes(b) == kv + qo + pages * 4 + b.B * 4
+    # e4m3 caches: one byte per cached value
+    assert bench.decode_bytes(b, elem=1) == kv // 2 + qo + pages * 4 + b.B * 4
+
+
+def test_traffic_gate_follows_the_kernel_sources(monkeypatch):
+    t = dict(bench.DECODE_TRAFFIC)
+    # recorded bytes are returned only while the sources hash as recorded
+    monkeypatch.setattr(bench, "DECODE_TRAFFIC", dict(t, sha256=bench.source_hash(t["sources"])))
+    assert bench.decode_traffic() == t["bytes"]
+    monkeypatch.setattr(bench, "DECODE_TRAFFIC", dict(t, sha256="0" * 64))
+    assert bench.decode_traffic() is None
+    monkeypatch.setattr(bench, "DECODE_TRAFFIC", dict(t, bytes=None))
+    assert bench.decode_traffic() is None
+
+
+def test_recorded_traffic_is_close_to_the_algorithmic_bytes():
+    """The recorded DRAM traffic of the decode split kernel stays within a few
+    percent above the algorithmic bytes (K/V read once per KV head); a value
+    far above would mean re-reads, far below a capture of another launch."""
+    b = W.decode_llama8b(device="cpu", gen_kv=False)
+    alg = bench.decode_bytes(b)
+    rec = bench.DECODE_TRAFFIC["bytes"]
+    assert 0.99 * alg <= rec <= 1.05 * alg
