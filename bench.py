@@ -82,6 +82,17 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value, ws, device=None):
+    """The slowest rank's value (every rank times the same K steps of its own
+    replica); the value itself when there is one rank."""
+    if ws <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
 def decode_bytes(b, elem=2):
     """Algorithmic bytes of one decode attention call: every cached K and V
     row once per KV head, q and out once, the block-table entries and
@@ -234,11 +245,7 @@ def run_ours(args):
         clk.mark("stop")
     if ws > 1:
         dist.barrier()
-    elapsed_ms = t0.elapsed_time(t1)
-    if ws > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
     attn_ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
     dbytes = decode_bytes(b)
     step_bytes = dbytes + kv_write_bytes(b.B, b.Hkv, b.D)

@@ -4,6 +4,7 @@ from their definitions, and the gate that attaches the recorded DRAM traffic
 only to the kernel sources it was captured from.  No GPU."""
 import os
 import sys
+import time
 
 import pytest
 import torch
@@ -64,3 +65,47 @@ def test_recorded_traffic_is_close_to_the_algorithmic_bytes():
     alg = bench.decode_bytes(b)
     rec = bench.DECODE_TRAFFIC["bytes"]
     assert 0.99 * alg <= rec <= 1.05 * alg
+
+
+# ------------------------------------------- several ranks (gloo, CPU)
+
+def _gloo_worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank, world_size=world)
+    try:
+        ws, r, local = bench.dist_env()
+        # each rank's own time; the line reports the slowest
+        slowest = bench.max_over_ranks(1.5 + rank, ws)
+
+        class Args:
+            steps, warmup = 1, 3
+        t0 = time.perf_counter()
+        ref = bench.run_reference(Args()) if rank != 0 else None     # non-zero ranks return at once
+        q.put((rank, ws, r, local, slowest, ref, time.perf_counter() - t0))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_report_the_slowest_and_only_rank0_works():
+    """world_size 2 over gloo: both ranks read their place from the
+    environment, agree on the slowest rank's time, and the reference arm does
+    no work on rank 1."""
+    import multiprocessing as mp
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_gloo_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [o[:4] for o in out] == [(0, 2, 0, 0), (1, 2, 1, 1)]
+    assert all(o[4] == 2.5 for o in out)
+    assert out[1][5] is None and out[1][6] < 5.0
