@@ -234,6 +234,27 @@ def test_fp8_kv_small(D):
         check(out, lse, ro, rl, TOL_FP8)
 
 
+def test_fp8_kv_verify_rows():
+    """e4m3 cache under verify-sized requests only (at most 8 query tokens,
+    so at most 32 packed rows in the call): the 16-row CTAs and the 32-row
+    CTAs whose key-slice pairs fetch and widen only their own rows, with bf16
+    and with e4m3 queries."""
+    b = W.make_batch([1, 5, 8, 3, 7, 1], [300, 64, 500, 40, 129, 2], 32, 8, 128, 16, seed=18, kv_dtype="fp8")
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    ro, rl = ref_attn(b, ck, cv)
+    for ns in (1, 0):
+        out, lse = gpu_attn(b, kc, vc, num_splits=ns)
+        check(out, lse, ro, rl, TOL_FP8)
+    qs = float(b.q.float().abs().max()) / 448.0
+    q8 = (b.q.float() / qs).to(torch.float8_e4m3fn)
+    out, lse = _q8_call(b, q8, qs, kc, vc)
+    ro8, rl8 = oracle.attention(q8, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                                k_scale=b.k_scale, v_scale=b.v_scale, q_scale=qs)
+    check(out, lse, ro8, rl8, TOL_FP8)
+    assert_no_device_error()
+
+
 # ------------------------------------------------------------- edge cases
 
 def test_empty_and_degenerate_requests():
