@@ -222,6 +222,19 @@ def test_fp16_path():
         check(out, lse, ro, rl, TOL)
 
 
+def test_fp16_single_token_calls():
+    """A call in which every request has one query token (fp16): the 16-row
+    CTAs run the two-stage configuration."""
+    b = W.make_batch([1, 1, 1, 1], [300, 1, 77, 1000], 8, 2, 128, 16, seed=9, q_dtype=torch.float16)
+    kc, vc = gpu_cache(b)
+    ro, rl = ref_attn(b, *cpu_cache(b))
+    for ns in (1, 4, 0):
+        out, lse = gpu_attn(b, kc, vc, num_splits=ns)
+        assert out.dtype == torch.float16
+        check(out, lse, ro, rl, TOL)
+    assert_no_device_error()
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_fp8_kv_small(D):
     b = W.make_batch([1, 1, 12, 3], [200, 33, 64, 3], 8, 2, D, 32, seed=8, kv_dtype="fp8")
