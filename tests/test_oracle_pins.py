@@ -188,32 +188,39 @@ def test_two_keys_closed_form():
 def test_equal_scores_give_mean_of_visible_values(ctx):
     """q = 0 makes every visible score 0: out = mean of the visible V rows
     and lse = ln(#visible).  With cached context ctx, query i sees ctx+i+1
-    keys (bottom-right alignment, multi-request page sec. 10)."""
+    keys (bottom-right alignment, multi-request page sec. 10).  Both the
+    paged oracle and the dense formulation."""
     q_len = 7
     b = W.make_batch([q_len], [ctx + q_len], Hq=2, Hkv=2, D=16, bs=16, seed=6)
     b.q.zero_()
     out, lse = run(b)
+    dense, dense_lse, _ = _dense(b)
     _, v = key_rows(b, 0)
     for i in range(q_len):
         n = ctx + i + 1
         for h in range(2):
-            np.testing.assert_allclose(out[i, h].numpy(), v[:n, h].double().mean(0).numpy(),
-                                       rtol=0, atol=1e-14)
+            want = v[:n, h].double().mean(0).numpy()
+            np.testing.assert_allclose(out[i, h].numpy(), want, rtol=0, atol=1e-14)
+            np.testing.assert_allclose(dense[i, h], want, rtol=0, atol=1e-14)
             assert abs(float(lse[i, h]) - math.log(n)) < 1e-13
+            assert abs(float(dense_lse[i, h]) - math.log(n)) < 1e-13
 
 
 def test_gqa_head_mapping():
     """Query head h reads KV head h // (Hq / Hkv).  Each KV head holds a
     different constant value row, so with q = 0 the output of head h is
-    exactly that constant."""
+    exactly that constant, in the paged oracle and in the dense formulation."""
     Hq, Hkv = 8, 2
     b = W.make_batch([3], [3], Hq=Hq, Hkv=Hkv, D=16, bs=16, seed=7)
     b.q.zero_()
     for g in range(Hkv):
         b.v_tok[:, g, :] = float(g + 1)
     out, _ = run(b)
+    dense, _, _ = _dense(b)
     for h in range(Hq):
-        assert torch.equal(out[:, h], torch.full((3, 16), float(h // (Hq // Hkv) + 1), dtype=torch.float64))
+        want = torch.full((3, 16), float(h // (Hq // Hkv) + 1), dtype=torch.float64)
+        assert torch.equal(out[:, h], want)
+        assert torch.equal(torch.from_numpy(dense[:, h]), want)
 
 
 def test_non_causal_sees_every_key():
@@ -238,17 +245,20 @@ def test_empty_kv_gives_zero_and_minus_inf():
 
 # ------------------------------------------------------------ brute force
 
-@pytest.mark.parametrize("seed,causal", [(10, True), (11, True), (12, False)])
-def test_oracle_equals_dense_brute_force(seed, causal):
+@pytest.mark.parametrize("seed,causal,dtype", [(10, True, torch.bfloat16), (11, True, torch.bfloat16),
+                                               (12, False, torch.bfloat16), (13, True, torch.float16)])
+def test_oracle_equals_dense_brute_force(seed, causal, dtype):
     """Random varlen batch with cached context and GQA: the per-row paged
-    oracle equals the dense whole-matrix formulation."""
+    oracle equals the dense whole-matrix formulation, for bf16 and fp16
+    storage (the dense side widens with torch's own conversion)."""
     rng = np.random.default_rng(seed)
     B = 4
     q_lens = rng.integers(1, 9, B).tolist()
     ctx = rng.integers(0, 20, B).tolist()
     kv = [c + q for c, q in zip(ctx, q_lens)]
-    b = W.make_batch(q_lens, kv, Hq=6, Hkv=2, D=32, bs=16, seed=seed, causal=causal)
-    out, lse = run(b)
+    b = W.make_batch(q_lens, kv, Hq=6, Hkv=2, D=32, bs=16, seed=seed, causal=causal, q_dtype=dtype)
+    kc, vc = cache_of(b, dtype)
+    out, lse = run(b, kc, vc)
     # the cached rows of request r are its kv_len tokens in position order
     cuk = [0] + np.cumsum(kv).tolist()
     ref, ref_lse, _ = oracle.dense_masked_attention(
@@ -458,6 +468,42 @@ def test_e4m3_decode_known_values():
     assert [oracle.e4m3_to_double(int(c)) for c in codes] == tv.tolist()
 
 
+def _fp16_value_by_definition(c):
+    """IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits."""
+    e, m = (c >> 10) & 31, c & 1023
+    v = m * 2.0 ** -24 if e == 0 else (1 + m / 1024.0) * 2.0 ** (e - 15)
+    return -v if c & 0x8000 else v
+
+
+def test_fp16_storage_decodes_by_definition():
+    """fp16 queries and caches ("FlashAttention deep dive", flash_attn_varlen_func:
+    fp16 or bf16 inputs) are widened exactly.  A request with one visible key
+    returns V_0 exactly, so a value row holding every finite binary16 code
+    comes back as the codes' values; and with K_0 = 1 and scale 1 a query
+    holding one code c has lse = value(c) exactly."""
+    codes = np.array([c for c in range(1 << 16) if (c >> 10) & 31 != 31], dtype=np.uint16)
+    want = [_fp16_value_by_definition(int(c)) for c in codes]
+    assert want[:2] == [0.0, 2.0 ** -24] and 65504.0 in want and -1.0 in want
+    as_fp16 = torch.from_numpy(codes.view(np.float16).copy())
+    assert as_fp16.double().tolist() == want                  # torch's own widening agrees
+    n = len(codes)
+    one = torch.tensor([0], dtype=torch.int32)
+    # values: one request, one key, D = every code
+    q = torch.zeros((1, 1, n), dtype=torch.float16)
+    kc = torch.zeros((1, 1, 1, n), dtype=torch.float16)
+    vc = as_fp16.view(1, 1, 1, n)
+    out, lse = oracle.attention(q, kc, vc, torch.tensor([0, 1]), torch.tensor([1]), one.view(1, 1), 1.0)
+    assert out[0, 0].tolist() == want and float(lse[0, 0]) == 0.0
+    # queries: n one-token requests on the same cached key K_0 = 1.0
+    q = as_fp16.view(n, 1, 1)
+    kc = torch.ones((1, 1, 1, 1), dtype=torch.float16)
+    vc = torch.zeros_like(kc)
+    cu = torch.arange(n + 1, dtype=torch.int32)
+    out, lse = oracle.attention(q, kc, vc, cu, torch.ones(n, dtype=torch.int32),
+                                torch.zeros((n, 1), dtype=torch.int32), 1.0)
+    assert lse[:, 0].tolist() == want
+
+
 def test_e4m3_encode_matches_brute_force_and_torch():
     rng = np.random.default_rng(19)
     xs = list(rng.normal(scale=50.0, size=600)) + list(rng.normal(scale=0.01, size=300))
@@ -561,6 +607,35 @@ def test_window_zero_left_returns_the_diagonal_value():
                 assert torch.equal(out[t, h], v[j, 0].double())
                 s = b.softmax_scale * float((b.q[t, h].double() * k[j, 0].double()).sum())
                 assert abs(float(lse[t, h]) - s) < 1e-12
+            t += 1
+
+
+@pytest.mark.parametrize("window", [(0, 0), (2, 1), (-1, 3), (4, -1), (1, 40)])
+def test_window_without_causal_bounds_both_sides(window):
+    """Non-causal with a window (left, right): the query at absolute position
+    p = ctx + i sees keys max(0, p - left) .. min(kv_len - 1, p + right).
+    With q = 0 the scores tie: out = mean of those V rows, lse = ln(count);
+    window (0, 0) returns V_p exactly.  Paged oracle and dense formulation."""
+    left, right = window
+    b = W.make_batch([5, 3], [12, 3], Hq=2, Hkv=1, D=16, bs=16, seed=35, causal=False)
+    b.q.zero_()
+    out, lse = run(b, window=window)
+    dense, dense_lse, _ = _dense(b, window=window)
+    t = 0
+    for r, (ql, kl) in enumerate(zip(b.q_lens, b.kv_lens)):
+        _, v = key_rows(b, r)
+        for i in range(ql):
+            p = kl - ql + i
+            lo = 0 if left < 0 else max(0, p - left)
+            hi = kl - 1 if right < 0 else min(kl - 1, p + right)
+            want = v[lo:hi + 1, 0].double().mean(0)
+            for h in range(2):
+                if window == (0, 0):
+                    assert torch.equal(out[t, h], v[p, 0].double())
+                np.testing.assert_allclose(out[t, h].numpy(), want.numpy(), rtol=0, atol=1e-14)
+                np.testing.assert_allclose(dense[t, h], want.numpy(), rtol=0, atol=1e-14)
+                assert abs(float(lse[t, h]) - math.log(hi - lo + 1)) < 1e-13
+                assert abs(float(dense_lse[t, h]) - math.log(hi - lo + 1)) < 1e-13
             t += 1
 
 
