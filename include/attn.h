@@ -15,9 +15,13 @@
  *             second reduction kernel (sec. 12).
  *
  * Conventions shared by every entry point
- *  - All tensor pointers are DEVICE pointers owned by the caller; the
- *    library never allocates, frees or retains device memory.  Scratch space
- *    comes from the caller through (workspace, ws_bytes).
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  No call
+ *    allocates or frees device memory, and none keeps a caller's pointer
+ *    after it returns.  Scratch space comes from the caller through
+ *    (workspace, ws_bytes).  The library itself holds three fixed device
+ *    arrays, loaded with it on every GPU that uses it: the error word
+ *    (4 bytes), the tensor-core kernel's 64 ticket slots (1 KB) and the
+ *    8 MiB scratch of attn_paged_decode_noalloc.
  *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
  *    does no host synchronisation, so a call can be captured in a CUDA graph
  *    when its pointers and host scalars stay fixed.
