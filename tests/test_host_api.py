@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import varlen_flashattention_causal_gb300 as va
 from varlen_flashattention_causal_gb300 import build as vb
@@ -47,7 +48,11 @@ def test_status_strings(lib):
     assert va.attn_status_string(ERR_HD).startswith("head size")
 
 
-FAKE = ctypes.c_void_p(4096)    # 16-byte aligned, never dereferenced on the validation path
+# A 16-byte-aligned placeholder address.  Every call below that gets it stops
+# before any launch on any machine: at a host validation error, at an empty
+# batch (B = 0 or T = 0 returns ATTN_OK before the device is looked up), or
+# at the workspace check, which also precedes every launch.
+FAKE = ctypes.c_void_p(4096)
 
 
 def prefill(lib, **kw):
@@ -194,13 +199,85 @@ def prefill_ext(lib, wl=-1, wr=-1, cap=0.0, sinks=None, **kw):
 @pytest.mark.parametrize("wl,wr,cap,status", [
     (-2, -1, 0.0, ERR_SHAPE), (-1, -3, 0.0, ERR_SHAPE), (-1, -1, -1.0, ERR_SHAPE),
     (-1, -1, float("nan"), ERR_SHAPE), (-1, -1, float("inf"), ERR_SHAPE),
-    (0, 0, 0.0, None), (16, -1, 30.0, None)])
+    (0, 0, 0.0, OK), (16, -1, 30.0, OK)])
 def test_variant_validation(lib, wl, wr, cap, status):
     """attn_varlen_prefill_ext: window bounds below -1 and negative, NaN or
-    infinite soft caps are refused before any launch; valid ones get past
-    validation (here they then fail for want of a device)."""
-    st = prefill_ext(lib, wl=wl, wr=wr, cap=cap)
-    if status is None:
-        assert st in (ERR_CUDA, ERR_DEV, OK)
-    else:
-        assert st == status
+    infinite soft caps are refused before any launch.  Valid ones pass
+    validation: with an empty batch the call then returns ATTN_OK at once,
+    before it looks for a device, so no placeholder pointer can reach a
+    launch on any machine."""
+    kw = {} if status != OK else dict(B=0, T=0)
+    assert prefill_ext(lib, wl=wl, wr=wr, cap=cap, **kw) == status
+
+
+# ------------------------------------------------ the Python binding's marshalling
+
+def test_binding_has_the_c_names():
+    """Every function include/attn.h declares has a Python function of the
+    same name in the binding, and every name the binding exports exists."""
+    for n in declared_functions():
+        assert callable(getattr(va, n, None)), n
+    for n in va.__all__:
+        assert hasattr(va, n), n
+
+
+def _cpu(*shape, dtype=torch.bfloat16):
+    return torch.zeros(shape, dtype=dtype)
+
+
+def _status_of(call):
+    with pytest.raises(va.AttnError) as e:
+        call()
+    return e.value.status
+
+
+def test_bindings_pass_arguments_in_the_declared_order(lib):
+    """Each Python wrapper hands its C entry point the declared number, types
+    and order of arguments.  Each call below uses small CPU tensors with one
+    argument chosen to fail one host check (head size, block size, dtype,
+    window, soft cap, scale), and must raise AttnError with exactly that
+    status.  Host validation precedes every device access, so these
+    pointers are never dereferenced and nothing is launched on any machine."""
+    cu = torch.tensor([0, 3], dtype=torch.int32)
+    su = torch.tensor([3], dtype=torch.int32)
+    bt = torch.zeros((1, 4), dtype=torch.int32)
+
+    def prefill(fn=va.attn_varlen_prefill, D=128, bs=16, qdt=torch.bfloat16, kdt=torch.bfloat16, **kw):
+        q, kc, out = _cpu(3, 8, D, dtype=qdt), _cpu(4, bs, 2, D, dtype=kdt), _cpu(3, 8, D)
+        return lambda: fn(q, kc, kc, out, cu, su, bt, 3, 3, 0.1, num_splits=1, stream=0, **kw)
+
+    assert _status_of(prefill(D=96)) == ERR_HD
+    assert _status_of(prefill(bs=24)) == ERR_BS
+    assert _status_of(prefill(kdt=torch.float16)) == ERR_DTYPE
+    assert _status_of(prefill(qdt=torch.float8_e4m3fn)) == ERR_DTYPE
+    assert _status_of(prefill(window=(-2, -1))) == ERR_SHAPE
+    assert _status_of(prefill(window=(-1, -5))) == ERR_SHAPE
+    assert _status_of(prefill(softcap=-1.0)) == ERR_SHAPE
+    assert _status_of(prefill(fn=va.attn_varlen_prefill_ext, D=64, bs=8)) == ERR_BS
+
+    sl = torch.tensor([5, 7], dtype=torch.int32)
+    bt2 = torch.zeros((2, 4), dtype=torch.int32)
+    for fn, extra in ((va.attn_paged_decode, {}), (va.attn_paged_decode_noalloc, {})):
+        def decode(D=128, bs=16, kdt=torch.bfloat16):
+            q, kc, out = _cpu(2, 8, D), _cpu(4, bs, 2, D, dtype=kdt), _cpu(2, 8, D)
+            return lambda: fn(q, kc, kc, out, sl, bt2, 7, 0.1, num_splits=1, stream=0, **extra)
+        assert _status_of(decode(D=96)) == ERR_HD
+        assert _status_of(decode(bs=48 + 8)) == ERR_BS
+        assert _status_of(decode(kdt=torch.float16)) == ERR_DTYPE
+
+    def merge(D=128, dt=torch.bfloat16):
+        o, l = _cpu(4, 8, D, dtype=dt), _cpu(4, 8, dtype=torch.float32)
+        return lambda: va.attn_merge_states(o, None, o, l, o, l, stream=0)
+    assert _status_of(merge(D=72)) == ERR_HD
+    assert _status_of(merge(dt=torch.float8_e4m3fn)) == ERR_DTYPE
+
+    slots = torch.zeros(3, dtype=torch.int64)
+
+    def write(D=128, bs=16, src=torch.bfloat16, kdt=torch.bfloat16, **kw):
+        k, kc = _cpu(3, 2, D, dtype=src), _cpu(4, bs, 2, D, dtype=kdt)
+        return lambda: va.kv_cache_write(k, k, kc, kc, slots, stream=0, **kw)
+    assert _status_of(write(D=96)) == ERR_HD
+    assert _status_of(write(bs=40)) == ERR_BS
+    assert _status_of(write(src=torch.float16)) == ERR_DTYPE
+    assert _status_of(write(kdt=torch.float8_e4m3fn, k_scale=0.0)) == ERR_SHAPE
+    assert _status_of(write(kdt=torch.float8_e4m3fn, v_scale=-1.0)) == ERR_SHAPE

@@ -18,9 +18,10 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "AttnError", "attn_varlen_prefill", "attn_paged_decode", "attn_merge_states",
-    "kv_cache_write", "attn_workspace_size", "attn_num_splits", "attn_tile_kind",
-    "attn_status_string", "attn_device_error_flag", "library_path",
+    "AttnError", "attn_varlen_prefill", "attn_varlen_prefill_ext", "attn_paged_decode",
+    "attn_paged_decode_noalloc", "attn_merge_states", "kv_cache_write", "attn_workspace_size",
+    "attn_num_splits", "attn_tile_kind", "attn_status_string", "attn_device_error_flag",
+    "library_path",
 ]
 
 ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3, ATTN_FP32 = 0, 1, 2, 3
@@ -63,6 +64,11 @@ def _load():
         vp, vp, vp, vp, vp, vp, vp, i64,
         i32, i32, i32, i32, i32, i32, i32, i32, i32,
         f32, f32, f32, i32, vp, sz, vp]
+    lib.attn_paged_decode_noalloc.restype = i32
+    lib.attn_paged_decode_noalloc.argtypes = [
+        vp, vp, vp, vp, vp, vp, vp, i64,
+        i32, i32, i32, i32, i32, i32, i32, i32, i32,
+        f32, f32, f32, i32, vp]
     lib.attn_merge_states.restype = i32
     lib.attn_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.kv_cache_write.restype = i32
@@ -171,6 +177,12 @@ def attn_varlen_prefill(q, k_cache, v_cache, out, cu_seqlens_q, seqused_k, block
     return out
 
 
+# The C ABI has a separate entry point for the variants and e4m3 queries;
+# attn_varlen_prefill above already calls it and takes its arguments
+# (window, softcap, sinks, q_descale), so the Python name is the same call.
+attn_varlen_prefill_ext = attn_varlen_prefill
+
+
 def attn_paged_decode(q, k_cache, v_cache, out, seq_lens, block_table, max_seq_len,
                       softmax_scale, lse_out=None, k_descale=1.0, v_descale=1.0,
                       num_splits=0, workspace=None, stream=None):
@@ -256,19 +268,12 @@ def attn_paged_decode_noalloc(q, k_cache, v_cache, out, seq_lens, block_table, m
     num_splits too large for the array raises AttnError (ATTN_ERR_WORKSPACE).
     """
     lib = _load()
-    fn = lib.attn_paged_decode_noalloc
-    if fn.argtypes is None:
-        c = ctypes
-        fn.restype = c.c_int
-        fn.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,
-                       c.c_int64, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
-                       c.c_int, c.c_float, c.c_float, c.c_float, c.c_int, c.c_void_p]
     B, Hq, D = q.shape
     nb, bs, Hkv, _ = k_cache.shape
     _i32(seq_lens, "seq_lens")
     if block_table.dtype != torch.int32 or block_table.stride(-1) != 1:
         raise TypeError("block_table must be int32 with unit column stride")
-    st = fn(_p(q), _p(k_cache), _p(v_cache), _p(out), _p(lse_out), _p(seq_lens), _p(block_table),
+    st = lib.attn_paged_decode_noalloc(_p(q), _p(k_cache), _p(v_cache), _p(out), _p(lse_out), _p(seq_lens), _p(block_table),
             block_table.stride(0), B, int(max_seq_len), Hq, Hkv, D, bs, nb, _dt(q), _dt(k_cache),
             float(softmax_scale), float(k_descale), float(v_descale), int(num_splits), _stream(stream))
     _check("attn_paged_decode_noalloc", st)

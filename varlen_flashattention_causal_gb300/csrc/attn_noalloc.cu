@@ -48,16 +48,24 @@ extern "C" attn_status attn_paged_decode_noalloc(
     int B, int max_seq_len, int Hq, int Hkv, int D, int block_size, int num_blocks,
     attn_dtype q_dtype, attn_dtype kv_dtype, float softmax_scale, float k_descale, float v_descale,
     int num_splits, attn_stream_t stream) {
-    // an explicit split count whose partial results do not fit is refused;
-    // the automatic choice (num_splits = 0) is capped to what fits
-    if (num_splits > 1 && attn_workspace_size(B, Hq, D, num_splits) > (size_t)ATTN_NOALLOC_SCRATCH_BYTES)
-        return ATTN_ERR_WORKSPACE;
+    // host validation comes first, as in every entry point: with an empty
+    // batch the regular entry point runs the same argument checks and
+    // returns before it looks up the device
+    const attn_status valid =
+        attn_paged_decode(q, k_cache, v_cache, out, lse_out, seq_lens, block_table, bt_row_stride, 0, max_seq_len,
+                          Hq, Hkv, D, block_size, num_blocks, q_dtype, kv_dtype, softmax_scale, k_descale,
+                          v_descale, num_splits, nullptr, 0, stream);
+    if (valid != ATTN_OK) return valid;
     if (B <= 0) {
-        // nothing to compute: let the regular entry point validate and return
+        // nothing to compute (a negative B is refused there)
         return attn_paged_decode(q, k_cache, v_cache, out, lse_out, seq_lens, block_table, bt_row_stride, B,
                                  max_seq_len, Hq, Hkv, D, block_size, num_blocks, q_dtype, kv_dtype,
                                  softmax_scale, k_descale, v_descale, num_splits, nullptr, 0, stream);
     }
+    // an explicit split count whose partial results do not fit is refused;
+    // the automatic choice (num_splits = 0) is capped to what fits
+    if (num_splits > 1 && attn_workspace_size(B, Hq, D, num_splits) > (size_t)ATTN_NOALLOC_SCRATCH_BYTES)
+        return ATTN_ERR_WORKSPACE;
     void *scratch = nullptr;
     const attn_status st = scratch_for_current_device(&scratch);
     if (st != ATTN_OK) return st;
