@@ -120,6 +120,70 @@ def test_multi_token_verify_equals_six_decodes():
         assert abs(float(lse0[i, 0]) - math.log(nvis[i])) < 1e-12
 
 
+def test_decode_rows_see_every_key():
+    """multi-request page, sec. 9: decode requests with contexts of 20,000 and
+    35,000 tokens have attention rows of 20,001 and 35,001 keys, all visible.
+    With q = 0 every score ties, so lse = ln(row length) and out is the mean
+    of all V rows; and the causal result equals the non-causal one exactly."""
+    g = read_golden("decode_20000_35000.txt")
+    ctx = [int(r[1]) for r in g]
+    row = [int(r[2]) for r in g]
+    assert row == [c + 1 for c in ctx]
+    b = W.make_batch([1, 1], row, Hq=2, Hkv=1, D=16, bs=64, seed=40)
+    kc, vc = cache_of(b)
+    out, lse = run(b, kc, vc)
+    b_nc = W.make_batch([1, 1], row, Hq=2, Hkv=1, D=16, bs=64, seed=40, causal=False)
+    out_nc, lse_nc = run(b_nc, kc, vc)
+    assert torch.equal(out, out_nc) and torch.equal(lse, lse_nc)
+    b.q.zero_()
+    out0, lse0 = run(b, kc, vc)
+    for r, n in enumerate(row):
+        _, v = key_rows(b, r)
+        assert v.shape[0] == n
+        for h in range(2):
+            assert abs(float(lse0[r, h]) - math.log(n)) < 1e-12
+            np.testing.assert_allclose(out0[r, h].numpy(), v[:, 0].double().mean(0).numpy(), rtol=0, atol=1e-14)
+
+
+def test_split_into_the_pages_segments():
+    """multi-request page, sec. 12: a 12,288-key decode row cut into the
+    page's three 4096-key segments.  Each segment's local max m_s, exponent
+    sum l_s and weighted output O_s are computed by brute force from the key
+    rows, then reduced by the page's formulas m = max m_s,
+    l = sum e^{m_s - m} l_s, O = sum e^{m_s - m} O_s / l.  That equals the
+    oracle's unsplit result, and so does the oracle's pairwise log-sum-exp
+    merge of its own per-segment results."""
+    segs = [(int(a), int(c)) for _, a, c in read_golden("split_segments_4096.txt")]
+    n = segs[-1][1] + 1
+    b = W.make_batch([1], [n], Hq=2, Hkv=1, D=16, bs=64, seed=41)
+    kc, vc = cache_of(b)
+    full, full_lse = run(b, kc, vc)
+    k, v = key_rows(b, 0)
+    for h in range(2):
+        q = b.q[0, h].double().numpy()
+        parts = []
+        for lo, hi in segs:
+            s = b.softmax_scale * (k[lo:hi + 1, 0].double().numpy() @ q)
+            m_s = s.max()
+            e = np.exp(s - m_s)
+            parts.append((m_s, e.sum(), e @ v[lo:hi + 1, 0].double().numpy()))
+        m = max(p[0] for p in parts)
+        l = sum(math.exp(m_s - m) * l_s for m_s, l_s, _ in parts)
+        o = sum(math.exp(m_s - m) * o_s for m_s, _, o_s in parts) / l
+        np.testing.assert_allclose(o, full[0, h].numpy(), rtol=0, atol=1e-13)
+        assert abs(m + math.log(l) - float(full_lse[0, h])) < 1e-11
+    # the oracle's own segments (keys lo..hi through the block table), merged
+    state = None
+    for lo, hi in segs:
+        bt = b.block_table[:, lo // b.bs:].contiguous()
+        o_s, l_s = oracle.attention(b.q, kc, vc, b.cu_seqlens_q, torch.tensor([hi - lo + 1], dtype=torch.int32),
+                                    bt, b.softmax_scale, causal=False)
+        o_s, l_s = o_s.view(-1, 16), l_s.view(-1)
+        state = (o_s, l_s) if state is None else oracle.merge_states(state[0], state[1], o_s, l_s)
+    np.testing.assert_allclose(state[0].numpy(), full.view(-1, 16).numpy(), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(state[1].numpy(), full_lse.view(-1).numpy(), rtol=0, atol=1e-11)
+
+
 def test_paged_lookup_example():
     """multi-request page, sec. 11: position 1024 -> physical block 37 for
     request A and 912 for request B; the KV write puts the token there and
