@@ -34,6 +34,9 @@ sys.path.insert(0, ROOT)
 from varlen_flashattention_causal_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged-decode KV GB/s + varlen-prefill TFLOP/s, % of 1×GB300 roofline"
+# the workload both arms of the default line measure (they are paired by it)
+DECODE_WORKLOAD = ("paged decode, Llama-3-8B shaped: B=64, Hq=32, Hkv=8, D=128, bf16, "
+                   "ctx U[512,4096], block_size 16, 40960-block pool")
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -327,8 +330,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "paged decode, Llama-3-8B shaped: B=64, Hq=32, Hkv=8, D=128, bf16, "
-                               "ctx U[512,4096], block_size 16, 40960-block pool",
+        "config": {"workload": DECODE_WORKLOAD,
                    "step": "kv_cache_write of 64 new tokens + attn_paged_decode (split-KV + combine)",
                    "num_splits": ns, "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2: %.0f MB of K/V read per step vs %d MB L2"
@@ -451,8 +453,7 @@ def run_reference(args, budget_s=150.0):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
-           "config": {"workload": "paged decode, Llama-3-8B shaped: B=64, Hq=32, Hkv=8, D=128, bf16, "
-                                  "ctx U[512,4096], block_size 16, 40960-block pool"},
+           "config": {"workload": DECODE_WORKLOAD},
            "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
                             "sample": sample},
            "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -109,3 +109,30 @@ def test_two_ranks_report_the_slowest_and_only_rank0_works():
     assert [o[:4] for o in out] == [(0, 2, 0, 0), (1, 2, 1, 1)]
     assert all(o[4] == 2.5 for o in out)
     assert out[1][5] is None and out[1][6] < 5.0
+
+
+def test_reference_arm_prints_one_contract_line(capsys, monkeypatch):
+    """bench.py --impl reference on one process: exactly one JSON line with
+    the benchmark contract's keys, the device arm's metric, unit and
+    workload, a cpu_baseline describing this run, and an e2e object with no
+    host<->device bytes (the oracle runs on the host)."""
+    import json
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+
+    class Args:
+        steps, warmup = 1, 3
+    bench.run_reference(Args(), budget_s=2.0)
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert {"impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+            "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+            "cpu_baseline", "e2e"} <= set(d)
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert (d["n_gpus"], d["steps"], d["warmup"], d["higher_is_better"]) == (1, 1, 3, True)
+    assert d["config"]["workload"] == bench.DECODE_WORKLOAD
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
