@@ -79,6 +79,9 @@ MUTANTS = [
     ("merge_lse_without_max", C, [("const double l = mx + log(exp(a - mx) + exp(b - mx));",
                                    "const double l = log(exp(a - mx) + exp(b - mx));")],
      "the max dropped from the merged log-sum-exp"),
+    ("merge_weights_unnormalised", C, [("const double w1 = exp(a - l), w2 = exp(b - l);",
+                                        "const double w1 = exp(a - mx), w2 = exp(b - mx);")],
+     "the merge weights taken relative to the max, not to the merged lse"),
     ("merge_empty_states_unhandled", C, [("if (a == -INFINITY && b == -INFINITY) {", "if (0) {")],
      "two empty states merged by the general formula"),
     # --- e4m3 decoding and encoding
@@ -91,6 +94,8 @@ MUTANTS = [
     ("e4m3_saturates_to_nan", C, [("if (a >= 448.0)\n        return (uint8_t)(sign | 0x7E);",
                                    "if (a >= 448.0)\n        return (uint8_t)(sign | 0x7F);")],
      "out-of-range values mapped to NaN instead of +-448"),
+    ("e4m3_subnormal_ties_away", C, [("double m = nearbyint(a * 512.0);", "double m = round(a * 512.0);")],
+     "ties in the subnormal range rounded away from zero"),
     ("e4m3_sign_lost", C, [("uint8_t sign = signbit(x) ? 0x80 : 0x00;", "uint8_t sign = 0x00;")],
      "negative values encoded as positive"),
     ("fp16_exponent_bias", C, [("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);")],
@@ -98,6 +103,8 @@ MUTANTS = [
     # --- the slot_mapping write
     ("kv_write_scale_multiplies", C, [("oracle_e4m3_from_float(kx / k_scale)", "oracle_e4m3_from_float(kx * k_scale)")],
      "the cache stores x * scale instead of x / scale"),
+    ("kv_write_values_use_key_scale", C, [("oracle_e4m3_from_float(vx / v_scale)", "oracle_e4m3_from_float(vx / k_scale)")],
+     "the e4m3 V cache quantised with the key scale"),
     ("kv_write_v_gets_keys", C, [("memcpy((char *)v_cache + dst * cb, (const char *)value + src * sb",
                                   "memcpy((char *)v_cache + dst * cb, (const char *)key + src * sb")],
      "the V cache written with keys"),

@@ -588,16 +588,20 @@ def test_e4m3_encode_matches_brute_force_and_torch():
 def test_fp8_kv_write_quantizes_x_over_scale():
     """FlashAttention deep dive, KV cache update: reshape_and_cache_flash
     with k_scale / v_scale.  Reading adopted: store e4m3(x / scale) with the
-    division in fp32."""
+    division in fp32.  Keys use k_scale and values v_scale (the batch's two
+    per-tensor scales differ)."""
     b = W.make_batch([2], [20], Hq=2, Hkv=2, D=16, bs=16, seed=20, kv_dtype="fp8")
+    assert b.k_scale != b.v_scale
     kc, vc = cache_of(b)
-    kb = kc.view(torch.uint8)
-    for t in (0, 7, 19):
+    kb, vb = kc.view(torch.uint8), vc.view(torch.uint8)
+    for t in range(20):
         slot = int(b.slot_mapping[t])
         for h in range(2):
-            for d in (0, 5, 15):
+            for d in range(16):
                 x = np.float32(b.k_tok[t, h, d].float().item()) / np.float32(b.k_scale)
                 assert int(kb[slot // 16, slot % 16, h, d]) == _e4m3_brute(float(x))
+                y = np.float32(b.v_tok[t, h, d].float().item()) / np.float32(b.v_scale)
+                assert int(vb[slot // 16, slot % 16, h, d]) == _e4m3_brute(float(y))
     # dequantised attention with an fp8 cache is the bf16 formula applied to
     # the widened values times the scale
     out, _ = run(b, kc, vc)
