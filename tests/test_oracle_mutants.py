@@ -28,6 +28,8 @@ MUTANTS = [
     # --- attention: the causal mask and its alignment
     ("causal_excludes_diagonal", C, [("                last = ctx + i;\n", "                last = ctx + i - 1;\n")],
      "the query does not see its own key"),
+    ("causal_flag_ignored", C, [("if (causal && ctx + i < last)", "if (ctx + i < last)")],
+     "non-causal calls (the cascade prefix) masked as causal"),
     ("top_left_alignment", C, [("const int64_t ctx = kv_len - q_len;", "const int64_t ctx = 0;")],
      "the causal mask aligned top-left instead of bottom-right"),
     ("request_bounds_inclusive", C, [("t < cu_seqlens_q[r + 1]))", "t <= cu_seqlens_q[r + 1]))")],
@@ -57,11 +59,16 @@ MUTANTS = [
     # --- attention: variants
     ("window_left_off_by_one", C, [("first = ctx + i - window_left;", "first = ctx + i - window_left + 1;")],
      "the sliding window one key short on the left"),
+    ("window_right_off_by_one", C, [("last = ctx + i + window_right;", "last = ctx + i + window_right - 1;")],
+     "the sliding window one key short on the right"),
     ("window_right_ignored", C, [("if (window_right >= 0 && ctx + i + window_right < last)",
                                   "if (0 && ctx + i + window_right < last)")],
      "the right window bound ignored"),
     ("softcap_unscaled", C, [("softcap * tanh(s[j] / softcap)", "softcap * tanh(s[j])")],
      "the soft cap applied to s instead of s / c"),
+    ("softcap_before_scale", C, [("s[j] = softmax_scale * dot;\n                if (softcap > 0.0)\n                    s[j] = softcap * tanh(s[j] / softcap);",
+                                  "s[j] = dot;\n                if (softcap > 0.0)\n                    s[j] = softcap * tanh(s[j] / softcap);\n                s[j] *= softmax_scale;")],
+     "the soft cap applied to q . k before the scale"),
     ("sink_dropped", C, [("double L = z == -INFINITY ? 0.0 : exp(z - M);", "double L = 0.0;")],
      "the sink logit left out of the normalisation"),
     ("q_scale_dropped", C, [("qv[d] = load_elem(q, q_off + d, q_dtype) * q_scale;",
@@ -105,6 +112,8 @@ MUTANTS = [
      "the cache stores x * scale instead of x / scale"),
     ("kv_write_values_use_key_scale", C, [("oracle_e4m3_from_float(vx / v_scale)", "oracle_e4m3_from_float(vx / k_scale)")],
      "the e4m3 V cache quantised with the key scale"),
+    ("kv_write_skips_slot_zero", C, [("        if (slot < 0)\n            continue;", "        if (slot <= 0)\n            continue;")],
+     "slot 0 treated as padding"),
     ("kv_write_v_gets_keys", C, [("memcpy((char *)v_cache + dst * cb, (const char *)value + src * sb",
                                   "memcpy((char *)v_cache + dst * cb, (const char *)key + src * sb")],
      "the V cache written with keys"),

@@ -728,6 +728,22 @@ def test_huge_softcap_is_no_cap():
     assert float((lse0 - lse1).abs().max()) < 1e-9
 
 
+@pytest.mark.parametrize("cap", [0.5, 3.0, 30.0])
+def test_softcap_of_a_single_key_is_the_capped_logit(cap):
+    """FlashAttention deep dive, argument table (softcap), as read: the cap
+    maps the scaled logit s = scale * q . K to c * tanh(s / c).  Row 0 of a
+    request without context sees only key 0, so its lse is exactly that
+    capped logit and its output is V_0."""
+    b = W.make_batch([3], [3], Hq=2, Hkv=1, D=32, bs=16, seed=42)
+    b.q = (b.q.float() * 4).to(torch.bfloat16)          # raw logits of a few units
+    out, lse = run(b, softcap=cap)
+    k, v = key_rows(b, 0)
+    for h in range(2):
+        s = b.softmax_scale * float((b.q[0, h].double() * k[0, 0].double()).sum())
+        assert abs(float(lse[0, h]) - cap * math.tanh(s / cap)) < 1e-12
+        assert torch.equal(out[0, h], v[0, 0].double())
+
+
 def test_softcap_bounds_every_logit():
     """With cap c every logit lies in (-c, c), so lse <= c + log(#keys)
     however large the raw scores are."""
