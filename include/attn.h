@@ -306,6 +306,18 @@ const char *attn_status_string(attn_status s);
  */
 int attn_device_error_flag(int reset);
 
+/*
+ * attn_selftest_wait_timeout -- failure-detection self-test of the bounded
+ * waits (not an operation of the pages).  Launches one thread that waits,
+ * through the same bounded wait as the tensor-core kernel's pipeline, on an
+ * mbarrier phase that nothing completes.  After the wait limit (2 s) it
+ * gives up and raises bit 2 (timeout) of the device error word, which
+ * attn_device_error_flag() then reports; the context stays usable.
+ * Asynchronous on `stream`.  ATTN_ERR_CUDA or ATTN_ERR_DEVICE as the other
+ * entry points.
+ */
+attn_status attn_selftest_wait_timeout(attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

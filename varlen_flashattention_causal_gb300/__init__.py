@@ -21,7 +21,7 @@ __all__ = [
     "AttnError", "attn_varlen_prefill", "attn_varlen_prefill_ext", "attn_paged_decode",
     "attn_paged_decode_noalloc", "attn_merge_states", "kv_cache_write", "attn_workspace_size",
     "attn_num_splits", "attn_tile_kind", "attn_status_string", "attn_device_error_flag",
-    "library_path",
+    "attn_selftest_wait_timeout", "library_path",
 ]
 
 ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3, ATTN_FP32 = 0, 1, 2, 3
@@ -83,6 +83,8 @@ def _load():
     lib.attn_status_string.argtypes = [i32]
     lib.attn_device_error_flag.restype = i32
     lib.attn_device_error_flag.argtypes = [i32]
+    lib.attn_selftest_wait_timeout.restype = i32
+    lib.attn_selftest_wait_timeout.argtypes = [vp]
     _lib = lib
     return lib
 
@@ -249,6 +251,13 @@ def attn_device_error_flag(reset=False):
     if v < 0:
         raise RuntimeError("attn_device_error_flag: CUDA call failed")
     return v
+
+
+def attn_selftest_wait_timeout(stream=None):
+    """Launch the bounded-wait self-test: a wait on a phase nothing completes
+    gives up after its limit (2 s) and raises ERR_TIMEOUT in the device error
+    word (read it with attn_device_error_flag)."""
+    _check("attn_selftest_wait_timeout", _load().attn_selftest_wait_timeout(_stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20   # ATTN_NOALLOC_SCRATCH_BYTES in include/attn.h

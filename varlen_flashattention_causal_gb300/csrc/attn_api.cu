@@ -7,9 +7,12 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
 #include "../../include/attn.h"
 #include "internal.h"
+#include "sm100.cuh"
 
 using namespace attn;
 
@@ -22,33 +25,60 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 256;
 constexpr int kTileN = 64;          // keys per K/V tile of the mma kernel
 
+// Filled on a device's first call.  Calls may come from several host
+// threads: the fields are written once, under g_dev_fill, before `ready` is
+// published with release order; readers that see `ready` (acquire) see them.
 struct DevInfo {
-    int ready = 0;
+    std::atomic<int> ready{0};
     int sms = 0;
     int major = 0, minor = 0;
     unsigned *err = nullptr;
 };
 DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_fill;
 
 attn_status device_info(DevInfo **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
     DevInfo &d = g_dev[dev];
-    if (!d.ready) {
-        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ATTN_ERR_CUDA;
-        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
-            return ATTN_ERR_CUDA;
-        if (cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-            return ATTN_ERR_CUDA;
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_attn_error_word) != cudaSuccess) return ATTN_ERR_CUDA;
-        d.err = static_cast<unsigned *>(p);
-        d.ready = 1;
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_dev_fill);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            int sms = 0, major = 0, minor = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_attn_error_word) != cudaSuccess || !p) return ATTN_ERR_CUDA;
+            d.sms = sms;
+            d.major = major;
+            d.minor = minor;
+            d.err = static_cast<unsigned *>(p);
+            d.ready.store(1, std::memory_order_release);
+        }
     }
     if (d.major != 10 || d.minor != 3) return ATTN_ERR_DEVICE;
     *out = &d;
     return ATTN_OK;
+}
+
+// Failure-detection self-test: one thread waits, through the bounded wait
+// of the tensor-core kernel's pipeline, on phase 0 of an mbarrier that
+// expects one arrival and never gets it.  After the wait limit it gives up
+// and raises the timeout bit of the error word.
+__global__ void wait_timeout_selftest_kernel(unsigned *err) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+    sm100::mbar_init(b, 1);
+    sm100::fence_mbar_init();
+    abort_flag = 0;
+    if (!sm100::mbar_wait(b, 0, &abort_flag)) atomicOr(err, ERR_TIMEOUT);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -343,6 +373,14 @@ const char *attn_status_string(attn_status s) {
     case ATTN_ERR_DEVICE: return "current device is not sm_103";
     }
     return "unknown status";
+}
+
+attn_status attn_selftest_wait_timeout(attn_stream_t stream) {
+    DevInfo *dev = nullptr;
+    const attn_status st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dev->err);
+    return check_cuda(cudaGetLastError());
 }
 
 int attn_device_error_flag(int reset) {

@@ -18,6 +18,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/attn.h"
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
@@ -26,17 +28,19 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-void *g_scratch_addr[kMaxDevices];   // device address of the array, per device
+// device address of the array, per device; host threads racing on a
+// device's first call store the same value, through an atomic
+std::atomic<void *> g_scratch_addr[kMaxDevices];
 
 attn_status scratch_for_current_device(void **addr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress((void **)&p, g_noalloc_scratch) != cudaSuccess || !p) return ATTN_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+    void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return ATTN_ERR_CUDA;
+        g_scratch_addr[dev].store(p, std::memory_order_release);
     }
-    *addr = g_scratch_addr[dev];
+    *addr = p;
     return ATTN_OK;
 }
 

@@ -981,19 +981,25 @@ cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int kv_dtype, int64_t
     tp.f = f;
     tp.kv_rows = gcd_int(f.bs, kBN);
     {
-        static unsigned long long *slots[kMaxSchedDevices] = {};
+        // device address of the ticket slots, looked up on a device's first
+        // launch; host threads racing on that first launch store the same
+        // value, through an atomic
+        static std::atomic<unsigned long long *> slots[kMaxSchedDevices];
         static std::atomic<unsigned> next[kMaxSchedDevices];
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < 0 || dev >= kMaxSchedDevices) return cudaErrorInvalidDevice;
-        if (!slots[dev]) {
+        unsigned long long *base = slots[dev].load(std::memory_order_acquire);
+        if (!base) {
             void *a = nullptr;
             e = cudaGetSymbolAddress(&a, g_tc_sched);
             if (e != cudaSuccess) return e;
-            slots[dev] = static_cast<unsigned long long *>(a);
+            if (!a) return cudaErrorInvalidSymbol;
+            base = static_cast<unsigned long long *>(a);
+            slots[dev].store(base, std::memory_order_release);
         }
-        tp.sched = slots[dev] + 2 * (next[dev].fetch_add(1u) % kSchedSlots);
+        tp.sched = base + 2 * (next[dev].fetch_add(1u) % kSchedSlots);
     }
     const bool q16 = q_dtype == DT_FP16;
     const bool q8 = q_dtype == DT_E4M3;
