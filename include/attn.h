@@ -18,19 +18,17 @@
  *  - All tensor pointers are DEVICE pointers owned by the caller.  No call
  *    allocates or frees device memory, and none keeps a caller's pointer
  *    after it returns.  Scratch space comes from the caller through
- *    (workspace, ws_bytes).  The library itself holds three fixed device
+ *    (workspace, ws_bytes).  The library itself holds two fixed device
  *    arrays, loaded with it on every GPU that uses it: the error word
- *    (4 bytes), the tensor-core kernel's 64 ticket slots (1 KB) and the
- *    8 MiB scratch of attn_paged_decode_noalloc.
+ *    (4 bytes) and the 8 MiB scratch of attn_paged_decode_noalloc.
  *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
  *    does no host synchronisation, so a call can be captured in a CUDA graph
  *    when its pointers and host scalars stay fixed.
- *  - The tensor-core kernel schedules its work with a ticket counter taken
- *    from a pool of 64 per device, one per call in turn.  So at most 64
- *    attention calls may run on one device at the same moment (different
- *    streams or host threads).  A captured graph keeps its counter: do not
- *    replay one graph on two streams at once.  The same holds for its
- *    workspace anyway.
+ *  - A call's workspace is its own while the call runs: calls that may run
+ *    at the same time (other streams, other host threads, graph replays)
+ *    need separate workspaces.  Nothing else is shared between calls: the
+ *    tensor-core kernel's work counter lives in the call's workspace and is
+ *    zeroed by the call itself.
  *  - Arguments are validated on the host before anything is launched.  On a
  *    non-zero status nothing was launched and no memory was touched.
  *  - Block ids and slots are also checked inside the kernels: an id outside
@@ -122,11 +120,17 @@ typedef enum {
  *   ([MR] sec. 12): 0 = choose automatically, 1 = no split.  Partial
  *   results go to the workspace and a second kernel merges them.
  * lse_out may be NULL.
- * workspace: device scratch of at least
+ * workspace: device scratch (16-byte aligned) of at least
  *   attn_workspace_size(total_q, Hq, D, splits) bytes for the split count the
  *   call ends up using; with num_splits = 0 the automatic choice is capped
- *   to what fits in ws_bytes (ws_bytes = 0 and workspace = NULL disable
- *   splitting).
+ *   to what fits in ws_bytes.  Its first 256 bytes hold the work counter of
+ *   the tensor-core kernel, which takes requests of more than 64 packed rows
+ *   (q_len * Hq / Hkv, head size 128): a call with
+ *   max_seqlen_q * Hq / Hkv > 64 (and head size 128) needs those 256 bytes
+ *   even with num_splits = 1, and returns ATTN_ERR_WORKSPACE without them.
+ *   Other calls may pass workspace = NULL and ws_bytes = 0, which disables
+ *   splitting.  The contents need no initial value and are scratch after
+ *   the call.
  */
 attn_status attn_varlen_prefill(
     const void *q, int64_t q_stride_tok,
@@ -210,9 +214,10 @@ attn_status attn_paged_decode(
  *
  * Arguments and results are those of attn_paged_decode without the
  * workspace.  num_splits = 0 picks the split count automatically and caps it
- * to what fits in the array; an explicit num_splits > 1 whose partials need
- * more than ATTN_NOALLOC_SCRATCH_BYTES (attn_workspace_size(B, Hq, D,
- * num_splits)) returns ATTN_ERR_WORKSPACE and launches nothing.
+ * to what fits in the array; an explicit num_splits whose scratch
+ * (attn_workspace_size(B, Hq, D, n) for the count n the call uses, which is
+ * num_splits clamped to 256) exceeds ATTN_NOALLOC_SCRATCH_BYTES returns
+ * ATTN_ERR_WORKSPACE and launches nothing.
  *
  * Notes for callers:
  *  - Every GPU that loads the library holds the array until the process
@@ -270,8 +275,9 @@ attn_status kv_cache_write(
 
 /*
  * attn_workspace_size -- bytes of scratch attn_varlen_prefill /
- * attn_paged_decode need for `num_splits` KV segments: fp32 partial outputs
- * and log-sum-exps for every (token, query head, segment).  0 when
+ * attn_paged_decode need for `num_splits` KV segments: 256 bytes for the
+ * tensor-core kernel's work counter, then fp32 partial outputs and
+ * log-sum-exps for every (token, query head, segment).  256 when
  * num_splits <= 1.
  */
 size_t attn_workspace_size(int total_q, int Hq, int D, int num_splits);

@@ -38,36 +38,121 @@ def cache_dtype(b):
     return torch.float8_e4m3fn if b.kv_dtype == "fp8" else b.k_tok.dtype
 
 
+# Dirty memory.  A serving engine reuses cache pages and scratch across
+# requests, so unwritten cache rows, workspace bytes and the memory around
+# an output hold whatever was there before ("vLLM 中 Attention Kernel 如何
+# 并行处理多个请求", sec. 11: pages are handed from request to request).
+# The tests therefore fill caches, workspaces and output surroundings with
+# quiet-NaN bit patterns: a kernel that reads an unwritten cache row into a
+# result (even as 0 * NaN), reads workspace it did not write, or writes
+# outside its output shows up as a NaN or as a changed guard.
+NAN_BITS = {torch.bfloat16: (torch.int16, 0x7FC0), torch.float16: (torch.int16, 0x7E00),
+            torch.float8_e4m3fn: (torch.uint8, 0x7F), torch.float32: (torch.int32, 0x7FC00000)}
+GUARD = 3          # NaN rows before and after every output and lse buffer
+PAD = 8            # NaN columns after each token row of a strided output
+
+
+def nan_filled(shape, dtype, device="cuda"):
+    it, bits = NAN_BITS[dtype]
+    return torch.full(shape, bits, dtype=it, device=device).view(dtype)
+
+
+def is_nan_pattern(t):
+    it, bits = NAN_BITS[t.dtype]
+    return bool((t.contiguous().view(it) == bits).all())
+
+
+def same_bytes(a, b):
+    return torch.equal(a.detach().cpu().contiguous().view(torch.uint8), b.detach().cpu().contiguous().view(torch.uint8))
+
+
 def gpu_cache(b):
-    kc = torch.zeros((b.num_blocks, b.bs, b.Hkv, b.D), dtype=cache_dtype(b), device="cuda")
-    vc = torch.zeros_like(kc)
+    kc = nan_filled((b.num_blocks, b.bs, b.Hkv, b.D), cache_dtype(b))
+    vc = nan_filled((b.num_blocks, b.bs, b.Hkv, b.D), cache_dtype(b))
     va.kv_cache_write(b.k_tok.cuda(), b.v_tok.cuda(), kc, vc, b.slot_mapping.cuda(), b.k_scale, b.v_scale)
     return kc, vc
 
 
 def cpu_cache(b):
-    kc = torch.zeros((b.num_blocks, b.bs, b.Hkv, b.D), dtype=cache_dtype(b))
-    vc = torch.zeros_like(kc)
+    kc = nan_filled((b.num_blocks, b.bs, b.Hkv, b.D), cache_dtype(b), "cpu")
+    vc = nan_filled((b.num_blocks, b.bs, b.Hkv, b.D), cache_dtype(b), "cpu")
     oracle.kv_write(b.k_tok, b.v_tok, kc, vc, b.slot_mapping, b.k_scale, b.v_scale)
     return kc, vc
 
 
+class Guarded:
+    """out [T, Hq, D] and lse [T, Hq] views into NaN-filled buffers with
+    GUARD rows on each side (and, unless `contiguous`, PAD columns after each
+    token row, so out has a token stride above Hq * D), plus a NaN-filled
+    workspace of `ws_bytes` followed by guard bytes.  verify() checks that
+    nothing outside out, lse and the workspace was written."""
+
+    def __init__(self, T, Hq, D, dtype, ws_bytes=0, contiguous=False):
+        pad = 0 if contiguous else PAD
+        self.T, self.row = T, Hq * D
+        self.o_full = nan_filled((T + 2 * GUARD, Hq * D + pad), dtype)
+        self.out = self.o_full[GUARD:GUARD + T, :Hq * D].view(T, Hq, D)
+        self.l_full = nan_filled((T + 2 * GUARD, Hq), torch.float32)
+        self.lse = self.l_full[GUARD:GUARD + T]
+        self.ws_full = torch.full((ws_bytes + 4096,), 0xFF, dtype=torch.uint8, device="cuda")
+        self.ws = self.ws_full[:ws_bytes] if ws_bytes else None
+
+    def verify(self):
+        torch.cuda.synchronize()
+        T = self.T
+        assert is_nan_pattern(self.o_full[:GUARD]) and is_nan_pattern(self.o_full[GUARD + T:]), "write above/below out"
+        if self.o_full.shape[1] > self.row:
+            assert is_nan_pattern(self.o_full[:, self.row:]), "write into the padding of a token row"
+        assert is_nan_pattern(self.l_full[:GUARD]) and is_nan_pattern(self.l_full[GUARD + T:]), "write around lse"
+        assert bool((self.ws_full[self.ws_full.numel() - 4096:] == 0xFF).all()), "write past the workspace"
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def ws_bytes_for(T, Hq, D, B, max_q, max_k, Hkv, num_splits):
+    ns = num_splits if num_splits > 0 else va.attn_num_splits(B, max_q, max_k, Hq, Hkv, _sms())
+    return va.attn_workspace_size(T, Hq, D, ns)
+
+
 def gpu_attn(b, kc, vc, num_splits=0, causal=None, q=None, block_table=None, seqused_k=None,
-             cu=None, max_q=None, max_k=None):
+             cu=None, max_q=None, max_k=None, q_descale=1.0, **ext):
+    """attn_varlen_prefill(_ext) on dirty memory: out and lse inside NaN guards
+    (out with a padded token stride), a NaN-filled workspace; checks the
+    guards after the call."""
     q = (b.q if q is None else q).cuda()
-    out = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    T, Hq, D = q.shape
+    odt = torch.bfloat16 if q.dtype == torch.float8_e4m3fn else q.dtype
     bt = (b.block_table if block_table is None else block_table).cuda()
     su = (b.seqused_k if seqused_k is None else seqused_k).cuda()
     cu = (b.cu_seqlens_q if cu is None else cu).cuda()
-    va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt,
-                           b.max_seqlen_q if max_q is None else max_q,
-                           b.max_seqlen_k if max_k is None else max_k,
-                           b.softmax_scale, causal=b.causal if causal is None else causal, lse_out=lse,
+    mq = b.max_seqlen_q if max_q is None else max_q
+    mk = b.max_seqlen_k if max_k is None else max_k
+    g = Guarded(T, Hq, D, odt, ws_bytes_for(T, Hq, D, su.numel(), mq, mk, b.Hkv, num_splits))
+    va.attn_varlen_prefill(q, kc, vc, g.out, cu, su, bt, mq, mk, b.softmax_scale,
+                           causal=b.causal if causal is None else causal, lse_out=g.lse,
+                           q_descale=q_descale,
                            k_descale=b.k_scale if b.kv_dtype == "fp8" else 1.0,
                            v_descale=b.v_scale if b.kv_dtype == "fp8" else 1.0,
-                           num_splits=num_splits)
-    return out, lse
+                           num_splits=num_splits, workspace=g.ws, **ext)
+    g.verify()
+    return g.out, g.lse
+
+
+def gpu_decode(b, kc, vc, num_splits=0, q=None):
+    """attn_paged_decode on dirty memory (contiguous out inside NaN guard
+    rows, NaN-filled workspace); checks the guards after the call."""
+    q = (b.q if q is None else q).cuda()
+    B, Hq, D = q.shape
+    g = Guarded(B, Hq, D, q.dtype, ws_bytes_for(B, Hq, D, B, 1, b.max_seqlen_k, b.Hkv, num_splits),
+                contiguous=True)
+    va.attn_paged_decode(q, kc, vc, g.out, b.seqused_k.cuda(), b.block_table.cuda(), b.max_seqlen_k,
+                         b.softmax_scale, lse_out=g.lse, num_splits=num_splits, workspace=g.ws,
+                         k_descale=b.k_scale if b.kv_dtype == "fp8" else 1.0,
+                         v_descale=b.v_scale if b.kv_dtype == "fp8" else 1.0)
+    g.verify()
+    return g.out, g.lse
 
 
 def ref_attn(b, kc, vc, rows=None, causal=None):
@@ -166,15 +251,11 @@ def test_tiny_packed_prefill_then_decode():
     # one decode step: write each request's new token, attend over len + 1
     va.kv_cache_write(dec.k_tok.cuda(), dec.v_tok.cuda(), kc, vc, dec.slot_mapping.cuda())
     oracle.kv_write(dec.k_tok, dec.v_tok, ck, cv, dec.slot_mapping)
-    assert torch.equal(kc.cpu(), ck) and torch.equal(vc.cpu(), cv)
+    assert same_bytes(kc, ck) and same_bytes(vc, cv)
     ro, rl = ref_attn(dec, ck, cv)
     out, lse = gpu_attn(dec, kc, vc)
     check(out, lse, ro, rl, TOL)
-    q = dec.q.cuda()
-    o2 = torch.empty_like(q)
-    l2 = torch.empty((4, 8), dtype=torch.float32, device="cuda")
-    va.attn_paged_decode(q, kc, vc, o2, dec.seqused_k.cuda(), dec.block_table.cuda(), dec.max_seqlen_k,
-                         dec.softmax_scale, lse_out=l2)
+    o2, l2 = gpu_decode(dec, kc, vc)
     check(o2, l2, ro, rl, TOL)
     assert_no_device_error()
 
@@ -307,10 +388,7 @@ def test_decode_equals_last_row_of_prefill():
     b = W.make_batch([64], [64], 8, 2, 128, 16, seed=12)
     kc, vc = gpu_cache(b)
     out, lse = gpu_attn(b, kc, vc, num_splits=1)
-    d_out = torch.empty((1, 8, 128), dtype=torch.bfloat16, device="cuda")
-    d_lse = torch.empty((1, 8), dtype=torch.float32, device="cuda")
-    va.attn_paged_decode(b.q[63:64].cuda(), kc, vc, d_out, b.seqused_k.cuda(), b.block_table.cuda(), 64,
-                         b.softmax_scale, lse_out=d_lse, num_splits=1)
+    d_out, d_lse = gpu_decode(b, kc, vc, num_splits=1, q=b.q[63:64])
     assert max_err(d_out[0], out[63].double().cpu()) <= 4e-3
     assert max_err(d_lse[0], lse[63].double().cpu()) <= 1e-4
 
@@ -348,9 +426,10 @@ def test_merge_states_against_oracle(dtype):
     l2 = torch.randn((T, Hq), generator=g) * 5
     l1[0, :3] = -math.inf
     l2[0, 1:5] = -math.inf
-    out = torch.empty((T, Hq, D), dtype=dtype, device="cuda")
-    lo = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+    g = Guarded(T, Hq, D, dtype, contiguous=True)
+    out, lo = g.out, g.lse
     va.attn_merge_states(out, lo, o1.cuda(), l1.cuda(), o2.cuda(), l2.cuda())
+    g.verify()
     ro, rl = oracle.merge_states(o1.view(-1, D), l1.view(-1), o2.view(-1, D), l2.view(-1))
     tol = 1e-2 if dtype != torch.float32 else 1e-5
     assert max_err(out.view(-1, D), ro) <= tol
@@ -380,12 +459,9 @@ def test_workload1_llama8b_decode_full():
     b = W.decode_llama8b()
     kc, vc = gpu_cache(b)
     ck, cv = cpu_cache(b)
-    assert torch.equal(kc.cpu(), ck) and torch.equal(vc.cpu(), cv)
+    assert same_bytes(kc, ck) and same_bytes(vc, cv)
     ro, rl = ref_attn(b, ck, cv)
-    out = torch.empty((b.B, b.Hq, b.D), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((b.B, b.Hq), dtype=torch.float32, device="cuda")
-    va.attn_paged_decode(b.q.cuda(), kc, vc, out, b.seqused_k.cuda(), b.block_table.cuda(), b.max_seqlen_k,
-                         b.softmax_scale, lse_out=lse)
+    out, lse = gpu_decode(b, kc, vc)
     check(out, lse, ro, rl, TOL)
     assert_no_device_error()
 
@@ -409,21 +485,76 @@ def test_workload2_longctx_decode_full(longctx_ref, bs):
     b.slot_mapping = torch.cat([W.slots(b.block_table, r, p, bs) for r, p in enumerate(positions)])
     b.k_tok, b.v_tok = b16.k_tok, b16.v_tok
     kc, vc = gpu_cache(b)
-    out = torch.empty((b.B, b.Hq, b.D), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((b.B, b.Hq), dtype=torch.float32, device="cuda")
-    va.attn_paged_decode(b.q.cuda(), kc, vc, out, b.seqused_k.cuda(), b.block_table.cuda(), b.max_seqlen_k,
-                         b.softmax_scale, lse_out=lse)
+    out, lse = gpu_decode(b, kc, vc)
     check(out, lse, ro, rl, TOL)
     assert_no_device_error()
 
 
-def test_workload3_chunked_prefill_full_sampled():
+def segment_keys(max_k, n, tile=64):
+    """Keys per split-KV segment for n segments of a call whose longest
+    request has max_k keys: the keys cut evenly, rounded up to whole 64-key
+    tiles (the library's host planning rule for an explicit num_splits)."""
+    per = -(-max_k // n)
+    return -(-per // tile) * tile
+
+
+def boundary_rows(b, n_segments=1, per_request=256, seed=3, tile_rows=128):
+    """Token rows of a prefill batch where a tiled kernel is most likely to
+    go wrong, plus a seeded random sample.  For every request:
+      - both sides of every 128-packed-row Q-tile boundary (packed rows
+        128k - 1 and 128k, i.e. tokens (128k - 1) // G and 128k // G); every
+        second one is also a 256-row work-item boundary;
+      - with n_segments > 1: the tokens whose causal limit ctx + i is the
+        last key of a segment, the first key of the next one, and the first
+        key of the segment's last 64-key tile;
+      - its first and last token, and per_request seeded random tokens.
+    Returns sorted packed token indices."""
+    G = b.Hq // b.Hkv
+    cu = b.cu_seqlens_q.tolist()
+    g = torch.Generator().manual_seed(W.SEED0 + 900 + seed)
+    chunk = segment_keys(b.max_seqlen_k, n_segments) if n_segments > 1 else None
+    rows = set()
+    for r in range(b.B):
+        q0, ql, kv = cu[r], cu[r + 1] - cu[r], b.kv_lens[r]
+        if ql <= 0:
+            continue
+        ctx = kv - ql
+        local = {0, ql - 1}
+        for pr in range(tile_rows, ql * G, tile_rows):
+            local.update([(pr - 1) // G, pr // G])
+        if chunk:
+            for end in range(chunk, kv + chunk, chunk):
+                local.update([end - 1 - ctx, end - ctx, end - 64 - ctx])
+        local.update(torch.randint(0, ql, (per_request,), generator=g).tolist())
+        rows.update(q0 + i for i in local if 0 <= i < ql)
+    return sorted(rows)
+
+
+@pytest.fixture(scope="module")
+def chunked_ref():
+    """The chunked prefill batch and the oracle on the union of the boundary
+    rows of every split setting tested below (computed once: about 7,800
+    token rows x 32 heads over up to 12k keys, fp64)."""
     b = W.chunked_prefill()
-    kc, vc = gpu_cache(b)
-    out, lse = gpu_attn(b, kc, vc)
-    rows = _rows_sample(b, 48, seed=3)
+    rows = sorted(set(boundary_rows(b, 1)) | set(boundary_rows(b, 3)))
     ro, rl = ref_attn(b, *cpu_cache(b), rows=rows)
-    check(out, lse, ro, rl, TOL, rows=rows)
+    return b, rows, ro, rl
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, 0])
+def test_workload3_chunked_prefill_full_sampled(chunked_ref, num_splits):
+    """The chunked prefill workload at full size (16 requests, 1k-8k new
+    tokens on 0-4k cached), compared with the oracle on every Q-tile and
+    work-item boundary row, the rows at split-segment edges and 256 seeded
+    rows per request (all heads, out and lse); caches, workspace and the
+    memory around out are dirty (NaN patterns)."""
+    b, rows, ro, rl = chunked_ref
+    kc, vc = gpu_cache(b)
+    out, lse = gpu_attn(b, kc, vc, num_splits=num_splits)
+    mine = boundary_rows(b, n_segments=num_splits)
+    at = {r: i for i, r in enumerate(rows)}
+    idx = torch.tensor([at[r] for r in mine])
+    check(out, lse, ro[idx], rl[idx], TOL, rows=mine)
     assert_no_device_error()
 
 
@@ -503,7 +634,9 @@ def test_workload4_fp8_mixed_full_sampled():
     assert torch.equal(kc.view(torch.uint8).cpu(), ck.view(torch.uint8))
     assert torch.equal(vc.view(torch.uint8).cpu(), cv.view(torch.uint8))
     out, lse = gpu_attn(b, kc, vc)
-    rows = sorted(set(range(128)) | set(_rows_sample(b, 40, seed=4)))
+    # every decode row; the chunks' Q-tile and item boundary rows plus 32
+    # seeded rows each
+    rows = boundary_rows(b, per_request=32, seed=4)
     ro, rl = ref_attn(b, ck, cv, rows=rows)
     check(out, lse, ro, rl, TOL_FP8, rows=rows)
     assert_no_device_error()
@@ -583,25 +716,83 @@ def test_cuda_graph_capture_and_replay():
     assert_no_device_error()
 
 
-def test_tensor_core_schedule_slots_cycle():
-    """More consecutive calls than the tensor-core kernel has schedule slots
-    (64): every call takes a slot in turn and must find its counter rewound,
-    so every output is bitwise the first one (which matches the oracle)."""
+def test_tensor_core_repeated_calls_on_one_workspace():
+    """Many consecutive calls on one workspace: each call zeroes the
+    tensor-core kernel's work counter in the workspace before its launch,
+    so no call inherits a counter from the one before and every output is
+    bitwise the first (which matches the oracle)."""
     b = W.make_batch([130, 200, 1], [400, 260, 300], 8, 2, 128, 16, seed=18)
     kc, vc = gpu_cache(b)
     ro, rl = ref_attn(b, *cpu_cache(b))
-    first = None
+    dev = torch.device("cuda")
+    q, cu, su, bt = b.q.to(dev), b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev)
+    ws = torch.full((va.attn_workspace_size(b.T, b.Hq, b.D, 2),), 0xFF, dtype=torch.uint8, device=dev)
+    first = {}
     for it in range(140):
-        out, lse = gpu_attn(b, kc, vc, num_splits=1 + it % 2)
-        if first is None:
+        ns = 1 + it % 2
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt, b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale,
+                               lse_out=lse, num_splits=ns, workspace=ws)
+        if ns not in first:
             check(out, lse, ro, rl, TOL)
-            first = {1: (out, lse)}
-        elif (1 + it % 2) not in first:
-            check(out, lse, ro, rl, TOL)
-            first[1 + it % 2] = (out, lse)
+            first[ns] = (out, lse)
         else:
-            o0, l0 = first[1 + it % 2]
+            o0, l0 = first[ns]
             assert torch.equal(out, o0) and torch.equal(lse, l0), "call %d differs" % it
+    assert_no_device_error()
+
+
+def test_graph_replays_beside_eager_calls_on_another_stream():
+    """A captured mixed-batch step replayed on one stream while eager
+    tensor-core calls run on another, interleaved without synchronisation.
+    Each call has its own workspace, and the tensor-core kernel's work
+    counter lives there, so the two never share a counter: both outputs
+    match the oracle after 4 replays beside 4 x 20 eager calls."""
+    dev = torch.device("cuda")
+    a = W.make_batch([300, 1, 1, 40, 1, 129], [700, 900, 64, 40, 2000, 129], 32, 8, 128, 16, seed=19)
+    e = W.make_batch([200, 90, 1, 333], [260, 400, 77, 333], 16, 4, 128, 32, seed=20)
+    kca, vca = gpu_cache(a)
+    kce, vce = gpu_cache(e)
+    roa, rla = ref_attn(a, *cpu_cache(a))
+    roe, rle = ref_attn(e, *cpu_cache(e))
+    sms = _sms()
+
+    def bufs(b):
+        q = b.q.to(dev)
+        ns = va.attn_num_splits(b.B, b.max_seqlen_q, b.max_seqlen_k, b.Hq, b.Hkv, sms)
+        ws = torch.full((va.attn_workspace_size(b.T, b.Hq, b.D, max(ns, 2)),), 0xFF, dtype=torch.uint8,
+                        device=dev)
+        return (q, torch.empty_like(q), torch.empty(q.shape[:2], dtype=torch.float32, device=dev),
+                b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev), ws)
+
+    qa, oa, la, cua, sua, bta, wsa = bufs(a)
+    qe, oe, le, cue, sue, bte, wse = bufs(e)
+
+    def step_a():
+        va.attn_varlen_prefill(qa, kca, vca, oa, cua, sua, bta, a.max_seqlen_q, a.max_seqlen_k, a.softmax_scale,
+                               lse_out=la, num_splits=0, workspace=wsa)
+
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        step_a()
+    torch.cuda.current_stream().wait_stream(s1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step_a()
+    torch.cuda.synchronize()
+    s2.wait_stream(torch.cuda.current_stream())
+    for _ in range(4):
+        with torch.cuda.stream(s1):
+            g.replay()
+        with torch.cuda.stream(s2):
+            for _ in range(20):
+                va.attn_varlen_prefill(qe, kce, vce, oe, cue, sue, bte, e.max_seqlen_q, e.max_seqlen_k,
+                                       e.softmax_scale, lse_out=le, num_splits=0, workspace=wse)
+    torch.cuda.synchronize()
+    check(oa, la, roa, rla, TOL)
+    check(oe, le, roe, rle, TOL)
     assert_no_device_error()
 
 
@@ -635,14 +826,8 @@ def test_variants_against_oracle(case, num_splits):
         sinks = (torch.randn(32, generator=g) * 2.0).float()
     window = kw.get("window", (-1, -1))
     softcap = kw.get("softcap", 0.0)
-    dev = torch.device("cuda")
-    q = b.q.to(dev)
-    out = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-    va.attn_varlen_prefill(q, kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev),
-                           b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale, causal=causal, lse_out=lse,
-                           num_splits=num_splits, window=window, softcap=softcap,
-                           sinks=None if sinks is None else sinks.to(dev))
+    out, lse = gpu_attn(b, kc, vc, num_splits=num_splits, causal=causal, window=window, softcap=softcap,
+                        sinks=None if sinks is None else sinks.cuda())
     ro, rl = oracle.attention(b.q, *cpu_cache(b), b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
                               causal=causal, window=window, softcap=softcap,
                               sinks=None if sinks is None else sinks.double())
@@ -662,15 +847,8 @@ def test_variants_other_paths(D, kv_dtype):
     fp8 = kv_dtype == "fp8"
     for window, softcap, use_sinks in [((64, -1), 0.0, False), ((-1, -1), 4.0, True), ((17, -1), 1.5, True)]:
         for ns in (1, 0):
-            dev = torch.device("cuda")
-            q = b.q.to(dev)
-            out = torch.empty_like(q)
-            lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-            va.attn_varlen_prefill(q, kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev),
-                                   b.block_table.to(dev), b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale,
-                                   lse_out=lse, k_descale=b.k_scale if fp8 else 1.0,
-                                   v_descale=b.v_scale if fp8 else 1.0, num_splits=ns, window=window,
-                                   softcap=softcap, sinks=sinks.to(dev) if use_sinks else None)
+            out, lse = gpu_attn(b, kc, vc, num_splits=ns, window=window, softcap=softcap,
+                                sinks=sinks.cuda() if use_sinks else None)
             ro, rl = oracle.attention(b.q, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
                                       k_scale=b.k_scale if fp8 else 1.0, v_scale=b.v_scale if fp8 else 1.0,
                                       window=window, softcap=softcap,
@@ -685,28 +863,24 @@ def test_workload_swa_decode_with_sinks():
     b = W.swa_decode(B=8, lo=2048, hi=8192, window=1000)
     kc, vc = gpu_cache(b)
     win, sinks = b.extra["window"], b.extra["sinks"]
-    dev = torch.device("cuda")
-    q = b.q.to(dev)
     for ns in (0, 1):
-        out = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-        va.attn_varlen_prefill(q, kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev),
-                               1, b.max_seqlen_k, b.softmax_scale, lse_out=lse, num_splits=ns, window=win,
-                               sinks=sinks.to(dev))
+        out, lse = gpu_attn(b, kc, vc, num_splits=ns, window=win, sinks=sinks.cuda())
         ro, rl = oracle.attention(b.q, *cpu_cache(b), b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
                                   window=win, sinks=sinks.double())
         check(out, lse, ro, rl, TOL)
     assert_no_device_error()
 
 
-def test_workload_verify_full():
-    """Multi-token verification (the verify bench workload, smaller): 2-8
-    query tokens per request over paged contexts; requests of up to 16
-    packed rows run on the rows-light kernel, longer ones on the
-    tensor-core kernel, all in one call."""
-    b = W.verify_decode(B=32, hi=4096)
+@pytest.mark.parametrize("num_splits", [0, 1])
+def test_workload_verify_full(num_splits):
+    """Multi-token verification at the benchmarked shape (64 requests, 2-8
+    query tokens each over paged contexts of 0.5k-8k keys), every row:
+    requests of up to 16 packed rows run on 16-row CTAs, longer ones on
+    32-row CTAs, all in one call, with the automatic split counts and
+    without splitting."""
+    b = W.verify_decode()
     kc, vc = gpu_cache(b)
-    out, lse = gpu_attn(b, kc, vc)
+    out, lse = gpu_attn(b, kc, vc, num_splits=num_splits)
     ro, rl = ref_attn(b, *cpu_cache(b))
     check(out, lse, ro, rl, TOL)
     assert_no_device_error()
@@ -726,12 +900,7 @@ def test_fp8_query_against_oracle(bs, num_splits):
     ck, cv = cpu_cache(b)
     qs = float(b.q.float().abs().max()) / 448.0
     q8 = (b.q.float() / qs).to(torch.float8_e4m3fn)
-    dev = torch.device("cuda")
-    out = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(q8.shape[:2], dtype=torch.float32, device=dev)
-    va.attn_varlen_prefill(q8.to(dev), kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev),
-                           b.block_table.to(dev), b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale, lse_out=lse,
-                           q_descale=qs, k_descale=b.k_scale, v_descale=b.v_scale, num_splits=num_splits)
+    out, lse = gpu_attn(b, kc, vc, num_splits=num_splits, q=q8, q_descale=qs)
     ro, rl = oracle.attention(q8, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
                               k_scale=b.k_scale, v_scale=b.v_scale, q_scale=qs)
     check(out, lse, ro, rl, TOL_FP8)
@@ -739,13 +908,7 @@ def test_fp8_query_against_oracle(bs, num_splits):
 
 
 def _q8_call(b, q8, qs, kc, vc, num_splits=0):
-    dev = torch.device("cuda")
-    out = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(q8.shape[:2], dtype=torch.float32, device=dev)
-    va.attn_varlen_prefill(q8.to(dev), kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev),
-                           b.block_table.to(dev), b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale, lse_out=lse,
-                           q_descale=qs, k_descale=b.k_scale, v_descale=b.v_scale, num_splits=num_splits)
-    return out, lse
+    return gpu_attn(b, kc, vc, num_splits=num_splits, q=q8, q_descale=qs)
 
 
 @pytest.mark.parametrize("bs", [64, 256])
@@ -777,7 +940,7 @@ def test_fp8_query_mixed_workload_sampled():
     qs = float(b.q.float().abs().max()) / 448.0
     q8 = (b.q.float() / qs).to(torch.float8_e4m3fn)
     out, lse = _q8_call(b, q8, qs, kc, vc)
-    rows = sorted(set(range(128)) | set(_rows_sample(b, 40, seed=5)))
+    rows = boundary_rows(b, per_request=32, seed=5)
     ro, rl = oracle.attention(q8, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
                               k_scale=b.k_scale, v_scale=b.v_scale, q_scale=qs, rows=rows)
     check(out, lse, ro, rl, TOL_FP8, rows=rows)
@@ -793,14 +956,9 @@ def test_fp8_query_with_variants():
     q8 = (b.q.float() / qs).to(torch.float8_e4m3fn)
     g = torch.Generator().manual_seed(W.SEED0 + 760)
     sinks = (torch.randn(32, generator=g) * 2.0).float()
-    dev = torch.device("cuda")
     for ns in (1, 0):
-        out = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
-        lse = torch.empty(q8.shape[:2], dtype=torch.float32, device=dev)
-        va.attn_varlen_prefill(q8.to(dev), kc, vc, out, b.cu_seqlens_q.to(dev), b.seqused_k.to(dev),
-                               b.block_table.to(dev), b.max_seqlen_q, b.max_seqlen_k, b.softmax_scale, lse_out=lse,
-                               q_descale=qs, k_descale=b.k_scale, v_descale=b.v_scale, num_splits=ns,
-                               window=(100, -1), softcap=5.0, sinks=sinks.to(dev))
+        out, lse = gpu_attn(b, kc, vc, num_splits=ns, q=q8, q_descale=qs, window=(100, -1), softcap=5.0,
+                            sinks=sinks.cuda())
         ro, rl = oracle.attention(q8, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
                                   k_scale=b.k_scale, v_scale=b.v_scale, q_scale=qs, window=(100, -1),
                                   softcap=5.0, sinks=sinks.double())

@@ -54,6 +54,12 @@ def test_status_strings(lib):
 # at the workspace check, which also precedes every launch.
 FAKE = ctypes.c_void_p(4096)
 
+try:
+    import torch
+    _HAVE_GPU = torch.cuda.is_available()
+except Exception:  # pragma: no cover
+    _HAVE_GPU = False
+
 
 def prefill(lib, **kw):
     a = dict(q=FAKE, qs=8 * 128, k=FAKE, v=FAKE, out=FAKE, os=8 * 128, lse=None, cu=FAKE, su=FAKE,
@@ -88,11 +94,27 @@ def prefill(lib, **kw):
     (dict(q=ctypes.c_void_p(4104)), ERR_ALIGN),
     (dict(qs=8 * 128 + 4), ERR_ALIGN),
     (dict(ns=4, ws=None, wsb=0), None),     # no device here: reaches CUDA or fails on workspace
+    # a request may have more than 64 packed rows (17 tokens x 4 heads): the
+    # tensor-core kernel's work counter needs the first 256 workspace bytes,
+    # checked before the device is looked up
+    (dict(mq=17), ERR_WS),
+    (dict(mq=17, ws=FAKE, wsb=255), ERR_WS),
+    (dict(mq=17, ws=ctypes.c_void_p(4100), wsb=256), ERR_ALIGN),
+    (dict(mq=17, ws=FAKE, wsb=256), "device"),
+    # head size 64 never runs the tensor-core kernel: no workspace needed
+    (dict(mq=17, D=64, qs=8 * 64, os=8 * 64), "device"),
 ])
 def test_prefill_validation(lib, kw, status):
+    if status == "device" and _HAVE_GPU:
+        # these pass every host check and would launch on the placeholder
+        # pointers: they are meaningful (and safe) only without a device
+        pytest.skip("would launch kernels on placeholder pointers")
     st = prefill(lib, **kw)
     if status is None:
         assert st in (ERR_WS, ERR_CUDA, ERR_DEV)
+    elif status == "device":
+        # host checks passed; the call stopped at the device lookup
+        assert st in (ERR_CUDA, ERR_DEV)
     else:
         assert st == status
 
@@ -165,9 +187,11 @@ def test_tile_kind_with_context_and_brute_force(lib):
 
 
 def test_workspace_and_split_rules(lib):
-    assert va.attn_workspace_size(64, 32, 128, 1) == 0
+    # 256 bytes for the tensor-core kernel's work counter, then the partials
+    assert va.attn_workspace_size(64, 32, 128, 1) == 256
+    assert va.attn_workspace_size(0, 32, 128, 5) == 256
     n = va.attn_workspace_size(64, 32, 128, 5)
-    assert n >= 64 * 32 * 5 * (128 + 1) * 4 and n % 256 == 0
+    assert n >= 256 + 64 * 32 * 5 * (128 + 1) * 4 and n % 256 == 0
     # decode with few (request, KV head) pairs and long contexts splits;
     # big prefill batches do not
     assert va.attn_num_splits(4, 1, 131072, 64, 8, 152) > 8

@@ -7,9 +7,12 @@ cudaFree may cause.  For them attn_paged_decode_noalloc keeps its split-KV
 scratch in a fixed array inside libattn.so instead of a caller workspace.
 
 This file checks, through the C ABI, that two calls in a row give the same
-result as the regular attn_paged_decode (within the parity tolerance), that
-the leftover contents of the shared array from the first call do not leak
-into the second, and that a split count too large for the array is refused.
+result as the regular attn_paged_decode (within the parity tolerance, and
+bitwise at the same explicit split count), that the leftover contents of the
+shared array from the first call do not leak into the second, that a batch
+whose automatic split count would overflow the array runs with fewer
+segments and still matches, and that an explicit split count too large for
+the array is refused.
 It is named to run after every other test file, and needs nothing from them.
 """
 import pytest
@@ -59,10 +62,32 @@ def test_noalloc_decode_matches_regular_entry_point_twice():
         assert _maxerr(got_l, ref_l) <= TOL
         assert torch.isfinite(got_o.float()).all() and torch.isfinite(got_l).all()
         # with the same explicit split count both run the very same kernels
+        # on the same partial layout, so the results are bitwise equal
         o1, l1 = _decode(va.attn_paged_decode, b, kc, vc, num_splits=4)
         o2, l2 = _decode(va.attn_paged_decode_noalloc, b, kc, vc, num_splits=4)
-        assert _maxerr(o2, o1) <= TOL and _maxerr(l2, l1) <= TOL
+        assert torch.equal(o2, o1) and torch.equal(l2, l1)
         del kc, vc
+    assert va.attn_device_error_flag(reset=True) == 0
+
+
+def test_noalloc_caps_the_automatic_split_count_to_its_array():
+    """64 requests, the longest of 16k keys: the automatic choice for this
+    batch is 8 segments, whose partials (about 8.1 MiB) do not fit in the
+    8 MiB array, so the entry point runs fewer segments.  Its result must
+    still match the regular entry point given a workspace for all 8 (within
+    the parity tolerance: different segment boundaries round differently)."""
+    from varlen_flashattention_causal_gb300 import build
+    build.build()
+    b = W.make_batch([1] * 64, [16384, 12000, 5000, 1] + [300] * 60, 32, 8, 128, 16, seed=79)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ns = va.attn_num_splits(b.B, 1, b.max_seqlen_k, b.Hq, b.Hkv, sms)
+    assert va.attn_workspace_size(b.B, b.Hq, b.D, ns) > va.NOALLOC_SCRATCH_BYTES
+    kc, vc = _cache(b)
+    ref_o, ref_l = _decode(va.attn_paged_decode, b, kc, vc, num_splits=ns)
+    got_o, got_l = _decode(va.attn_paged_decode_noalloc, b, kc, vc)
+    torch.cuda.synchronize()
+    assert _maxerr(got_o, ref_o) <= TOL and _maxerr(got_l, ref_l) <= TOL
+    assert torch.isfinite(got_o.float()).all() and torch.isfinite(got_l).all()
     assert va.attn_device_error_flag(reset=True) == 0
 
 

@@ -125,10 +125,9 @@ def _i32(t, name):
 def _workspace(T, Hq, D, ns, device, workspace):
     if workspace is not None:
         return workspace, workspace.numel() * workspace.element_size()
-    if ns == 1:
-        return None, 0
+    # at least the tensor-core kernel's work counter, then the split partials
     n = attn_workspace_size(T, Hq, D, ns)
-    return torch.empty(max(n, 1), dtype=torch.uint8, device=device), n
+    return torch.empty(n, dtype=torch.uint8, device=device), n
 
 
 def _sms(device):

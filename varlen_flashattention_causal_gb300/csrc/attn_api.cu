@@ -88,6 +88,11 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t part_o_bytes(int T, int Hq, int D, int ns) { return align256((size_t)T * Hq * ns * D * sizeof(float)); }
 
+// Workspace layout: the tensor-core kernel's work counters in the first
+// kSchedBytes (zeroed by the call that uses them), then the split-KV
+// partials (O_s, then LSE_s) when a call splits.
+constexpr size_t kSchedBytes = 256;
+
 // Request classes by packed row count (q_len * G):
 //   0  rows <= 16: decode and short verify rows, mma.sync kernel with 16-row
 //      CTAs (one token x up to 16 heads of a group);
@@ -216,11 +221,20 @@ attn_status run_fwd(const FwdArgs &a) {
     attn_status st = validate_fwd(a);
     if (st != ATTN_OK) return st;
     if (a.B == 0 || a.T == 0) return ATTN_OK;
+    const int G = a.Hq / a.Hkv;
+    // A request of more than kMidRows packed rows may run on the tensor-core
+    // kernel, whose work counters live at the start of the workspace: such a
+    // call needs one even without split-KV (checked from host scalars alone,
+    // before the device is looked up).
+    const bool tc_on = tc_supported(a.D, a.q_dtype, a.kv_dtype, G) && (long long)std::max(1, a.max_q) * G > kMidRows;
+    if (tc_on) {
+        if (!a.ws || a.ws_bytes < kSchedBytes) return ATTN_ERR_WORKSPACE;
+        if (!aligned16(a.ws)) return ATTN_ERR_ALIGN;
+    }
     DevInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != ATTN_OK) return st;
 
-    const int G = a.Hq / a.Hkv;
     const bool uniform = (long long)a.T == (long long)a.B * a.max_q;
     // a window bound at least max_seqlen_k long excludes nothing
     const int wl = (a.window_left >= a.max_k) ? -1 : a.window_left;
@@ -286,8 +300,17 @@ attn_status run_fwd(const FwdArgs &a) {
     p.sinks = a.sinks;
     p.part_stride = stride;
     if (stride > 1) {
-        p.part_o = static_cast<float *>(a.ws);
-        p.part_lse = reinterpret_cast<float *>(static_cast<char *>(a.ws) + part_o_bytes(a.T, a.Hq, a.D, stride));
+        char *base = static_cast<char *>(a.ws) + kSchedBytes;
+        p.part_o = reinterpret_cast<float *>(base);
+        p.part_lse = reinterpret_cast<float *>(base + part_o_bytes(a.T, a.Hq, a.D, stride));
+    }
+    if (pl.c[2].on) {
+        // the work counters start at zero in every call (a stream-ordered
+        // memset: capturable, and no counter state carries over between
+        // calls, captured graphs or streams)
+        p.sched = static_cast<unsigned long long *>(a.ws);
+        st = check_cuda(cudaMemsetAsync(a.ws, 0, 2 * sizeof(unsigned long long), a.stream));
+        if (st != ATTN_OK) return st;
     }
     // every segment spans a whole number of K/V tiles
     auto chunk_for = [&](int n) {
@@ -343,8 +366,9 @@ attn_status run_fwd(const FwdArgs &a) {
 extern "C" {
 
 size_t attn_workspace_size(int total_q, int Hq, int D, int num_splits) {
-    if (num_splits <= 1 || total_q <= 0 || Hq <= 0 || D <= 0) return 0;
-    return part_o_bytes(total_q, Hq, D, num_splits) + align256((size_t)total_q * Hq * num_splits * sizeof(float));
+    if (num_splits <= 1 || total_q <= 0 || Hq <= 0 || D <= 0) return kSchedBytes;
+    return kSchedBytes + part_o_bytes(total_q, Hq, D, num_splits) +
+           align256((size_t)total_q * Hq * num_splits * sizeof(float));
 }
 
 int attn_num_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int num_sms) {

@@ -66,15 +66,15 @@ extern "C" attn_status attn_paged_decode_noalloc(
                                  max_seq_len, Hq, Hkv, D, block_size, num_blocks, q_dtype, kv_dtype,
                                  softmax_scale, k_descale, v_descale, num_splits, nullptr, 0, stream);
     }
-    // an explicit split count whose partial results do not fit is refused;
-    // the automatic choice (num_splits = 0) is capped to what fits
-    if (num_splits > 1 && attn_workspace_size(B, Hq, D, num_splits) > (size_t)ATTN_NOALLOC_SCRATCH_BYTES)
-        return ATTN_ERR_WORKSPACE;
+    // the regular entry point refuses an explicit split count whose partial
+    // results do not fit in ws_bytes (ATTN_ERR_WORKSPACE, before any launch)
+    // and caps the automatic choice (num_splits = 0) to what fits
     void *scratch = nullptr;
     const attn_status st = scratch_for_current_device(&scratch);
     if (st != ATTN_OK) return st;
     // every partial slot the kernels read is written earlier in the same
-    // call (empty segments write -inf), so nothing needs clearing first
+    // call (empty segments write -inf), and a work counter, when used, is
+    // zeroed by the call itself, so nothing needs clearing first
     return attn_paged_decode(q, k_cache, v_cache, out, lse_out, seq_lens, block_table, bt_row_stride, B,
                              max_seq_len, Hq, Hkv, D, block_size, num_blocks, q_dtype, kv_dtype, softmax_scale,
                              k_descale, v_descale, num_splits, scratch, (size_t)ATTN_NOALLOC_SCRATCH_BYTES,

@@ -73,7 +73,6 @@
 #include "tma_host.h"
 
 #include <algorithm>
-#include <atomic>
 
 namespace attn {
 
@@ -165,14 +164,7 @@ __device__ __forceinline__ void derive(const FwdParams &p, Item &it) {
 struct TcParams {
     FwdParams f;
     int kv_rows;                  // rows per TMA page load: gcd(block_size, 64)
-    unsigned long long *sched;    // {next ticket, CTAs done} of this launch's schedule slot
 };
-
-// Ticket counters of the persistent schedule.  Each launch takes the next
-// slot of its device in turn; the slot's counters are zero when a launch
-// starts because the previous launch on it rewound them as it finished.
-constexpr int kSchedSlots = 64;
-__device__ unsigned long long g_tc_sched[kSchedSlots][2];
 
 // max of three (one instruction on this architecture)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -324,7 +316,7 @@ __global__ void __launch_bounds__(TcLayout<FP8, Q8>::kThreads, 1)
             long long v = blockIdx.x;
             if (k > 0) {
                 unsigned long long t = 0;
-                if (lane == 0) t = atomicAdd(tp.sched, 1ull);
+                if (lane == 0) t = atomicAdd(p.sched, 1ull);
                 v = P + (long long)__shfl_sync(0xffffffffu, t, 0);
             }
             while (sc_chunk < p.B && v >= sc_base + sc_total) {
@@ -931,19 +923,8 @@ __global__ void __launch_bounds__(TcLayout<FP8, Q8>::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    if (tid == 0) {
-        if (*abort_flag) raise_error(p.err, ERR_TIMEOUT);
-        // the last CTA to finish rewinds the ticket counter for the slot's next launch
-        // (every CTA has drawn its last ticket before it counts itself done)
-        __threadfence();
-        if (atomicAdd(tp.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
-            atomicExch(tp.sched, 0ull);
-            atomicExch(tp.sched + 1, 0ull);
-        }
-    }
+    if (tid == 0 && *abort_flag) raise_error(p.err, ERR_TIMEOUT);
 }
-
-constexpr int kMaxSchedDevices = 64;
 
 static int gcd_int(int a, int b) {
     while (b) {
@@ -977,30 +958,10 @@ static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &qmap, const 
 
 cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int kv_dtype, int64_t T, int num_sms,
                           cudaStream_t stream) {
+    if (!f.sched) return cudaErrorInvalidValue;
     TcParams tp{};
     tp.f = f;
     tp.kv_rows = gcd_int(f.bs, kBN);
-    {
-        // device address of the ticket slots, looked up on a device's first
-        // launch; host threads racing on that first launch store the same
-        // value, through an atomic
-        static std::atomic<unsigned long long *> slots[kMaxSchedDevices];
-        static std::atomic<unsigned> next[kMaxSchedDevices];
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        if (dev < 0 || dev >= kMaxSchedDevices) return cudaErrorInvalidDevice;
-        unsigned long long *base = slots[dev].load(std::memory_order_acquire);
-        if (!base) {
-            void *a = nullptr;
-            e = cudaGetSymbolAddress(&a, g_tc_sched);
-            if (e != cudaSuccess) return e;
-            if (!a) return cudaErrorInvalidSymbol;
-            base = static_cast<unsigned long long *>(a);
-            slots[dev].store(base, std::memory_order_release);
-        }
-        tp.sched = base + 2 * (next[dev].fetch_add(1u) % kSchedSlots);
-    }
     const bool q16 = q_dtype == DT_FP16;
     const bool q8 = q_dtype == DT_E4M3;
     const bool fp8 = kv_dtype == DT_E4M3;

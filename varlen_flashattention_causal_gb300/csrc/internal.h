@@ -49,6 +49,9 @@ struct FwdParams {
     int window_left, window_right;
     float cap_in, cap_out;
     const float *sinks;
+    // tensor-core kernel only: {next ticket, unused} of this call's work
+    // counter, in the caller's workspace, zeroed before the launch
+    unsigned long long *sched;
 };
 
 // Split-KV reduction over the partial states of every token whose request
