@@ -136,3 +136,25 @@ def test_reference_arm_prints_one_contract_line(capsys, monkeypatch):
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_prefill_sample_rows_and_their_pairs():
+    """The prefill CPU baseline's sample: per_request distinct rows of each
+    request (all rows of a shorter one), and its unmasked-pair count
+    recounted key by key."""
+    b = W.make_batch([5, 40, 1], [9, 60, 30], 8, 2, 64, 16, seed=5)
+    per_req = bench.prefill_sample_rows(b, 16, seed=1)
+    cu = b.cu_seqlens_q.tolist()
+    assert [len(r) for r in per_req] == [5, 16, 1]
+    for r, rows in enumerate(per_req):
+        assert len(set(rows)) == len(rows) and all(cu[r] <= t < cu[r + 1] for t in rows)
+    rows = sorted(t for rr in per_req for t in rr)
+    want = 0
+    for t in rows:
+        r = [i for i in range(b.B) if cu[i] <= t < cu[i + 1]][0]
+        i, ctx = t - cu[r], b.kv_lens[r] - b.q_lens[r]
+        want += sum(1 for j in range(b.kv_lens[r]) if j <= ctx + i)
+    assert bench.rows_pairs(b, rows) == want
+    # all rows of the batch: the prefill flop count's pairs
+    all_rows = list(range(b.T))
+    assert 4 * b.D * b.Hq * bench.rows_pairs(b, all_rows) == bench.prefill_flops(b)

@@ -32,14 +32,15 @@ def test_bounded_wait_gives_up_and_the_context_survives():
     assert va.attn_device_error_flag() == 0
 
     # the next call runs normally and matches the oracle
-    b = W.make_batch([1] * 4, [40, 130, 7, 300], 8, 2, 128, 16, seed=90, device="cuda")
+    b = W.make_batch([1] * 4, [40, 130, 7, 300], 8, 2, 128, 16, seed=90)
     kc = torch.zeros((b.num_blocks, b.bs, b.Hkv, b.D), dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
-    va.kv_cache_write(b.k_tok, b.v_tok, kc, vc, b.slot_mapping)
-    out = torch.empty_like(b.q)
+    va.kv_cache_write(b.k_tok.cuda(), b.v_tok.cuda(), kc, vc, b.slot_mapping.cuda())
+    q = b.q.cuda()
+    out = torch.empty_like(q)
     lse = torch.empty((b.T, b.Hq), dtype=torch.float32, device="cuda")
-    va.attn_paged_decode(b.q, kc, vc, out, b.seqused_k, b.block_table, max(b.kv_lens), b.softmax_scale,
-                         lse_out=lse)
+    va.attn_paged_decode(q, kc, vc, out, b.seqused_k.cuda(), b.block_table.cuda(), max(b.kv_lens),
+                         b.softmax_scale, lse_out=lse)
     ref, ref_lse = oracle.attention(b.q, kc, vc, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale)
     assert float((out.double().cpu() - ref).abs().max()) < 1e-2
     assert float((lse.double().cpu() - ref_lse).abs().max()) < 1e-2
