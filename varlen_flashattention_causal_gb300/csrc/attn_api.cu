@@ -330,7 +330,9 @@ attn_status run_fwd(const FwdArgs &a) {
         t.rows_hi = c.hi;
         t.n_row_blocks = (std::min(max_rows, c.hi) + c.rpc - 1) / c.rpc;
         if ((long long)t.n_row_blocks * ns[k] > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-        if (c.tc)
+        if (c.tc && tc2_supported(a.D, a.q_dtype, a.kv_dtype, G))
+            st = check_cuda(launch_fwd_tc2(t, a.q_dtype, a.T, dev->sms, a.stream));
+        else if (c.tc)
             st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.kv_dtype, a.T, dev->sms, a.stream));
         else
             st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, c.rpc, a.max_q <= 1, a.stream));

@@ -122,5 +122,9 @@ int tc_rows_per_cta();
 // (persistent: at most num_sms CTAs)
 cudaError_t launch_fwd_tc(const FwdParams &p, int q_dtype, int kv_dtype, int64_t T, int num_sms,
                           cudaStream_t stream);
+// the same work on pairs of SMs (16-bit q and cache, head size 128): whether
+// it takes the shape, and its launcher (persistent clusters of two CTAs)
+bool tc2_supported(int D, int q_dtype, int kv_dtype, int G);
+cudaError_t launch_fwd_tc2(const FwdParams &p, int q_dtype, int64_t T, int num_sms, cudaStream_t stream);
 
 }  // namespace attn
