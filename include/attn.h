@@ -75,7 +75,9 @@ typedef enum {
     ATTN_ERR_HEAD_SIZE = 6,   /* head size not 64 or 128 */
     ATTN_ERR_WORKSPACE = 7,   /* workspace NULL or smaller than required */
     ATTN_ERR_CUDA = 8,        /* a CUDA runtime call failed (no device, launch error) */
-    ATTN_ERR_DEVICE = 9       /* the current device is not an sm_103 GPU */
+    ATTN_ERR_DEVICE = 9,      /* the current device is not an sm_103 GPU */
+    ATTN_ERR_TABLE = 10       /* ATTN_DEBUG_VALIDATE=1 or attn_validate_*: an
+                                 integer table breaks the contract */
 } attn_status;
 
 typedef enum {
@@ -298,6 +300,46 @@ int attn_num_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, 
  * element mask).  Host mirror of the rule the kernels apply.
  */
 int attn_tile_kind(int q_lo, int q_hi, int k_lo, int k_hi, int ctx);
+
+/*
+ * Debug validation of the integer tables ("FlashAttention deep dive",
+ * flash_attn_varlen_func argument table; [MR] sec. 10-11).
+ *
+ * With ATTN_DEBUG_VALIDATE set to a non-empty value other than "0" in the
+ * environment, attn_varlen_prefill(_ext), attn_paged_decode(_noalloc) and
+ * kv_cache_write copy their integer tables to the host after the work
+ * already queued on `stream`, synchronise the stream, and return
+ * ATTN_ERR_TABLE (launching nothing) when a check below fails.  The block
+ * table is read only where the kernels would read it (ceil(kv_len /
+ * block_size) entries a row), and only after every kv_len has been checked
+ * against max_seqlen_k and the row stride.  Calls on a stream that is
+ * being captured into a CUDA graph are not checked (no synchronisation is
+ * possible there).  Without the variable no call reads its tables on the
+ * host.
+ *
+ * attn_validate_tables -- the same checks on tables the caller holds in
+ * HOST memory.  cu_seqlens_q may be NULL (decode: request r owns query row
+ * r, and total_q must equal B); block_table holds B rows of bt_row_stride
+ * entries.  ATTN_ERR_TABLE when
+ *   cu_seqlens_q[0] != 0, cu_seqlens_q[B] != total_q, or a q_len is
+ *   negative or above max_seqlen_q;
+ *   a kv_len (seqused_k[r]) is negative or above max_seqlen_k;
+ *   causal != 0 and kv_len < q_len (the new tokens' keys are part of kv_len);
+ *   B > 1 and ceil(kv_len / block_size) > bt_row_stride;
+ *   a block id among the first ceil(kv_len / block_size) of its row is
+ *   outside [0, num_blocks).
+ * ATTN_ERR_SHAPE for negative sizes, ATTN_ERR_NULL for a missing table.
+ *
+ * attn_validate_slots -- HOST slot_mapping of T tokens: ATTN_ERR_TABLE when
+ * a slot is below -1 (padding) or at least num_blocks * block_size.
+ *
+ * attn_debug_validate_enabled -- 1 when the environment switch is on.
+ */
+attn_status attn_validate_tables(const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                                 const int32_t *block_table, int64_t bt_row_stride, int B, int total_q,
+                                 int max_seqlen_q, int max_seqlen_k, int block_size, int num_blocks, int causal);
+attn_status attn_validate_slots(const int64_t *slot_mapping, int T, int block_size, int num_blocks);
+int attn_debug_validate_enabled(void);
 
 /* Human-readable name of a status code. */
 const char *attn_status_string(attn_status s);

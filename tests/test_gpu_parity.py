@@ -414,6 +414,73 @@ def test_out_of_range_block_id_reads_zeros_and_is_flagged():
     check(out[1:], lse[1:], ro[1:], rl[1:], TOL)
 
 
+def test_debug_validation_refuses_bad_tables_and_launches_nothing(monkeypatch):
+    """With ATTN_DEBUG_VALIDATE=1 the entry points copy their integer tables
+    to the host and refuse a call that breaks the contract (ATTN_ERR_TABLE)
+    before anything is launched: out, lse, the workspace and the cache keep
+    their bytes and the device error word stays clear.  A valid call runs
+    and gives the same bytes as without the check, and a call captured into
+    a CUDA graph is not checked (no host synchronisation under capture)."""
+    b = W.make_batch([5, 1, 140], [64, 300, 140], 8, 2, 128, 16, seed=21)
+    kc, vc = gpu_cache(b)
+    ref_out, ref_lse = gpu_attn(b, kc, vc, num_splits=1)
+    va.attn_device_error_flag(reset=True)
+    monkeypatch.setenv("ATTN_DEBUG_VALIDATE", "1")
+    out, lse = gpu_attn(b, kc, vc, num_splits=1)
+    assert same_bytes(out, ref_out) and same_bytes(lse, ref_lse)
+
+    bt, su, cu = b.block_table.clone(), b.seqused_k.clone(), b.cu_seqlens_q.clone()
+    bt[1, 3] = b.num_blocks                      # a block id the request reads, outside the pool
+    su_short = su.clone()
+    su_short[2] = 139                            # 140 new tokens, 139 cached keys
+    cu_bad = cu.clone()
+    cu_bad[0] = 1                                # cu_seqlens_q must start at 0
+    T, Hq, D = b.q.shape
+    cases = [dict(bt=bt), dict(mk=b.max_seqlen_k - 1), dict(mq=b.max_seqlen_q - 1), dict(su=su_short),
+             dict(cu=cu_bad)]
+    for c in cases:
+        g = Guarded(T, Hq, D, b.q.dtype, va.attn_workspace_size(T, Hq, D, 1))
+        with pytest.raises(va.AttnError) as e:
+            va.attn_varlen_prefill(b.q.cuda(), kc, vc, g.out, c.get("cu", cu).cuda(), c.get("su", su).cuda(),
+                                   c.get("bt", b.block_table).cuda(), c.get("mq", b.max_seqlen_q),
+                                   c.get("mk", b.max_seqlen_k), b.softmax_scale, lse_out=g.lse,
+                                   num_splits=1, workspace=g.ws)
+        assert e.value.status == va.ATTN_ERR_TABLE, c.keys()
+        g.verify()
+        assert is_nan_pattern(g.out) and is_nan_pattern(g.lse)
+        assert bool((g.ws_full == 0xFF).all())
+    # decode with the bad block id
+    qd = b.q[:3].contiguous().cuda()
+    od = nan_filled((3, Hq, D), b.q.dtype)
+    with pytest.raises(va.AttnError) as e:
+        va.attn_paged_decode(qd, kc, vc, od, su.cuda(), bt.cuda(), b.max_seqlen_k, b.softmax_scale, num_splits=1)
+    assert e.value.status == va.ATTN_ERR_TABLE and is_nan_pattern(od)
+    # KV write with a slot past the cache
+    k0, v0 = kc.clone(), vc.clone()
+    slots = b.slot_mapping.clone()
+    slots[7] = b.num_blocks * b.bs
+    with pytest.raises(va.AttnError) as e:
+        va.kv_cache_write(b.k_tok.cuda(), b.v_tok.cuda(), kc, vc, slots.cuda())
+    assert e.value.status == va.ATTN_ERR_TABLE
+    assert same_bytes(kc, k0) and same_bytes(vc, v0)
+    torch.cuda.synchronize()
+    assert va.attn_device_error_flag(reset=True) == 0
+
+    # under capture: not checked, and the replay gives the same bytes
+    g = Guarded(T, Hq, D, b.q.dtype, va.attn_workspace_size(T, Hq, D, 1))
+    args = (b.q.cuda(), kc, vc, g.out, cu.cuda(), su.cuda(), b.block_table.cuda(), b.max_seqlen_q,
+            b.max_seqlen_k, b.softmax_scale)
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            va.attn_varlen_prefill(*args, lse_out=g.lse, num_splits=1, workspace=g.ws)
+    graph.replay()
+    g.verify()
+    assert same_bytes(g.out, ref_out) and same_bytes(g.lse, ref_lse)
+
+
 # ------------------------------------------------------------------- merge
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])

@@ -43,8 +43,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(10):
-        assert va.attn_status_string(s)
+    for s in range(11):
+        assert va.attn_status_string(s) != "unknown status"
     assert va.attn_status_string(ERR_HD).startswith("head size")
 
 
@@ -305,3 +305,96 @@ def test_bindings_pass_arguments_in_the_declared_order(lib):
     assert _status_of(write(src=torch.float16)) == ERR_DTYPE
     assert _status_of(write(kdt=torch.float8_e4m3fn, k_scale=0.0)) == ERR_SHAPE
     assert _status_of(write(kdt=torch.float8_e4m3fn, v_scale=-1.0)) == ERR_SHAPE
+
+
+# ------------------------------------------------ debug validation of the integer tables
+
+def _tables():
+    """Two requests ("vLLM 中 Attention Kernel 如何并行处理多个请求" sec. 5: packed
+    rows; sec. 11: block table): q_len 3 and 5, kv_len 20 and 5 at block size
+    16, a 4-column table whose unused columns hold garbage."""
+    cu = torch.tensor([0, 3, 8], dtype=torch.int32)
+    su = torch.tensor([20, 5], dtype=torch.int32)
+    bt = torch.tensor([[7, 2, -99, 12345], [4, 99999, -1, 0]], dtype=torch.int32)
+    return cu, su, bt
+
+
+def _v(cu, su, bt, mq=5, mk=20, bs=16, nb=8, causal=True, total_q=None):
+    return va.attn_validate_tables(cu, su, bt, mq, mk, bs, nb, causal, total_q)
+
+
+def test_validate_tables_accepts_a_valid_batch(lib):
+    cu, su, bt = _tables()
+    assert _v(cu, su, bt) == 0
+    # only the first ceil(kv_len / block_size) entries of a row are read
+    assert _v(cu, su, bt[:, :2].contiguous()) == 0
+    # bounds above the truth are fine; decode form (one row per request)
+    assert _v(cu, su, bt, mq=100, mk=1000) == 0
+    assert _v(None, su, bt, mq=1) == 0
+    assert _v(cu, su.new_zeros(2), bt, causal=False) == 0
+
+
+@pytest.mark.parametrize("edit", [
+    "cu0", "cu_end", "cu_back", "mq_small", "mk_small", "kv_neg", "causal_short", "block_neg",
+    "block_big", "stride_short", "decode_total"])
+def test_validate_tables_rejects_each_broken_rule(lib, edit):
+    cu, su, bt = _tables()
+    kw = {}
+    if edit == "cu0":
+        cu[0] = 1
+    elif edit == "cu_end":
+        kw["total_q"] = 9                       # q holds 9 rows, cu_seqlens_q ends at 8
+    elif edit == "cu_back":
+        cu[1] = 9                                # request 1 gets q_len -1
+        kw["mq"] = 100
+    elif edit == "mq_small":
+        kw["mq"] = 4                             # q_len 5 > max_seqlen_q
+    elif edit == "mk_small":
+        kw["mk"] = 19                            # kv_len 20 > max_seqlen_k
+    elif edit == "kv_neg":
+        su[1] = -1
+    elif edit == "causal_short":
+        su[1] = 4                                # 5 new tokens but 4 cached keys
+    elif edit == "block_neg":
+        bt[0, 1] = -1
+    elif edit == "block_big":
+        bt[1, 0] = 8                             # num_blocks = 8
+    elif edit == "stride_short":
+        bt = bt[:, :1]                           # request 0 needs two columns
+        bt = torch.as_strided(bt.contiguous().view(-1), (2, 1), (1, 1))
+    elif edit == "decode_total":
+        assert _v(None, su, bt, mq=1, total_q=3) == va.ATTN_ERR_TABLE
+        return
+    assert _v(cu, su, bt, **kw) == va.ATTN_ERR_TABLE
+    # the same batch without the mask accepts short caches
+    if edit == "causal_short":
+        assert _v(cu, su, bt, causal=False, **kw) == 0
+
+
+def test_validate_tables_on_a_generated_batch(lib):
+    from varlen_flashattention_causal_gb300 import workloads as W
+    b = W.make_batch([37, 1, 64, 0], [300, 129, 64, 17], Hq=8, Hkv=2, D=64, bs=16, seed=3)
+    nb = 1 + max(int(b.block_table[r, :(L + 15) // 16].max()) for r, L in enumerate(b.kv_lens))
+    st = va.attn_validate_tables(b.cu_seqlens_q, b.seqused_k, b.block_table, b.max_seqlen_q,
+                                 b.max_seqlen_k, 16, nb)
+    assert st == 0
+    assert va.attn_validate_tables(b.cu_seqlens_q, b.seqused_k, b.block_table, b.max_seqlen_q,
+                                   b.max_seqlen_k, 16, nb - 1) == va.ATTN_ERR_TABLE
+
+
+def test_validate_slots(lib):
+    ok = torch.tensor([0, -1, 127, 64], dtype=torch.int64)
+    assert va.attn_validate_slots(ok, 16, 8) == 0
+    for bad in (-2, 128, 1 << 40):
+        t = ok.clone()
+        t[2] = bad
+        assert va.attn_validate_slots(t, 16, 8) == va.ATTN_ERR_TABLE
+
+
+def test_debug_switch_reads_the_environment(lib, monkeypatch):
+    monkeypatch.delenv("ATTN_DEBUG_VALIDATE", raising=False)
+    assert not va.attn_debug_validate_enabled()
+    monkeypatch.setenv("ATTN_DEBUG_VALIDATE", "0")
+    assert not va.attn_debug_validate_enabled()
+    monkeypatch.setenv("ATTN_DEBUG_VALIDATE", "1")
+    assert va.attn_debug_validate_enabled()

@@ -21,11 +21,13 @@ __all__ = [
     "AttnError", "attn_varlen_prefill", "attn_varlen_prefill_ext", "attn_paged_decode",
     "attn_paged_decode_noalloc", "attn_merge_states", "kv_cache_write", "attn_workspace_size",
     "attn_num_splits", "attn_tile_kind", "attn_status_string", "attn_device_error_flag",
-    "attn_selftest_wait_timeout", "library_path",
+    "attn_selftest_wait_timeout", "attn_validate_tables", "attn_validate_slots",
+    "attn_debug_validate_enabled", "library_path",
 ]
 
 ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3, ATTN_FP32 = 0, 1, 2, 3
 ERR_BLOCK_ID, ERR_SLOT, ERR_TIMEOUT = 1, 2, 4
+ATTN_ERR_TABLE = 10
 
 _lib = None
 
@@ -85,6 +87,12 @@ def _load():
     lib.attn_device_error_flag.argtypes = [i32]
     lib.attn_selftest_wait_timeout.restype = i32
     lib.attn_selftest_wait_timeout.argtypes = [vp]
+    lib.attn_validate_tables.restype = i32
+    lib.attn_validate_tables.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, i32]
+    lib.attn_validate_slots.restype = i32
+    lib.attn_validate_slots.argtypes = [vp, i32, i32, i32]
+    lib.attn_debug_validate_enabled.restype = i32
+    lib.attn_debug_validate_enabled.argtypes = []
     _lib = lib
     return lib
 
@@ -257,6 +265,44 @@ def attn_selftest_wait_timeout(stream=None):
     gives up after its limit (2 s) and raises ERR_TIMEOUT in the device error
     word (read it with attn_device_error_flag)."""
     _check("attn_selftest_wait_timeout", _load().attn_selftest_wait_timeout(_stream(stream)))
+
+
+def _host_i32(t, name):
+    t = torch.as_tensor(t)
+    if t.device.type != "cpu" or t.dtype != torch.int32:
+        raise TypeError("%s must be an int32 CPU tensor" % name)
+    return t
+
+
+def attn_validate_tables(cu_seqlens_q, seqused_k, block_table, max_seqlen_q, max_seqlen_k, block_size,
+                         num_blocks, causal=True, total_q=None):
+    """Check host copies of a call's integer tables (the ATTN_DEBUG_VALIDATE
+    checks); returns the attn_status code (0 = ok, ATTN_ERR_TABLE = 10).
+    cu_seqlens_q may be None (decode: one query row per request)."""
+    su = _host_i32(seqused_k, "seqused_k").contiguous()
+    bt = _host_i32(block_table, "block_table")
+    if bt.dim() != 2 or bt.stride(1) != 1:
+        raise TypeError("block_table must be 2-D with unit column stride")
+    B = su.numel()
+    cu = None if cu_seqlens_q is None else _host_i32(cu_seqlens_q, "cu_seqlens_q").contiguous()
+    if total_q is None:
+        total_q = B if cu is None else int(cu[-1])
+    return int(_load().attn_validate_tables(_p(cu), _p(su), _p(bt), bt.stride(0), B, int(total_q),
+                                            int(max_seqlen_q), int(max_seqlen_k), int(block_size),
+                                            int(num_blocks), int(bool(causal))))
+
+
+def attn_validate_slots(slot_mapping, block_size, num_blocks):
+    """Check a host slot_mapping (int64); returns the attn_status code."""
+    sm = torch.as_tensor(slot_mapping)
+    if sm.device.type != "cpu" or sm.dtype != torch.int64:
+        raise TypeError("slot_mapping must be an int64 CPU tensor")
+    sm = sm.contiguous()
+    return int(_load().attn_validate_slots(_p(sm), sm.numel(), int(block_size), int(num_blocks)))
+
+
+def attn_debug_validate_enabled():
+    return bool(_load().attn_debug_validate_enabled())
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20   # ATTN_NOALLOC_SCRATCH_BYTES in include/attn.h

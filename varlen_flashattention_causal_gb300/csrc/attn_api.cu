@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "../../include/attn.h"
 #include "internal.h"
@@ -217,10 +218,51 @@ attn_status validate_fwd(const FwdArgs &a) {
     return ATTN_OK;
 }
 
+// ATTN_DEBUG_VALIDATE=1: copy the integer tables of the call to the host,
+// after the work already queued on the stream (which may be writing them),
+// and check them with attn_validate_tables.  The block table is copied row
+// by row, ceil(kv_len / block_size) entries a row: exactly the entries the
+// kernels would read, and only once every kv_len is known to be within
+// max_seqlen_k.  A stream that is being captured cannot be synchronised,
+// so calls captured into a graph are not checked.
+attn_status debug_check_fwd(const FwdArgs &a) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(a.stream, &cs) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return ATTN_OK;
+    std::vector<int32_t> cu(a.cu_seqlens_q ? a.B + 1 : 0), used(a.B);
+    if (a.cu_seqlens_q && cudaMemcpyAsync(cu.data(), a.cu_seqlens_q, cu.size() * sizeof(int32_t),
+                                          cudaMemcpyDefault, a.stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (cudaMemcpyAsync(used.data(), a.seqused_k, used.size() * sizeof(int32_t), cudaMemcpyDefault, a.stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(a.stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    for (int r = 0; r < a.B; ++r) {
+        if (used[r] < 0 || used[r] > a.max_k) return ATTN_ERR_TABLE;
+        // rows of a [B, W] table: a row never reaches into the next one
+        if (a.B > 1 && (used[r] + a.bs - 1) / a.bs > a.bt_stride) return ATTN_ERR_TABLE;
+    }
+    const int w = (a.max_k + a.bs - 1) / a.bs;
+    std::vector<int32_t> bt((size_t)a.B * std::max(w, 1), 0);
+    for (int r = 0; r < a.B; ++r) {
+        const int n = (used[r] + a.bs - 1) / a.bs;
+        if (n > 0 && cudaMemcpyAsync(bt.data() + (size_t)r * w, a.block_table + (int64_t)r * a.bt_stride,
+                                     n * sizeof(int32_t), cudaMemcpyDefault, a.stream) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    if (cudaStreamSynchronize(a.stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    return attn_validate_tables(a.cu_seqlens_q ? cu.data() : nullptr, used.data(), bt.data(), std::max(w, 1), a.B,
+                                a.T, a.max_q, a.max_k, a.bs, a.num_blocks, a.causal);
+}
+
 attn_status run_fwd(const FwdArgs &a) {
     attn_status st = validate_fwd(a);
     if (st != ATTN_OK) return st;
     if (a.B == 0 || a.T == 0) return ATTN_OK;
+    if (attn_debug_validate_enabled()) {
+        st = debug_check_fwd(a);
+        if (st != ATTN_OK) return st;
+    }
     const int G = a.Hq / a.Hkv;
     // A request of more than kMidRows packed rows may run on the tensor-core
     // kernel, whose work counters live at the start of the workspace: such a
@@ -397,6 +439,7 @@ const char *attn_status_string(attn_status s) {
     case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
     case ATTN_ERR_CUDA: return "CUDA runtime error";
     case ATTN_ERR_DEVICE: return "current device is not sm_103";
+    case ATTN_ERR_TABLE: return "cu_seqlens_q, seqused_k, block_table or slot_mapping breaks the contract";
     }
     return "unknown status";
 }
@@ -555,6 +598,21 @@ attn_status kv_cache_write(const void *key, int64_t key_stride_tok, const void *
         key_stride_tok % 8 != 0 || value_stride_tok % 8 != 0)
         return ATTN_ERR_ALIGN;
     if (T == 0) return ATTN_OK;
+    if (attn_debug_validate_enabled()) {
+        // see debug_check_fwd: host copy of the slots, skipped under capture
+        const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cs == cudaStreamCaptureStatusNone) {
+            std::vector<int64_t> slots(T);
+            if (cudaMemcpyAsync(slots.data(), slot_mapping, slots.size() * sizeof(int64_t), cudaMemcpyDefault, s) !=
+                    cudaSuccess ||
+                cudaStreamSynchronize(s) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            const attn_status vs = attn_validate_slots(slots.data(), T, block_size, num_blocks);
+            if (vs != ATTN_OK) return vs;
+        }
+    }
     DevInfo *dev = nullptr;
     attn_status st = device_info(&dev);
     if (st != ATTN_OK) return st;
