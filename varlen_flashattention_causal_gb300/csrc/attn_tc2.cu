@@ -80,13 +80,6 @@ constexpr int kPThreads = 352;
 constexpr int kPConsumersEven = 10;                     // warps 1-10 read the item ring
 constexpr int kPConsumersOdd = 10;                      // warps 0-9
 constexpr float kPRescale = 8.0f;                       // log2 units
-// one pair of P values in every kPEmuPeriod takes its exponentials on the
-// FMA pipe (ex2_fma2), the others on the MUFU unit, whose rate alone would
-// match the tensor-core time of a tile (0: all on the MUFU unit)
-#ifndef ATTN_TC2_EMU_PERIOD
-#define ATTN_TC2_EMU_PERIOD 4
-#endif
-constexpr int kPEmuPeriod = ATTN_TC2_EMU_PERIOD;
 constexpr uint16_t kPairMask = 3;
 static_assert(kPSmem <= 232448, "shared memory per CTA");
 
@@ -669,15 +662,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 for (int e = 0; e < 64; e += 2) {
                     const float2 x2 =
                         __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nb2);
-                    float2 p2;
-                    if (kPEmuPeriod > 0 && (e / 2) % kPEmuPeriod == kPEmuPeriod - 1) {
-                        p2 = ex2_fma2(x2);
-                    } else {
-                        p2.x = ex2(x2.x);
-                        p2.y = ex2(x2.y);
-                    }
-                    rs2[(e >> 1) & 3] = __fadd2_rn(rs2[(e >> 1) & 3], p2);
-                    pk[e / 2] = pack2<BF16>(p2.x, p2.y);
+                    const float p0 = ex2(x2.x);
+                    const float p1 = ex2(x2.y);
+                    rs2[(e >> 1) & 3] = __fadd2_rn(rs2[(e >> 1) & 3], make_float2(p0, p1));
+                    pk[e / 2] = pack2<BF16>(p0, p1);
                 }
                 const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
                 const float2 r03 = __fadd2_rn(r01, r23);

@@ -134,41 +134,6 @@ __device__ __forceinline__ float tanh_ex2(float y) {
     return 1.f - __fdividef(2.f, 1.f + ex2(t));
 }
 
-// 2^x for a pair of fp32 values on the FMA pipe instead of the MUFU unit,
-// for softmax tiles where the MUFU exponentials alone take as long as the
-// tensor-core work.  Cody-Waite style reduction: 2^x = 2^j * 2^f with
-// j = floor(x) (an fp32 add rounded toward -infinity against 1.5 * 2^23
-// leaves j in the low bits of the sum) and f = x - j in [0, 1); 2^f is a
-// cubic 1 + f (a + f (b + f c)) whose coefficients were fitted for this
-// library: the minimax relative error on [0, 1] under p(0) = 1, p(1) = 2
-// (a + b + c = 1), found by Lawson's iteratively reweighted least squares;
-// the largest relative error is 1.03e-4, far below the rounding of P to
-// bf16 or fp16.  2^j is added into the exponent field of p.  Inputs are
-// clamped to >= -127, where j = -127, f = 0, p = 1 and the sum of the
-// fields is exactly +0: masked scores (-inf) give P = 0 as with ex2.
-// Inputs in (-127, -126) give values below 2^-126 with a wrong scale, and
-// inputs must stay below 128 (softmax inputs here are at most 8).
-constexpr float kEx2PolyA = 0.6954243f;
-constexpr float kEx2PolyB = 0.22630768f;
-constexpr float kEx2PolyC = 0.07826797f;
-__device__ __forceinline__ float2 ex2_fma2(float2 x) {
-    x.x = fmaxf(x.x, -127.f);
-    x.y = fmaxf(x.y, -127.f);
-    uint64_t xv, mv, tv;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(xv) : "f"(x.x), "f"(x.y));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(mv) : "f"(12582912.f));
-    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(tv) : "l"(xv), "l"(mv));
-    float2 t;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(t.x), "=f"(t.y) : "l"(tv));
-    const float2 j = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));
-    const float2 f = __fadd2_rn(x, make_float2(-j.x, -j.y));
-    float2 q = __ffma2_rn(f, make_float2(kEx2PolyC, kEx2PolyC), make_float2(kEx2PolyB, kEx2PolyB));
-    q = __ffma2_rn(q, f, make_float2(kEx2PolyA, kEx2PolyA));
-    q = __ffma2_rn(q, f, make_float2(1.f, 1.f));
-    return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
-                       __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
-}
-
 // Programmatic dependent launch.  Every kernel of the library is launched
 // with programmatic stream serialisation, so it may be scheduled while the
 // previous kernel in the stream drains.  pdl_wait() blocks until that
