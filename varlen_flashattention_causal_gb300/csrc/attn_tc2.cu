@@ -702,7 +702,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 4; ++c) vr[c] = make_uint4(0, 0, 0, 0);
                     }
-                    fence_proxy_async_smem();
+                    // both SMs' tensor cores read this CTA's V half, the peer's
+                    // through the cluster: a CTA-scope proxy fence is not enough
+                    // for that (measured: a stand-alone converter writing the
+                    // whole half this way was read stale now and then by the peer
+                    // until it fenced all proxies and ordered at cluster scope)
+                    fence_proxy_async_all();
+                    fence_acq_rel_cluster();
                 }
                 // P -> TMEM over the S buffer it came from (packed columns
                 // 32 sg .. 32 sg + 31: this group's 64 keys)
