@@ -291,7 +291,7 @@ def wl_prefill(va, dev, steps, warmup, pk):
     return {"workload": "chunked varlen causal prefill: B=16, new U[1k,8k] on cached U[0,4k], Hq=32, Hkv=8, "
                         "D=128, bf16, block_size 64",
             "metric": "varlen causal prefill TFLOP/s", "value": round(fl / (med * 1e-3) / 1e12, 1),
-            "unit": "TFLOP/s", "ms": round(med, 4), "flops": fl, "kernel": "fwd_tc_kernel (tcgen05)",
+            "unit": "TFLOP/s", "ms": round(med, 4), "flops": fl, "kernel": "fwd_tc2_kernel (tcgen05 cta_group::2, pairs of SMs)",
             "roofline": roofline("tensor", fl, med, tc, "TFLOP/s"), "clocks": clk}
 
 
@@ -345,40 +345,27 @@ def wl_longctx(bs):
 
 def wl_cascade(va, dev, steps, warmup, pk):
     hbm, tc = pk
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     b = W.cascade_decode()
     kc, vc, _, _ = _device_cache(b, dev)
     P = b.extra["prefix"]
     nblk = P // b.bs
     T, Hq, D = b.q.shape
     q = b.q.to(dev)
-    pre_o, suf_o, out = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    pre_l = torch.empty((T, Hq), dtype=torch.float32, device=dev)
-    suf_l, lse = torch.empty_like(pre_l), torch.empty_like(pre_l)
+    out = torch.empty_like(q)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
     cu0 = torch.tensor([0, T], dtype=torch.int32, device=dev)
     su0 = torch.tensor([P], dtype=torch.int32, device=dev)
     bt = b.block_table.to(dev)
     cu, su = b.cu_seqlens_q.to(dev), (b.seqused_k - P).to(dev)
-    # automatic split counts assume the call has the GPU to itself; with
-    # the two calls running side by side, 4 prefix and 2 suffix segments
-    # measured fastest (sweep of {1,2,4,8,16} x {2,4,8} on a GB300)
-    ns_pair = (4, 2)
-    w1 = torch.empty(va.attn_workspace_size(T, Hq, D, ns_pair[0]), dtype=torch.uint8, device=dev)
-    w2 = torch.empty(va.attn_workspace_size(T, Hq, D, ns_pair[1]), dtype=torch.uint8, device=dev)
-    pre_stream = torch.cuda.Stream()
+    # one attn_cascade call: the prefix half on a second stream, both halves'
+    # segments merged by one combine; the library picks both split counts
+    ns_pair = va.attn_cascade_splits(b.B, T, 1, P, b.max_seqlen_k - P, Hq, b.Hkv, D)
+    wsp = torch.empty(va.attn_workspace_size(T, Hq, D, sum(ns_pair)), dtype=torch.uint8, device=dev)
+    aux = torch.cuda.Stream()
 
     def step():
-        # the prefix and suffix calls share no output or workspace: the
-        # prefix runs on a second stream, joined before the merge
-        cur = torch.cuda.current_stream()
-        pre_stream.wait_stream(cur)
-        with torch.cuda.stream(pre_stream):
-            va.attn_varlen_prefill(q, kc, vc, pre_o, cu0, su0, bt[:1], T, P, b.softmax_scale, causal=False,
-                                   lse_out=pre_l, num_splits=ns_pair[0], workspace=w1)
-        va.attn_varlen_prefill(q, kc, vc, suf_o, cu, su, bt[:, nblk:], 1, b.max_seqlen_k - P,
-                               b.softmax_scale, causal=True, lse_out=suf_l, num_splits=ns_pair[1], workspace=w2)
-        cur.wait_stream(pre_stream)
-        va.attn_merge_states(out, lse, pre_o, pre_l, suf_o, suf_l)
+        va.attn_cascade(q, kc, vc, out, cu0, su0, bt[0], P, cu, su, bt[:, nblk:], 1, b.max_seqlen_k - P,
+                        b.softmax_scale, lse_out=lse, workspace=wsp, aux_stream=aux)
 
     # the step as a serving loop runs it: captured once in a CUDA graph and
     # replayed (no host work between the launches)
@@ -402,7 +389,7 @@ def wl_cascade(va, dev, steps, warmup, pk):
                         "Hq=32, Hkv=8, D=128, bf16, block_size 64",
             "metric": "cascade decode GB/s (prefix read once)", "value": round(by / (med * 1e-3) / 1e9, 1),
             "unit": "GB/s", "ms": round(med, 4), "bytes": by, "splits": list(ns_pair),
-            "timing": "cuda graph of prefix + suffix + merge, prefix call on a second stream",
+            "timing": "cuda graph of one attn_cascade call (prefix half on a second stream, one combine)",
             "l2": "flushed between timed steps (%d MB write)" % (2 * L2_BYTES >> 20),
             "roofline": roofline("hbm", by, med, hbm, "GB/s"), "clocks": clk}
 

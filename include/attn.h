@@ -302,6 +302,66 @@ int attn_num_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, 
 int attn_tile_kind(int q_lo, int q_hi, int k_lo, int k_hi, int ctx);
 
 /*
+ * attn_cascade -- [vLLM-FA] Cascade Attention in one call: every query
+ * token attends to a prefix of keys shared by all requests and to its own
+ * request's suffix, and the two states are merged by log-sum-exp
+ * (merge_attn_states).  The result equals attn_varlen_prefill over the
+ * concatenated block rows (prefix blocks, then the request's own), causal.
+ *
+ * Prefix half (the pages' cu_prefix_query_lens / prefix_kv_lens form):
+ *   cu_prefix_query_lens  device int32 [2] = {0, total_q}
+ *   prefix_kv_lens        device int32 [1] = {prefix_len}
+ *   prefix_block_table    device int32, ceil(prefix_len / block_size) ids
+ *   prefix_len            host copy of prefix_kv_lens[0]; a multiple of
+ *                         block_size (ATTN_ERR_SHAPE otherwise), may be 0
+ *   Every prefix key precedes every query: no mask.
+ * Suffix half: cu_seqlens_q, suffix_kv_lens (the request's keys after the
+ *   prefix, its new tokens' keys included), suffix_block_table (row stride
+ *   bt_row_stride; a view block_table[:, prefix_len / block_size:] of the
+ *   full table is allowed), max_seqlen_q, max_suffix_len: as in
+ *   attn_varlen_prefill, causal with bottom-right alignment within the suffix.
+ * Both halves write the partial states of their KV segments into one
+ *   workspace array and a single combine writes out / lse_out (lse_out may
+ *   be NULL): three launches instead of the five of two split calls and a
+ *   merge.  prefix_splits / suffix_splits: segments of each half, 0 = the
+ *   library's choice for the two halves running side by side
+ *   (attn_cascade_splits).
+ * workspace: at least attn_workspace_size(total_q, Hq, D, ns_p + ns_s) bytes
+ *   (16-byte aligned) for the counts the call uses; ATTN_ERR_WORKSPACE
+ *   otherwise.
+ * aux_stream: a second stream for the prefix half, forked from `stream`
+ *   after the work already queued there and joined before the combine (the
+ *   library records two events it owns per host thread and device); NULL or
+ *   equal to `stream`: both halves on `stream`.  Capturable in a CUDA graph
+ *   (fork and join become graph edges).
+ * Types, head sizes, alignment and errors as attn_varlen_prefill, with
+ * 16-bit q (out in q's type) over a cache of q's type or e4m3.
+ */
+attn_status attn_cascade(
+    const void *q, int64_t q_stride_tok, const void *k_cache, const void *v_cache,
+    void *out, int64_t out_stride_tok, float *lse_out,
+    const int32_t *cu_prefix_query_lens, const int32_t *prefix_kv_lens,
+    const int32_t *prefix_block_table, int prefix_len,
+    const int32_t *cu_seqlens_q, const int32_t *suffix_kv_lens,
+    const int32_t *suffix_block_table, int64_t bt_row_stride,
+    int B, int total_q, int max_seqlen_q, int max_suffix_len,
+    int Hq, int Hkv, int D, int block_size, int num_blocks,
+    attn_dtype q_dtype, attn_dtype kv_dtype, float softmax_scale,
+    float k_descale, float v_descale, int prefix_splits, int suffix_splits,
+    void *workspace, size_t ws_bytes, attn_stream_t stream, attn_stream_t aux_stream);
+
+/*
+ * attn_cascade_splits -- the segment counts attn_cascade(prefix_splits = 0,
+ * suffix_splits = 0) chooses for these host scalars on num_sms SMs: each
+ * half gets a share of the SMs in proportion to its estimated time alone
+ * (the prefix's tensor-core work, the suffix's cache bytes) and enough
+ * segments to fill it.  Returns 0, or -1 for invalid sizes.
+ */
+int attn_cascade_splits(int B, int total_q, int max_seqlen_q, int prefix_len, int max_suffix_len, int Hq,
+                        int Hkv, int D, int q_dtype, int kv_dtype, int num_sms, int *prefix_splits,
+                        int *suffix_splits);
+
+/*
  * Debug validation of the integer tables ("FlashAttention deep dive",
  * flash_attn_varlen_func argument table; [MR] sec. 10-11).
  *

@@ -694,6 +694,63 @@ def test_workload3_cascade_decode_full():
         assert_no_device_error()
 
 
+def test_cascade_entry_point_against_oracle():
+    """attn_cascade: the shared prefix and every request's suffix in one
+    call, their segments merged by one combine ("FlashAttention deep
+    dive", Cascade Attention), against plain attention over prefix + suffix:
+    the library's split counts and explicit ones, with and without a second
+    stream for the prefix half, and as a CUDA graph replayed three times
+    (bit-identical to the eager call with the same counts)."""
+    b = W.cascade_decode()
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    ro, rl = ref_attn(b, ck, cv)
+    P = b.extra["prefix"]
+    nblk = P // b.bs
+    T, Hq, D = b.q.shape
+    q, bt = b.q.cuda(), b.block_table.cuda()
+    cu0 = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    pk = torch.tensor([P], dtype=torch.int32, device="cuda")
+    cu, su = b.cu_seqlens_q.cuda(), (b.seqused_k - P).cuda()
+    auto = va.attn_cascade_splits(b.B, T, 1, P, b.max_seqlen_k - P, Hq, b.Hkv, D)
+    aux = torch.cuda.Stream()
+
+    def call(g, nsp, nss, use_aux):
+        va.attn_cascade(q, kc, vc, g.out, cu0, pk, bt[0], P, cu, su, bt[:, nblk:], 1, b.max_seqlen_k - P,
+                        b.softmax_scale, lse_out=g.lse, prefix_splits=nsp, suffix_splits=nss, workspace=g.ws,
+                        aux_stream=aux if use_aux else None)
+
+    ref_auto = None
+    for nsp, nss, use_aux in ((0, 0, True), (0, 0, False), (1, 1, True), (4, 2, True), (8, 8, False)):
+        tot = (nsp or auto[0]) + (nss or auto[1])
+        g = Guarded(T, Hq, D, b.q.dtype, va.attn_workspace_size(T, Hq, D, tot))
+        call(g, nsp, nss, use_aux)
+        g.verify()
+        check(g.out, g.lse, ro, rl, TOL)
+        if nsp == 0 and use_aux:
+            ref_auto = (g.out.clone(), g.lse.clone())
+        elif nsp == 0:
+            assert torch.equal(g.out, ref_auto[0]) and torch.equal(g.lse, ref_auto[1])
+    assert_no_device_error()
+
+    g = Guarded(T, Hq, D, b.q.dtype, va.attn_workspace_size(T, Hq, D, auto[0] + auto[1]))
+    warm = torch.cuda.Stream()
+    warm.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(warm):
+        call(g, 0, 0, True)
+    torch.cuda.current_stream().wait_stream(warm)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(g, 0, 0, True)
+    for _ in range(3):
+        g.out.fill_(0)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(g.out, ref_auto[0]) and torch.equal(g.lse, ref_auto[1])
+    g.verify()
+    assert_no_device_error()
+
+
 def test_workload4_fp8_mixed_full_sampled():
     b = W.fp8_mixed()
     kc, vc = gpu_cache(b)

@@ -398,3 +398,43 @@ def test_debug_switch_reads_the_environment(lib, monkeypatch):
     assert not va.attn_debug_validate_enabled()
     monkeypatch.setenv("ATTN_DEBUG_VALIDATE", "1")
     assert va.attn_debug_validate_enabled()
+
+
+# ------------------------------------------------ cascade entry point (host side)
+
+def _casc(D=128, bs=16, qdt=torch.bfloat16, kdt=torch.bfloat16, P=32):
+    q, kc, out = _cpu(3, 8, D, dtype=qdt), _cpu(8, bs, 2, D, dtype=kdt), _cpu(3, 8, D)
+    cu0 = torch.tensor([0, 3], dtype=torch.int32)
+    pk = torch.tensor([P], dtype=torch.int32)
+    pbt = torch.zeros(4, dtype=torch.int32)
+    cu = torch.tensor([0, 1, 2, 3], dtype=torch.int32)
+    su = torch.tensor([5, 5, 5], dtype=torch.int32)
+    bt = torch.zeros((3, 4), dtype=torch.int32)
+    return lambda: va.attn_cascade(q, kc, kc, out, cu0, pk, pbt, P, cu, su, bt, 1, 5, 0.1, prefix_splits=1,
+                                   suffix_splits=1, stream=0)
+
+
+def test_cascade_host_checks(lib):
+    """attn_cascade checks both halves on the host before anything runs:
+    head size, block size, dtypes, and a prefix that does not end on a block
+    boundary ("FlashAttention deep dive", Cascade Attention: the common
+    prefix is a whole number of blocks)."""
+    assert _status_of(_casc(D=96)) == ERR_HD
+    assert _status_of(_casc(bs=24)) == ERR_BS
+    assert _status_of(_casc(P=40)) == ERR_SHAPE
+    assert _status_of(_casc(kdt=torch.float16)) == ERR_DTYPE
+    assert _status_of(_casc(qdt=torch.float8_e4m3fn, kdt=torch.float8_e4m3fn)) == ERR_DTYPE
+
+
+def test_cascade_split_rule(lib):
+    """The library's split counts for the two halves of a cascade call: each
+    at least one, more prefix segments for a longer prefix, more suffix
+    segments for longer suffixes, and none above the 256 clamp."""
+    a, b = va.attn_cascade_splits(64, 64, 1, 4096, 1024, 32, 8, 128, num_sms=152)
+    assert 1 <= a <= 256 and 1 <= b <= 256
+    a2, _ = va.attn_cascade_splits(64, 64, 1, 65536, 1024, 32, 8, 128, num_sms=152)
+    _, b2 = va.attn_cascade_splits(64, 64, 1, 4096, 16384, 32, 8, 128, num_sms=152)
+    assert a2 >= a and b2 >= b
+    for args in ((0, 64, 1, 4096, 1024, 32, 8, 128), (64, 64, 1, 4096, 1024, 32, 7, 128)):
+        with pytest.raises(ValueError):
+            va.attn_cascade_splits(*args, num_sms=152)

@@ -21,7 +21,8 @@ __all__ = [
     "AttnError", "attn_varlen_prefill", "attn_varlen_prefill_ext", "attn_paged_decode",
     "attn_paged_decode_noalloc", "attn_merge_states", "kv_cache_write", "attn_workspace_size",
     "attn_num_splits", "attn_tile_kind", "attn_status_string", "attn_device_error_flag",
-    "attn_selftest_wait_timeout", "attn_validate_tables", "attn_validate_slots",
+    "attn_selftest_wait_timeout", "attn_validate_tables", "attn_validate_slots", "attn_cascade",
+    "attn_cascade_splits",
     "attn_debug_validate_enabled", "library_path",
 ]
 
@@ -87,6 +88,13 @@ def _load():
     lib.attn_device_error_flag.argtypes = [i32]
     lib.attn_selftest_wait_timeout.restype = i32
     lib.attn_selftest_wait_timeout.argtypes = [vp]
+    lib.attn_cascade.restype = i32
+    lib.attn_cascade.argtypes = [
+        vp, i64, vp, vp, vp, i64, vp, vp, vp, vp, i32, vp, vp, vp, i64,
+        i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+        f32, f32, f32, i32, i32, vp, sz, vp, vp]
+    lib.attn_cascade_splits.restype = i32
+    lib.attn_cascade_splits.argtypes = [i32] * 11 + [c.POINTER(i32), c.POINTER(i32)]
     lib.attn_validate_tables.restype = i32
     lib.attn_validate_tables.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, i32]
     lib.attn_validate_slots.restype = i32
@@ -210,6 +218,58 @@ def attn_paged_decode(q, k_cache, v_cache, out, seq_lens, block_table, max_seq_l
         float(softmax_scale), float(k_descale), float(v_descale), int(num_splits), _p(ws), ws_bytes,
         _stream(stream))
     _check("attn_paged_decode", st)
+    return out
+
+
+def attn_cascade_splits(B, total_q, max_seqlen_q, prefix_len, max_suffix_len, Hq, Hkv, D, q_dtype=ATTN_BF16,
+                        kv_dtype=ATTN_BF16, num_sms=None):
+    """(prefix_splits, suffix_splits) attn_cascade chooses by itself."""
+    if num_sms is None:
+        num_sms = _sms(torch.device("cuda", torch.cuda.current_device()))
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    st = _load().attn_cascade_splits(int(B), int(total_q), int(max_seqlen_q), int(prefix_len), int(max_suffix_len),
+                                     int(Hq), int(Hkv), int(D), int(q_dtype), int(kv_dtype), int(num_sms),
+                                     ctypes.byref(a), ctypes.byref(b))
+    if st != 0:
+        raise ValueError("attn_cascade_splits: invalid sizes")
+    return a.value, b.value
+
+
+def attn_cascade(q, k_cache, v_cache, out, cu_prefix_query_lens, prefix_kv_lens, prefix_block_table, prefix_len,
+                 cu_seqlens_q, suffix_kv_lens, suffix_block_table, max_seqlen_q, max_suffix_len, softmax_scale,
+                 lse_out=None, k_descale=1.0, v_descale=1.0, prefix_splits=0, suffix_splits=0, workspace=None,
+                 stream=None, aux_stream=None):
+    """Cascade attention in one call (see include/attn.h): prefix shared by
+    every request (cu_prefix_query_lens = [0, T], prefix_kv_lens =
+    [prefix_len], one row of block ids) plus each request's causal suffix,
+    merged in one combine.  aux_stream: optional second stream for the
+    prefix half.  The workspace is allocated here when not given."""
+    lib = _load()
+    T, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    B = suffix_kv_lens.numel()
+    for t, n in ((cu_prefix_query_lens, "cu_prefix_query_lens"), (prefix_kv_lens, "prefix_kv_lens"),
+                 (prefix_block_table, "prefix_block_table"), (cu_seqlens_q, "cu_seqlens_q"),
+                 (suffix_kv_lens, "suffix_kv_lens")):
+        _i32(t, n)
+    if suffix_block_table.dtype != torch.int32 or suffix_block_table.stride(-1) != 1:
+        raise TypeError("suffix_block_table must be int32 with unit column stride")
+    if prefix_splits > 0 and suffix_splits > 0:
+        ns = prefix_splits + suffix_splits
+    else:
+        a, b = attn_cascade_splits(B, T, max_seqlen_q, prefix_len, max_suffix_len, Hq, Hkv, D, _dt(q),
+                                   _dt(k_cache), _sms(q.device))
+        ns = (prefix_splits or a) + (suffix_splits or b)
+    ws, ws_bytes = _workspace(T, Hq, D, ns, q.device, workspace)
+    aux = None if aux_stream is None else _stream(aux_stream)
+    st = lib.attn_cascade(
+        _p(q), q.stride(0), _p(k_cache), _p(v_cache), _p(out), out.stride(0), _p(lse_out),
+        _p(cu_prefix_query_lens), _p(prefix_kv_lens), _p(prefix_block_table), int(prefix_len),
+        _p(cu_seqlens_q), _p(suffix_kv_lens), _p(suffix_block_table), suffix_block_table.stride(0),
+        B, T, int(max_seqlen_q), int(max_suffix_len), Hq, Hkv, D, bs, nb, _dt(q), _dt(k_cache),
+        float(softmax_scale), float(k_descale), float(v_descale), int(prefix_splits), int(suffix_splits),
+        _p(ws), ws_bytes, _stream(stream), aux)
+    _check("attn_cascade", st)
     return out
 
 

@@ -255,6 +255,131 @@ attn_status debug_check_fwd(const FwdArgs &a) {
                                 a.T, a.max_q, a.max_k, a.bs, a.num_blocks, a.causal);
 }
 
+// window bounds that exclude nothing become -1; the keys one CTA can see
+// (with a left window bound, at most the window plus the CTA's query span and
+// the right bound, from a tile-aligned start) size the split segments
+struct Span {
+    int wl, wr, max_k_eff;
+};
+Span key_span(const FwdArgs &a) {
+    Span sp;
+    sp.wl = (a.window_left >= a.max_k) ? -1 : a.window_left;
+    sp.wr = (a.window_right >= a.max_k) ? -1 : a.window_right;
+    long long span_k = a.max_k;
+    if (sp.wl >= 0 && (a.causal || sp.wr >= 0))
+        span_k = std::min<long long>(span_k, (long long)sp.wl + a.max_q + std::max(sp.wr, 0) + kTileN);
+    sp.max_k_eff = (int)span_k;
+    return sp;
+}
+
+Plan plan_for(const FwdArgs &a, const Span &sp, int sms) {
+    const bool uniform = (long long)a.T == (long long)a.B * a.max_q;
+    return make_plan(a.B, a.max_q, sp.max_k_eff, uniform, a.Hq, a.Hkv, a.D, a.q_dtype, a.kv_dtype, sms);
+}
+
+// the kernel parameters every class of a call shares
+FwdParams base_params(const FwdArgs &a, const Span &sp, const DevInfo *dev) {
+    FwdParams p{};
+    p.q = a.q;
+    p.q_stride = a.q_stride;
+    p.k_cache = a.k_cache;
+    p.v_cache = a.v_cache;
+    p.out = a.out;
+    p.out_stride = a.out_stride;
+    p.lse = a.lse;
+    p.cu_seqlens_q = a.cu_seqlens_q;
+    p.seqused_k = a.seqused_k;
+    p.block_table = a.block_table;
+    p.bt_stride = a.bt_stride;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.bs = a.bs;
+    p.num_blocks = a.num_blocks;
+    p.causal = a.causal ? 1 : 0;
+    p.scale_log2 = a.scale * a.q_descale * a.k_descale * 1.4426950408889634f;
+    p.v_descale = a.v_descale;
+    p.err = dev->err;
+    p.window_left = sp.wl;
+    p.window_right = sp.wr;
+    if (a.softcap > 0.f) {
+        p.cap_in = a.scale * a.q_descale * a.k_descale / a.softcap;
+        p.cap_out = a.softcap * 1.4426950408889634f;
+    }
+    p.sinks = a.sinks;
+    return p;
+}
+
+// Launch every class of the plan on `stream`, class k with ns[k] segments.
+// A class writes partial states when it is split or when `partials` is set;
+// p.sched must already point at a zeroed work counter if a tensor-core class
+// is on.
+attn_status launch_classes(const FwdArgs &a, const FwdParams &p, const Plan &pl, const int ns[3], int max_k_eff,
+                           bool partials, const DevInfo *dev, cudaStream_t stream) {
+    const int G = a.Hq / a.Hkv;
+    // every segment spans a whole number of K/V tiles
+    auto chunk_for = [&](int n) {
+        if (n <= 1) return 1 << 30;
+        const int per = (max_k_eff + n - 1) / n;
+        return ((per + kTileN - 1) / kTileN) * kTileN;
+    };
+    const int max_rows = std::max(1, a.max_q) * G;
+    for (int k = 0; k < 3; ++k) {
+        const ClassPlan &c = pl.c[k];
+        if (!c.on) continue;
+        FwdParams t = p;
+        t.nsplit = ns[k];
+        t.partials = (partials || ns[k] > 1) ? 1 : 0;
+        t.split_chunk = chunk_for(ns[k]);
+        t.rows_lo = c.lo;
+        t.rows_hi = c.hi;
+        t.n_row_blocks = (std::min(max_rows, c.hi) + c.rpc - 1) / c.rpc;
+        if ((long long)t.n_row_blocks * ns[k] > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+        attn_status st;
+        if (c.tc && tc2_supported(a.D, a.q_dtype, a.kv_dtype, G))
+            st = check_cuda(launch_fwd_tc2(t, a.q_dtype, a.T, dev->sms, stream));
+        else if (c.tc)
+            st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.kv_dtype, a.T, dev->sms, stream));
+        else
+            st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, c.rpc, a.max_q <= 1, stream));
+        if (st != ATTN_OK) return st;
+    }
+    return ATTN_OK;
+}
+
+// merge the partial states in (part_o, part_lse), part_stride slots per
+// (token, head): a token's count by its class (ns), or every token `all`
+// slots when all > 0
+attn_status launch_combine_for(const FwdArgs &a, const Plan &pl, const int ns[3], int part_stride, float *part_o,
+                               float *part_lse, int all, cudaStream_t stream) {
+    CombineParams c{};
+    c.part_o = part_o;
+    c.part_lse = part_lse;
+    c.out = a.out;
+    c.out_stride = a.out_stride;
+    c.lse = a.lse;
+    c.cu_seqlens_q = a.cu_seqlens_q;
+    c.B = a.B;
+    c.T = a.T;
+    c.Hq = a.Hq;
+    c.D = a.D;
+    c.G = a.Hq / a.Hkv;
+    c.max_q = a.max_q;
+    if (all > 0) {
+        c.rows_hi0 = c.rows_hi1 = INT32_MAX;
+        c.ns0 = c.ns1 = c.ns2 = all;
+    } else {
+        c.rows_hi0 = pl.c[0].hi;
+        c.rows_hi1 = pl.c[1].hi;
+        c.ns0 = ns[0];
+        c.ns1 = ns[1];
+        c.ns2 = ns[2];
+    }
+    c.part_stride = part_stride;
+    return check_cuda(launch_combine(c, a.q_dtype == ATTN_FP8_E4M3 ? ATTN_BF16 : a.q_dtype, stream));
+}
+
 attn_status run_fwd(const FwdArgs &a) {
     attn_status st = validate_fwd(a);
     if (st != ATTN_OK) return st;
@@ -277,18 +402,8 @@ attn_status run_fwd(const FwdArgs &a) {
     st = device_info(&dev);
     if (st != ATTN_OK) return st;
 
-    const bool uniform = (long long)a.T == (long long)a.B * a.max_q;
-    // a window bound at least max_seqlen_k long excludes nothing
-    const int wl = (a.window_left >= a.max_k) ? -1 : a.window_left;
-    const int wr = (a.window_right >= a.max_k) ? -1 : a.window_right;
-    // keys one CTA can see: with a left window bound, at most the window
-    // plus the CTA's query span (and the right bound), from a tile-aligned
-    // start; this sizes the split segments
-    long long span_k = a.max_k;
-    if (wl >= 0 && (a.causal || wr >= 0))
-        span_k = std::min<long long>(span_k, (long long)wl + a.max_q + std::max(wr, 0) + kTileN);
-    const int max_k_eff = (int)span_k;
-    const Plan pl = make_plan(a.B, a.max_q, max_k_eff, uniform, a.Hq, a.Hkv, a.D, a.q_dtype, a.kv_dtype, dev->sms);
+    const Span sp = key_span(a);
+    const Plan pl = plan_for(a, sp, dev->sms);
     int ns[3];
     for (int k = 0; k < 3; ++k)
         ns[k] = !pl.c[k].on ? 1 : (a.num_splits > 0 ? std::min(a.num_splits, kMaxSplits) : pl.c[k].ns);
@@ -311,35 +426,7 @@ attn_status run_fwd(const FwdArgs &a) {
         if (!aligned16(a.ws)) return ATTN_ERR_ALIGN;
     }
 
-    FwdParams p{};
-    p.q = a.q;
-    p.q_stride = a.q_stride;
-    p.k_cache = a.k_cache;
-    p.v_cache = a.v_cache;
-    p.out = a.out;
-    p.out_stride = a.out_stride;
-    p.lse = a.lse;
-    p.cu_seqlens_q = a.cu_seqlens_q;
-    p.seqused_k = a.seqused_k;
-    p.block_table = a.block_table;
-    p.bt_stride = a.bt_stride;
-    p.B = a.B;
-    p.Hq = a.Hq;
-    p.Hkv = a.Hkv;
-    p.G = G;
-    p.bs = a.bs;
-    p.num_blocks = a.num_blocks;
-    p.causal = a.causal ? 1 : 0;
-    p.scale_log2 = a.scale * a.q_descale * a.k_descale * 1.4426950408889634f;
-    p.v_descale = a.v_descale;
-    p.err = dev->err;
-    p.window_left = wl;
-    p.window_right = wr;
-    if (a.softcap > 0.f) {
-        p.cap_in = a.scale * a.q_descale * a.k_descale / a.softcap;
-        p.cap_out = a.softcap * 1.4426950408889634f;
-    }
-    p.sinks = a.sinks;
+    FwdParams p = base_params(a, sp, dev);
     p.part_stride = stride;
     if (stride > 1) {
         char *base = static_cast<char *>(a.ws) + kSchedBytes;
@@ -354,55 +441,159 @@ attn_status run_fwd(const FwdArgs &a) {
         st = check_cuda(cudaMemsetAsync(a.ws, 0, 2 * sizeof(unsigned long long), a.stream));
         if (st != ATTN_OK) return st;
     }
-    // every segment spans a whole number of K/V tiles
-    auto chunk_for = [&](int n) {
-        if (n <= 1) return 1 << 30;
-        const int per = (max_k_eff + n - 1) / n;
-        return ((per + kTileN - 1) / kTileN) * kTileN;
-    };
+    st = launch_classes(a, p, pl, ns, sp.max_k_eff, false, dev, a.stream);
+    if (st != ATTN_OK) return st;
+    if (stride > 1) st = launch_combine_for(a, pl, ns, stride, p.part_o, p.part_lse, 0, a.stream);
+    return st;
+}
 
-    const int max_rows = std::max(1, a.max_q) * G;
-    for (int k = 0; k < 3; ++k) {
-        const ClassPlan &c = pl.c[k];
-        if (!c.on) continue;
-        FwdParams t = p;
-        t.nsplit = ns[k];
-        t.split_chunk = chunk_for(ns[k]);
-        t.rows_lo = c.lo;
-        t.rows_hi = c.hi;
-        t.n_row_blocks = (std::min(max_rows, c.hi) + c.rpc - 1) / c.rpc;
-        if ((long long)t.n_row_blocks * ns[k] > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-        if (c.tc && tc2_supported(a.D, a.q_dtype, a.kv_dtype, G))
-            st = check_cuda(launch_fwd_tc2(t, a.q_dtype, a.T, dev->sms, a.stream));
-        else if (c.tc)
-            st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.kv_dtype, a.T, dev->sms, a.stream));
-        else
-            st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, c.rpc, a.max_q <= 1, a.stream));
+// ---------------------------------------------------------------- cascade
+//
+// "FlashAttention deep dive", Cascade Attention: every query attends to a
+// prefix shared by all requests (one non-causal call over all query tokens)
+// and to its own request's suffix (a causal call), and the two states are
+// merged by log-sum-exp.  Here both halves write their segments' partial
+// states into one array -- the prefix's ns_p segments in slots [0, ns_p) of
+// every (token, head), the suffix's ns_s in [ns_p, ns_p + ns_s) -- and one
+// combine merges them all: three launches where the pages' form takes five
+// (two split calls with their combines, then the merge).  The prefix half
+// runs on a second stream when the caller gives one, so the prefix's
+// tensor-core work and the suffix's cache reads overlap.
+
+// Split counts for the two halves sharing the GPU.  The prefix is
+// compute-heavy (every query x every prefix key), the suffix reads its
+// caches once: each gets a share of the SMs in proportion to its estimated
+// time alone (tensor-core work at 0.6 PFLOP/s -- a prefix spread over few
+// items runs well below the kernel's full-GPU rate -- and cache bytes at
+// 5.5 TB/s), and its segment count fills its share, rounded up for the
+// prefix.  On 64 requests over a 4096-key prefix with suffixes of 256-1024
+// keys this picks (2, 4): 61.7 us against 60.4 us for the best pair
+// measured, (2, 2), and 78 us for the worst, (8, 8).
+constexpr double kCascadeFlops = 0.6e15;
+constexpr double kCascadeBytes = 5.5e12;
+void cascade_splits(const FwdArgs &pre, const FwdArgs &suf, const Plan &pp, const Plan &ps, int sms, int *ns_p,
+                    int *ns_s) {
+    const int G = pre.Hq / pre.Hkv;
+    const double kv_elem = pre.kv_dtype == ATTN_FP8_E4M3 ? 1.0 : 2.0;
+    const double t_p = 4.0 * pre.T * pre.Hq * (double)pre.max_k * pre.D / kCascadeFlops;
+    const double t_s = (double)suf.B * suf.max_k * suf.Hkv * suf.D * 2.0 * kv_elem / kCascadeBytes +
+                       4.0 * suf.T * suf.Hq * (double)suf.max_k * suf.D / kCascadeFlops;
+    const double share = (t_p + t_s) > 0.0 ? t_p / (t_p + t_s) : 0.5;
+    const int sms_p = std::max(2, std::min(sms - 2, (int)(share * sms + 0.5)));
+    const int sms_s = std::max(2, sms - sms_p);
+    // prefix: work units per segment (a pair of SMs per item on the tensor
+    // cores, else about three CTAs an SM)
+    const int rows = std::max(1, pre.T) * G;
+    int units = 0;
+    double per_unit = 1.0;
+    for (int k = 0; k < 3; ++k)
+        if (pp.c[k].on && rows >= pp.c[k].lo && rows <= pp.c[k].hi) {
+            units = ((rows + pp.c[k].rpc - 1) / pp.c[k].rpc) * pre.Hkv;
+            per_unit = pp.c[k].tc ? 2.0 : 1.0 / 3.0;
+        }
+    const int tiles_p = (pre.max_k + kTileN - 1) / kTileN;
+    int np = units > 0 ? (int)std::ceil(sms_p / (per_unit * units)) : 1;
+    np = std::max(1, std::min(np, std::max(1, tiles_p / 4)));
+    *ns_p = std::min(np, kMaxSplits);
+    // suffix: the class-0 rule on its share of the SMs
+    int nsx = 1;
+    for (int k = 0; k < 3; ++k)
+        if (ps.c[k].on) {
+            const int rows_cap = std::min(std::max(1, suf.max_q) * G, ps.c[k].hi);
+            const long long rb = (rows_cap + ps.c[k].rpc - 1) / ps.c[k].rpc;
+            nsx = std::max(nsx, split_rule((long long)suf.B * suf.Hkv * rb, suf.max_k, 6LL * sms_s, 2, 32));
+        }
+    *ns_s = nsx;
+}
+
+struct CascadeArgs {
+    FwdArgs pre, suf;             // the two halves (ws, stream, num_splits unused)
+    int prefix_splits, suffix_splits;
+    void *ws;
+    size_t ws_bytes;
+    cudaStream_t stream, aux;
+};
+
+// host checks of a cascade call; fills the split counts
+attn_status check_cascade(CascadeArgs &c, DevInfo **dev_out) {
+    attn_status st = validate_fwd(c.pre);
+    if (st != ATTN_OK) return st;
+    st = validate_fwd(c.suf);
+    if (st != ATTN_OK) return st;
+    if (c.pre.max_k % c.pre.bs != 0) return ATTN_ERR_SHAPE;   // the suffix starts at a block boundary
+    if (c.prefix_splits < 0 || c.suffix_splits < 0) return ATTN_ERR_SHAPE;
+    return device_info(dev_out);
+}
+
+attn_status run_cascade(CascadeArgs &c) {
+    if (c.suf.B == 0 || c.suf.T == 0) return ATTN_OK;
+    if (!c.ws || !aligned16(c.ws)) return !c.ws ? ATTN_ERR_WORKSPACE : ATTN_ERR_ALIGN;
+    DevInfo *dev = nullptr;
+    attn_status st = check_cascade(c, &dev);
+    if (st != ATTN_OK) return st;
+    if (attn_debug_validate_enabled()) {
+        c.pre.stream = c.suf.stream = c.stream;
+        st = debug_check_fwd(c.pre);
+        if (st == ATTN_OK) st = debug_check_fwd(c.suf);
         if (st != ATTN_OK) return st;
     }
-    if (stride > 1) {
-        CombineParams c{};
-        c.part_o = p.part_o;
-        c.part_lse = p.part_lse;
-        c.out = a.out;
-        c.out_stride = a.out_stride;
-        c.lse = a.lse;
-        c.cu_seqlens_q = a.cu_seqlens_q;
-        c.B = a.B;
-        c.T = a.T;
-        c.Hq = a.Hq;
-        c.D = a.D;
-        c.G = G;
-        c.max_q = a.max_q;
-        c.rows_hi0 = pl.c[0].hi;
-        c.rows_hi1 = pl.c[1].hi;
-        c.ns0 = ns[0];
-        c.ns1 = ns[1];
-        c.ns2 = ns[2];
-        c.part_stride = stride;
-        st = check_cuda(launch_combine(c, a.q_dtype == ATTN_FP8_E4M3 ? ATTN_BF16 : a.q_dtype, a.stream));
+    const Span spp = key_span(c.pre), sps = key_span(c.suf);
+    const Plan pp = plan_for(c.pre, spp, dev->sms), ps = plan_for(c.suf, sps, dev->sms);
+    int ns_p = 1, ns_s = 1;
+    cascade_splits(c.pre, c.suf, pp, ps, dev->sms, &ns_p, &ns_s);
+    if (c.prefix_splits > 0) ns_p = std::min(c.prefix_splits, kMaxSplits);
+    if (c.suffix_splits > 0) ns_s = std::min(c.suffix_splits, kMaxSplits);
+    const int stride = ns_p + ns_s;
+    if (c.ws_bytes < attn_workspace_size(c.suf.T, c.suf.Hq, c.suf.D, stride)) return ATTN_ERR_WORKSPACE;
+
+    char *base = static_cast<char *>(c.ws) + kSchedBytes;
+    float *part_o = reinterpret_cast<float *>(base);
+    float *part_lse = reinterpret_cast<float *>(base + part_o_bytes(c.suf.T, c.suf.Hq, c.suf.D, stride));
+    const int D = c.suf.D;
+    FwdParams fp = base_params(c.pre, spp, dev), fs = base_params(c.suf, sps, dev);
+    fp.part_stride = fs.part_stride = stride;
+    fp.part_o = part_o;                       // prefix segments: slots [0, ns_p)
+    fp.part_lse = part_lse;
+    fs.part_o = part_o + (size_t)ns_p * D;    // suffix segments: slots [ns_p, ns_p + ns_s)
+    fs.part_lse = part_lse + ns_p;
+    // separate work counters (the halves may run at the same time)
+    fp.sched = static_cast<unsigned long long *>(c.ws);
+    fs.sched = static_cast<unsigned long long *>(c.ws) + 2;
+    int nsp[3] = {ns_p, ns_p, ns_p}, nss[3] = {ns_s, ns_s, ns_s};
+
+    // fork: the prefix half on the aux stream after the work already queued
+    // on the main stream; join before the combine.  The two events are this
+    // host thread's own (created on its first cascade call on the device),
+    // recorded and waited on at once, so calls never share an event.
+    const bool fork = c.aux != nullptr && c.aux != c.stream;
+    cudaStream_t sp_stream = fork ? c.aux : c.stream;
+    static thread_local cudaEvent_t tl_ev[kMaxDevices][2];
+    int devno = 0;
+    if (cudaGetDevice(&devno) != cudaSuccess || devno < 0 || devno >= kMaxDevices) return ATTN_ERR_CUDA;
+    cudaEvent_t *ev = tl_ev[devno];
+    if (fork) {
+        for (int i = 0; i < 2; ++i)
+            if (!ev[i] && cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaEventRecord(ev[0], c.stream) != cudaSuccess || cudaStreamWaitEvent(c.aux, ev[0], 0) != cudaSuccess)
+            return ATTN_ERR_CUDA;
     }
-    return st;
+    if (pp.c[2].on) {
+        st = check_cuda(cudaMemsetAsync(fp.sched, 0, 2 * sizeof(unsigned long long), sp_stream));
+        if (st != ATTN_OK) return st;
+    }
+    st = launch_classes(c.pre, fp, pp, nsp, spp.max_k_eff, true, dev, sp_stream);
+    if (st != ATTN_OK) return st;
+    if (ps.c[2].on) {
+        st = check_cuda(cudaMemsetAsync(fs.sched, 0, 2 * sizeof(unsigned long long), c.stream));
+        if (st != ATTN_OK) return st;
+    }
+    st = launch_classes(c.suf, fs, ps, nss, sps.max_k_eff, true, dev, c.stream);
+    if (st != ATTN_OK) return st;
+    if (fork) {
+        if (cudaEventRecord(ev[1], c.aux) != cudaSuccess || cudaStreamWaitEvent(c.stream, ev[1], 0) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    return launch_combine_for(c.suf, ps, nss, stride, part_o, part_lse, stride, c.stream);
 }
 
 }  // namespace
@@ -564,6 +755,96 @@ attn_status attn_paged_decode(const void *q, const void *k_cache, const void *v_
     a.ws_bytes = ws_bytes;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     return run_fwd(a);
+}
+
+static void fill_cascade(CascadeArgs &c, const void *q, int64_t q_stride_tok, const void *k_cache,
+                         const void *v_cache, void *out, int64_t out_stride_tok, float *lse_out,
+                         const int32_t *cu_prefix_query_lens, const int32_t *prefix_kv_lens,
+                         const int32_t *prefix_block_table, int prefix_len, const int32_t *cu_seqlens_q,
+                         const int32_t *suffix_kv_lens, const int32_t *suffix_block_table, int64_t bt_row_stride,
+                         int B, int total_q, int max_seqlen_q, int max_suffix_len, int Hq, int Hkv, int D,
+                         int block_size, int num_blocks, attn_dtype q_dtype, attn_dtype kv_dtype, float softmax_scale,
+                         float k_descale, float v_descale) {
+    for (int h = 0; h < 2; ++h) {
+        FwdArgs &a = h ? c.suf : c.pre;
+        a.q = q;
+        a.q_stride = q_stride_tok;
+        a.k_cache = k_cache;
+        a.v_cache = v_cache;
+        a.out = out;
+        a.out_stride = out_stride_tok;
+        a.lse = lse_out;
+        a.T = total_q;
+        a.Hq = Hq;
+        a.Hkv = Hkv;
+        a.D = D;
+        a.bs = block_size;
+        a.num_blocks = num_blocks;
+        a.q_dtype = q_dtype;
+        a.kv_dtype = kv_dtype;
+        a.scale = softmax_scale;
+        a.k_descale = k_descale;
+        a.v_descale = v_descale;
+    }
+    // prefix: one "request" holding every query token, non-causal (all prefix
+    // keys precede every query), over the shared block row
+    c.pre.cu_seqlens_q = cu_prefix_query_lens;
+    c.pre.seqused_k = prefix_kv_lens;
+    c.pre.block_table = prefix_block_table;
+    c.pre.bt_stride = 0;
+    c.pre.B = 1;
+    c.pre.max_q = total_q;
+    c.pre.max_k = prefix_len;
+    c.pre.causal = 0;
+    // suffix: each request over its own blocks, causal with bottom-right alignment
+    c.suf.cu_seqlens_q = cu_seqlens_q;
+    c.suf.seqused_k = suffix_kv_lens;
+    c.suf.block_table = suffix_block_table;
+    c.suf.bt_stride = bt_row_stride;
+    c.suf.B = B;
+    c.suf.max_q = max_seqlen_q;
+    c.suf.max_k = max_suffix_len;
+    c.suf.causal = 1;
+}
+
+attn_status attn_cascade(const void *q, int64_t q_stride_tok, const void *k_cache, const void *v_cache, void *out,
+                         int64_t out_stride_tok, float *lse_out, const int32_t *cu_prefix_query_lens,
+                         const int32_t *prefix_kv_lens, const int32_t *prefix_block_table, int prefix_len,
+                         const int32_t *cu_seqlens_q, const int32_t *suffix_kv_lens,
+                         const int32_t *suffix_block_table, int64_t bt_row_stride, int B, int total_q,
+                         int max_seqlen_q, int max_suffix_len, int Hq, int Hkv, int D, int block_size,
+                         int num_blocks, attn_dtype q_dtype, attn_dtype kv_dtype, float softmax_scale,
+                         float k_descale, float v_descale, int prefix_splits, int suffix_splits, void *workspace,
+                         size_t ws_bytes, attn_stream_t stream, attn_stream_t aux_stream) {
+    if (B > 0 && (!cu_seqlens_q || !cu_prefix_query_lens || !prefix_kv_lens)) return ATTN_ERR_NULL;
+    if (q_dtype == ATTN_FP8_E4M3) return ATTN_ERR_DTYPE;   // no q_descale in this entry point
+    CascadeArgs c{};
+    fill_cascade(c, q, q_stride_tok, k_cache, v_cache, out, out_stride_tok, lse_out, cu_prefix_query_lens,
+                 prefix_kv_lens, prefix_block_table, prefix_len, cu_seqlens_q, suffix_kv_lens, suffix_block_table,
+                 bt_row_stride, B, total_q, max_seqlen_q, max_suffix_len, Hq, Hkv, D, block_size, num_blocks,
+                 q_dtype, kv_dtype, softmax_scale, k_descale, v_descale);
+    c.prefix_splits = prefix_splits;
+    c.suffix_splits = suffix_splits;
+    c.ws = workspace;
+    c.ws_bytes = ws_bytes;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    c.aux = reinterpret_cast<cudaStream_t>(aux_stream);
+    return run_cascade(c);
+}
+
+int attn_cascade_splits(int B, int total_q, int max_seqlen_q, int prefix_len, int max_suffix_len, int Hq, int Hkv,
+                        int D, int q_dtype, int kv_dtype, int num_sms, int *prefix_splits, int *suffix_splits) {
+    if (B <= 0 || total_q <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_sms <= 0 || !prefix_splits ||
+        !suffix_splits)
+        return -1;
+    CascadeArgs c{};
+    fill_cascade(c, nullptr, 0, nullptr, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, prefix_len, nullptr,
+                 nullptr, nullptr, 0, B, total_q, max_seqlen_q, max_suffix_len, Hq, Hkv, D, 16, 1,
+                 (attn_dtype)q_dtype, (attn_dtype)kv_dtype, 1.f, 1.f, 1.f);
+    const Span spp = key_span(c.pre), sps = key_span(c.suf);
+    const Plan pp = plan_for(c.pre, spp, num_sms), ps = plan_for(c.suf, sps, num_sms);
+    cascade_splits(c.pre, c.suf, pp, ps, num_sms, prefix_splits, suffix_splits);
+    return 0;
 }
 
 attn_status attn_merge_states(void *out, float *lse_out, const void *o1, const float *lse1, const void *o2,

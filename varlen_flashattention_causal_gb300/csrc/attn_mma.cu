@@ -24,7 +24,7 @@
 // WN = 4 (decode shapes) each warp also fetches exactly its own keys, so the
 // warps stream their slices independently, synchronising only at the start
 // (Q) and at the end (the merge); with
-// nsplit > 1 each CTA writes a normalised partial state that the combine
+// partials (nsplit > 1) each CTA writes a normalised partial state that the combine
 // kernel merges by log-sum-exp (sec. 12).
 #include <type_traits>
 
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(128, C::MIN_BLOCKS) fwd_mma_kernel(const FwdPa
             const int64_t tok = q_start + pr / G;
             const int h = kvh * G + pr % G;
             const float zl = (p.sinks && s_idx == 0) ? p.sinks[h] : -INFINITY;
-            if (p.nsplit > 1) {
+            if (p.partials) {
                 const int64_t slot = (tok * p.Hq + h) * p.part_stride + s_idx;
                 p.part_lse[slot] = zl;
                 if (zl != -INFINITY)
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(128, C::MIN_BLOCKS) fwd_mma_kernel(const FwdPa
         acc.z *= inv;
         acc.w *= inv;
         const float lse_v = lf > 0.f ? (mf + __log2f(lf)) * 0.6931471805599453f : -INFINITY;
-        if (p.nsplit == 1) {
+        if (!p.partials) {
             using OT = typename C::OutT;
             OT *dst = reinterpret_cast<OT *>(p.out) + tok * p.out_stride + (int64_t)h * D + c4 * 4;
             uint2 pk;

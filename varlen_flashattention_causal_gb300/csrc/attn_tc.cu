@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(TcLayout<FP8, Q8>::kThreads, 1)
                     const int64_t tok = it.q_start + pr / G;
                     const int h = it.kvh * G + pr % G;
                     const float zl = (p.sinks && it.s == 0) ? p.sinks[h] : -INFINITY;
-                    if (p.nsplit > 1) {
+                    if (p.partials) {
                         const int64_t slot = (tok * p.Hq + h) * p.part_stride + it.s;
                         p.part_lse[slot] = zl;
                         if (zl != -INFINITY)
@@ -789,7 +789,7 @@ __global__ void __launch_bounds__(TcLayout<FP8, Q8>::kThreads, 1)
                         tmem_ld32(tO + c * 32, o);
                         tmem_wait_ld();
                         if (!row_ok) continue;
-                        if (p.nsplit == 1) {
+                        if (!p.partials) {
                             uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
                                                                    (tok * p.out_stride + (int64_t)h * kD + c * 32) * 2);
 #pragma unroll
@@ -817,7 +817,7 @@ __global__ void __launch_bounds__(TcLayout<FP8, Q8>::kThreads, 1)
                         }
                     }
                     if (row_ok) {
-                        if (p.nsplit == 1) {
+                        if (!p.partials) {
                             if (p.lse) p.lse[tok * p.Hq + h] = lse_v;
                         } else {
                             p.part_lse[(tok * p.Hq + h) * p.part_stride + it.s] = lse_v;

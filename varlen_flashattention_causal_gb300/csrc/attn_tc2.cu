@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const int64_t tok = it.q_start + prow / G;
                     const int h = it.kvh * G + prow % G;
                     const float zl = (p.sinks && it.s == 0) ? p.sinks[h] : -INFINITY;
-                    if (p.nsplit > 1) {
+                    if (p.partials) {
                         const int64_t slot = (tok * p.Hq + h) * p.part_stride + it.s;
                         p.part_lse[slot] = zl;
                         if (zl != -INFINITY)
@@ -755,7 +755,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     tmem_wait_ld();
                     if (!row_ok) continue;
                     const int d0 = 64 * sg + c * 32;
-                    if (p.nsplit == 1) {
+                    if (!p.partials) {
                         uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
                                                                (tok * p.out_stride + (int64_t)h * kPD + d0) * 2);
 #pragma unroll
@@ -778,7 +778,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     }
                 }
                 if (row_ok && sg == 0) {
-                    if (p.nsplit == 1) {
+                    if (!p.partials) {
                         if (p.lse) p.lse[tok * p.Hq + h] = lse_v;
                     } else {
                         p.part_lse[(tok * p.Hq + h) * p.part_stride + it.s] = lse_v;

@@ -36,8 +36,10 @@ struct FwdParams {
     int nsplit;                  // KV segments per (request, KV head, row block)
     int split_chunk;             // keys per segment (multiple of the KV tile)
     int part_stride;             // segment slots per (token, head) in the workspace
-    float *part_o;               // [T, Hq, part_stride, D] fp32 (used when nsplit > 1)
+    float *part_o;               // [T, Hq, part_stride, D] fp32, segment s at slot s
     float *part_lse;             // [T, Hq, part_stride]
+    int partials;                // 1: write normalised partial states there instead of
+                                 // out / lse (split-KV, and both halves of a cascade call)
     int rows_lo, rows_hi;
     int n_row_blocks;            // row blocks of the largest request of the class
     unsigned *err;
