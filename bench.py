@@ -56,15 +56,15 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# the decode split kernel on this workload, from one `ncu --set full` capture
-# (its summary under profiles/ gives the command).  It is reported only while
+# the decode split kernel on this workload, from one ncu capture of those
+# metrics (its summary under profiles/ gives the command).  It is reported only while
 # the kernel's sources hash to the value recorded with the capture.
 DECODE_TRAFFIC = {
-    "bytes": 593427456 + 5427968,        # dram__bytes_read.sum + dram__bytes_write.sum, 4 segments
+    "bytes": 593427200 + 5125632,        # dram__bytes_read.sum + dram__bytes_write.sum, 4 segments
     "sources": ["varlen_flashattention_causal_gb300/csrc/attn_mma.cu",
                 "varlen_flashattention_causal_gb300/csrc/common.cuh",
                 "varlen_flashattention_causal_gb300/csrc/internal.h"],
-    "sha256": "99f0d6d6ddab0a8ffc5c1d885e2aaf85ee5772c5c0319e47f97188fa6e48fd5e",
+    "sha256": "bfd111e623f86482ab14900351548b673fbff41757c8667eeacdae9828570694",
 }
 
 
