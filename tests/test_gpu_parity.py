@@ -751,6 +751,51 @@ def test_cascade_entry_point_against_oracle():
     assert_no_device_error()
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_cascade_entry_point_other_shapes(kv_dtype):
+    """attn_cascade beyond decode: suffixes of several query tokens (one
+    request above 64 packed rows, so the suffix half also runs a tensor-core
+    class beside the prefix half's), on a bf16 or e4m3 cache, and an empty
+    prefix (prefix_len 0: the prefix half contributes no key)."""
+    bs = 32
+    P = 4 * bs
+    q_lens = [1, 3, 40, 7]
+    suf = [50, 3, 300, 20]
+    kv = [P + s for s in suf]
+    g = W.generator(171)
+    npre = P // bs
+    used = npre + sum((L + bs - 1) // bs - npre for L in kv)
+    bt = W.block_tables(kv, bs, used + 8, g, shared_prefix_blocks=npre)
+    b = W.Batch("cascade-shapes", 32, 8, 128, bs, used + 8, q_lens, kv, block_table=bt, kv_dtype=kv_dtype)
+    # the shared prefix's keys are written once (row 0), each suffix's per row
+    b = W._finish(b, g, "cpu", [range(L) if r == 0 else range(P, L) for r, L in enumerate(kv)])
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    ro, rl = ref_attn(b, ck, cv)
+    tol = TOL_FP8 if kv_dtype == "fp8" else TOL
+    T, Hq, D = b.q.shape
+    q, btd = b.q.cuda(), b.block_table.cuda()
+    cu = b.cu_seqlens_q.cuda()
+    kd = b.k_scale if kv_dtype == "fp8" else 1.0
+    vd = b.v_scale if kv_dtype == "fp8" else 1.0
+    for pl in (P, 0):
+        nb = pl // bs
+        cu0 = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+        pk = torch.tensor([pl], dtype=torch.int32, device="cuda")
+        su = (b.seqused_k - pl).cuda()
+        for nsp, nss in ((0, 0), (2, 3)):
+            auto = va.attn_cascade_splits(b.B, T, max(q_lens), pl, max(kv) - pl, Hq, b.Hkv, D,
+                                          q_dtype=va.ATTN_BF16, kv_dtype=va.ATTN_FP8_E4M3 if kv_dtype == "fp8" else va.ATTN_BF16)
+            tot = (nsp or auto[0]) + (nss or auto[1])
+            g = Guarded(T, Hq, D, b.q.dtype, va.attn_workspace_size(T, Hq, D, tot))
+            va.attn_cascade(q, kc, vc, g.out, cu0, pk, btd[0], pl, cu, su, btd[:, nb:], max(q_lens), max(kv) - pl,
+                            b.softmax_scale, lse_out=g.lse, k_descale=kd, v_descale=vd, prefix_splits=nsp,
+                            suffix_splits=nss, workspace=g.ws, aux_stream=torch.cuda.Stream())
+            g.verify()
+            check(g.out, g.lse, ro, rl, tol)
+    assert_no_device_error()
+
+
 def test_workload4_fp8_mixed_full_sampled():
     b = W.fp8_mixed()
     kc, vc = gpu_cache(b)
