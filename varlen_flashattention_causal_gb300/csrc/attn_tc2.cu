@@ -26,19 +26,22 @@
 // 并行处理多个请求" sec. 10, only on tiles that are not full (sec. 4); O is
 // rescaled only when a row's maximum grows by more than 2^8.
 //
-// Roles (6 warps in each CTA of the pair):
+// Roles (12 warps in each CTA of the pair):
 //   warp 0      even CTA: scheduler (publishes every item to both CTAs'
 //               two-entry rings) and TMA producer of its halves; odd CTA:
 //               reads the items and loads its halves
 //   warp 1      both: TMEM allocation for the pair; even CTA: issues S = Q K^T
-//               (one thread); odd CTA: forwards the completion of each of its
-//               loads (Q and every K/V slot) to a barrier of the even CTA, so
-//               the issuers know both halves have landed
+//               (one thread); odd CTA: forwards the completion of its Q and K
+//               loads to barriers of the even CTA, so the S issuer knows both
+//               halves have landed
 //   warp 10     even CTA: issues O += P V (one thread).  Two issuing warps:
 //               a warp issuing tcgen05 MMAs is held about 100 cycles per MMA,
 //               more than an M = 256 MMA takes, so one issuer would starve
 //               the tensor core; S(j) may run ahead of O += P(j-1) V, and
 //               the S buffer of tile j is reused once O += P(j-3) V is done
+//   warp 11     both: V gate -- waits for each of the CTA's V halves, zeroes
+//               its rows past the segment end on a segment's last tile, and
+//               reports the half ready to the even CTA's P V issuer
 //   warps 2-9   softmax and epilogue of the CTA's own 128 rows in two
 //               groups: warps 2-5 take keys 0-63 of every tile and head dims
 //               0-63 of O, warps 6-9 keys 64-127 and dims 64-127, one thread
@@ -76,9 +79,9 @@ constexpr uint32_t kPOffBar = kPOffKV + kPSlots * kPSlot;
 constexpr uint32_t kPOffMisc = kPOffBar + 8 * 64;
 constexpr uint32_t kPOffX = kPOffMisc + 128;           // softmax exchange: row maxima, row sums
 constexpr uint32_t kPSmem = kPOffX + 3 * 1024 + 1024;    // + alignment slack
-constexpr int kPThreads = 352;
-constexpr int kPConsumersEven = 10;                     // warps 1-10 read the item ring
-constexpr int kPConsumersOdd = 10;                      // warps 0-9
+constexpr int kPThreads = 384;
+constexpr int kPConsumersEven = 11;                     // warps 1-11 read the item ring
+constexpr int kPConsumersOdd = 11;                      // warps 0-9 and 11
 constexpr float kPRescale = 8.0f;                       // log2 units
 constexpr uint16_t kPairMask = 3;
 static_assert(kPSmem <= 232448, "shared memory per CTA");
@@ -172,7 +175,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
     auto BQ = [](int q) { return q ? kB3 + 10 : B_Q; };       // own Q buffer q landed (TMA)
     auto BPQ = [](int q) { return q ? kB3 + 11 : B_PQ; };     // even: the odd CTA's Q buffer q landed
     auto BQFREE = [](int q) { return q ? kB3 + 12 : B_QFREE; };   // S MMAs done with Q buffer q (commit, both)
-    constexpr int kNumBars = kB3 + 13;
+    // per K/V slot s holding a V half: both CTAs' halves landed (and, on a
+    // segment's last tile, zeroed past its end) -- one arrival from each
+    // CTA's V gate warp on the even CTA's copy
+    auto B_VREADY = [](int s) { return kB3 + 13 + s; };
+    constexpr int kNumBars = kB3 + 13 + kPSlots;
     static_assert(kNumBars <= 64, "barrier area");
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kPOffMisc);
     uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(sm + kPOffMisc + 8);
@@ -215,6 +222,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_init(bar(BQFREE(1)), 1);
         mbar_init(bar(B_QFREE), 1);
         mbar_init(bar(B_DRAIN), 2);
+        for (int s = 0; s < kPSlots; ++s) mbar_init(bar(B_VREADY(s)), 2);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -488,8 +496,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const int LV = Lbase + 2 * j + 1;    // load index of V_j
                     const int jg = jx + j;
                     const int sv = LV % kPSlots;
-                    ok = mbar_wait(bar(B_FULL(sv)), (LV / kPSlots) & 1, abort_flag);
-                    if (ok) ok = mbar_wait(bar(B_PFULLS(sv)), (LV / kPSlots) & 1, abort_flag);
+                    // V_j: both CTAs' halves landed and tail-zeroed (V gate warps)
+                    ok = mbar_wait_cl(bar(B_VREADY(sv)), (LV / kPSlots) & 1, abort_flag);
                     if (ok) ok = mbar_wait(bar(B_PFULL(jg % kPSBufs)), (jg / kPSBufs) & 1, abort_flag);
                     // the item's first P V overwrites O: both CTAs must have read
                     // the previous item's O out
@@ -526,7 +534,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (lane == 0) {
                 ok = mbar_wait(bar(BQ(npipe & 1)), (npipe >> 1) & 1, abort_flag);
                 if (ok) mbar_arrive_cluster(even_bar(BPQ(npipe & 1)));
-                for (int L = Lbase; L < Lbase + 2 * it.n_kv && ok; ++L) {
+                // (K loads only: the V gate warps report the V halves)
+                for (int L = Lbase; L < Lbase + 2 * it.n_kv && ok; L += 2) {
                     ok = mbar_wait(bar(B_FULL(L % kPSlots)), (L / kPSlots) & 1, abort_flag);
                     if (ok) mbar_arrive_cluster(even_bar(B_PFULLS(L % kPSlots)));
                 }
@@ -536,6 +545,47 @@ __global__ void __launch_bounds__(kPThreads, 1)
             ++npipe;
         }
         if (lane == 0) mbar_wait(bar(B_DRAIN), 0, never);
+    } else if (warp == 11) {
+        // ============ V gate (both CTAs): each V half of the CTA, once it has
+        // landed; on a segment's last tile its rows past the segment end are
+        // zeroed first (P is exactly 0 there, but the rows may hold anything --
+        // unwritten cache rows, pages not loaded -- and 0 * NaN is NaN).  Both
+        // SMs' tensor cores read the half, the peer's through the cluster, so
+        // zeroed rows are published with a proxy fence over all state spaces and
+        // cluster-scope ordering (a CTA-scope proxy fence measurably left the
+        // peer reading stale rows now and then).  The gate then arrives on the
+        // even CTA's B_VREADY, which the P V issuer waits for in place of the
+        // load completions.  Off the softmax's path, the fences cost little.
+        int Lbase = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            PItem it;
+            ok = read_item(k, it);
+            if (!ok || it.r < 0) break;
+            if (it.n_kv == 0) continue;
+            for (int j = 0; j < it.n_kv && ok; ++j) {
+                const int L = Lbase + 2 * j + 1;          // load index of V_j
+                const int sv = L % kPSlots;
+                ok = pwarp_wait(bar(B_FULL(sv)), (L / kPSlots) & 1, abort_flag);
+                if (!ok) break;
+                const int nvalid = it.kv_hi - (it.kv_lo + j * kPN);   // keys of the tile in the segment
+                if (nvalid < kPN) {
+                    uint4 *half = reinterpret_cast<uint4 *>(sm + kPOffKV + sv * kPSlot);
+                    for (int i = nvalid * 8 + lane; i < kPN * 8; i += 32) half[i] = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_all();
+                    fence_acq_rel_cluster();
+                    __syncwarp();
+                    if (lane == 0) {
+                        fence_acq_rel_cluster();
+                        mbar_arrive_cluster_release(even_bar(B_VREADY(sv)));
+                    }
+                } else {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_release(even_bar(B_VREADY(sv)));
+                }
+            }
+            Lbase += 2 * it.n_kv;
+        }
     } else if (warp >= 2 && warp <= 9) {
         // ============ softmax and epilogue (own rows), in two groups of columns
         const int sg = (warp - 2) >> 2;             // 0: keys / dims 0-63, 1: 64-127
@@ -685,30 +735,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tmem_st32(tO + c * 32, o);
                     }
-                }
-                if (n0 + kPN > kv_hi) {
-                    // keys past the segment end: P is exactly 0 there, but this
-                    // CTA's V rows may hold anything (unwritten cache rows, pages
-                    // not loaded) -- zero them so 0 * V cannot produce NaN, after
-                    // the half has landed and before P is published (each group
-                    // zeroes half of every such row)
-                    const int Lv = Lbase + 2 * j + 1;
-                    const int sv = Lv % kPSlots;
-                    ok = pwarp_wait(bar(B_FULL(sv)), (Lv / kPSlots) & 1, abort_flag);
-                    if (!ok) break;
-                    __syncwarp();
-                    if (trow >= kv_hi - n0) {
-                        uint4 *vr = reinterpret_cast<uint4 *>(sm + kPOffKV + sv * kPSlot + trow * 128) + 4 * sg;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) vr[c] = make_uint4(0, 0, 0, 0);
-                    }
-                    // both SMs' tensor cores read this CTA's V half, the peer's
-                    // through the cluster: a CTA-scope proxy fence is not enough
-                    // for that (measured: a stand-alone converter writing the
-                    // whole half this way was read stale now and then by the peer
-                    // until it fenced all proxies and ordered at cluster scope)
-                    fence_proxy_async_all();
-                    fence_acq_rel_cluster();
                 }
                 // P -> TMEM over the S buffer it came from (packed columns
                 // 32 sg .. 32 sg + 31: this group's 64 keys)
