@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     auto B_ITEMF = [](int i) { return kB3 + 2 + i; };         // ring entry i written (both)
     auto B_ITEME = [](int i) { return kB3 + 4 + i; };         // even: entry i read by every consumer warp
     constexpr int B_DRAIN = kB3 + 6;                          // both issuers' MMAs are done (commits, both)
-    auto B_XMAX = [](int i) { return kB3 + 7 + i; };          // both softmax groups posted tile maxima (8 warps)
+    // the two softmax warps of TMEM lane quarter q (one per group, the same
+    // rows) posted their tile maxima, by tile parity i
+    auto B_XMAX = [](int i, int q) { return kB3 + 13 + kPSlots + 4 * i + q; };
     constexpr int B_XSUM = kB3 + 9;                           // both groups posted row sums (8 warps)
     // Q is double-buffered (buffer = parity of the item's index among items
     // with keys): the next item's Q loads while the current item's S MMAs run
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // segment's last tile, zeroed past its end) -- one arrival from each
     // CTA's V gate warp on the even CTA's copy
     auto B_VREADY = [](int s) { return kB3 + 13 + s; };
-    constexpr int kNumBars = kB3 + 13 + kPSlots;
+    constexpr int kNumBars = kB3 + 13 + kPSlots + 8;
     static_assert(kNumBars <= 64, "barrier area");
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kPOffMisc);
     uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(sm + kPOffMisc + 8);
@@ -214,8 +216,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(bar(B_ITEME(i)), (uint32_t)(kPConsumersEven + kPConsumersOdd));
         }
         mbar_init(bar(B_OFREE), 16);
-        mbar_init(bar(B_XMAX(0)), 8);
-        mbar_init(bar(B_XMAX(1)), 8);
+        for (int i = 0; i < 8; ++i) mbar_init(bar(B_XMAX(i >> 2, i & 3)), 2);
         mbar_init(bar(B_XSUM), 8);
         mbar_init(bar(BQ(1)), 1);
         mbar_init(bar(BPQ(1)), 1);
@@ -692,8 +693,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const float mxl = pfmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
                 xmax[((jg & 1) * 2 + sg) * kPM + trow] = mxl;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_XMAX(jg & 1)));
-                ok = pwarp_wait(bar(B_XMAX(jg & 1)), (jg >> 1) & 1, abort_flag);
+                if (lane == 0) mbar_arrive(bar(B_XMAX(jg & 1, quarter)));
+                ok = pwarp_wait(bar(B_XMAX(jg & 1, quarter)), (jg >> 1) & 1, abort_flag);
                 if (!ok) break;
                 const float mx = fmaxf(mxl, xmax[((jg & 1) * 2 + (sg ^ 1)) * kPM + trow]) * sl2;
                 const bool bump = mx > m_ref + kPRescale;
