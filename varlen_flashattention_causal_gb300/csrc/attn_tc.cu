@@ -1,9 +1,10 @@
 // attn_tc.cu -- varlen causal attention over a paged KV cache on the
 // Blackwell tensor cores (tcgen05 MMAs, accumulators in TMEM, TMA loads).
 //
-// This kernel takes the rows-heavy side of the hot path: prefill and
-// chunked prefill, where S = Q K^T and O = P V are genuine dense
-// contractions.  A work item is one request x one KV head x 256 packed
+// This kernel takes the rows-heavy side of the hot path over e4m3 caches:
+// prefill and chunked prefill, where S = Q K^T and O = P V are genuine dense
+// contractions.  (16-bit caches run on pairs of SMs, attn_tc2.cu; the
+// template's 16-bit form is not instantiated.)  A work item is one request x one KV head x 256 packed
 // query rows (two 128-row Q tiles; a row is a (query token, head-in-group)
 // pair, so each K/V tile serves all G query heads of its group) x one KV
 // segment.
@@ -1000,8 +1001,9 @@ cudaError_t launch_fwd_tc(const FwdParams &f, int q_dtype, int kv_dtype, int64_t
         return q16 ? launch_tc<false, false, true>(tp, qmap, kmap, vmap, grid, stream)
                    : launch_tc<false, true, true>(tp, qmap, kmap, vmap, grid, stream);
     }
-    return q16 ? launch_tc<false, false, false>(tp, qmap, kmap, vmap, grid, stream)
-               : launch_tc<true, true, false>(tp, qmap, kmap, vmap, grid, stream);
+    // 16-bit caches run on fwd_tc2_kernel (tc2_supported covers every shape
+    // this kernel would take)
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace attn
