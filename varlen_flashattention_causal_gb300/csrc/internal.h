@@ -118,9 +118,7 @@ __host__ __device__ inline int tile_kind(int q_lo, int q_hi, int k_lo, int k_hi,
 // rows per CTA of the mma kernel for a given largest packed row count
 int mma_rows_per_cta(int max_rows);
 
-// tcgen05 kernels: whether one of them takes this shape (16-bit caches:
-// fwd_tc2_kernel on pairs of SMs; e4m3 caches: fwd_tc_kernel), rows per
-// work item, launchers
+// tcgen05 kernel: whether it handles this shape, rows per CTA, launcher
 bool tc_supported(int D, int q_dtype, int kv_dtype, int G);
 int tc_rows_per_cta();
 // (persistent: at most num_sms CTAs)
