@@ -64,8 +64,7 @@ struct MmaCfg {
     // quad t covers dims 32t + 4kk .. 32t + 4kk + 3, the same order for the
     // Q fragments, so Q K^T is unchanged -- which makes a lane's B
     // fragments of all eight k-steps 32 contiguous bytes of its key row,
-    // widened in registers.  V still goes through shared memory (its
-    // fragments run along keys, which are rows of the cache).
+    // widened in registers.  V takes the same route under VDIRECT below.
     static constexpr bool KDIRECT = (KVT == DT_E4M3) && WARP_LOCAL && D == 128 && QT != DT_E4M3;
     // e4m3 queries: Q K^T on e4m3 operands (m16n8k32), the K fragments
     // read straight from the staged bytes with no widening, in the same
@@ -73,16 +72,26 @@ struct MmaCfg {
     // 32t + 8kk .. 32t + 8kk + 7); output in bf16
     static constexpr bool Q8 = (QT == DT_E4M3);
     static constexpr bool STAGE_SWZ = KDIRECT || Q8;   // staged e4m3 rows chunk-swizzled
+    // e4m3 V fragments straight from the staged bytes too (decode shape, D
+    // 128, the warp's own 16 keys): the head dimension of P V's output is
+    // read in a permuted order -- n8 tile j of lane (g, t) covers dims 16n + j
+    // (n = g for V, n = 2t, 2t + 1 for O) -- so a lane's B fragments of all
+    // sixteen n8 tiles are bytes 16g .. 16g + 15 of its four key rows (one
+    // 16-byte load each), paired by key and widened in registers; the
+    // epilogue writes O back in the natural order.  No fp16 V tile, no
+    // ldmatrix, and no CTA-wide widening pass.
+    static constexpr bool VDIRECT = (KVT == DT_E4M3) && WARP_LOCAL && D == 128 && (KDIRECT || Q8);
     static_assert(!Q8 || (KVT == DT_E4M3 && D == 128), "e4m3 queries need an e4m3 cache and head size 128");
-    // e4m3: widened fp16 tiles (V only with KDIRECT) after the staging ring
-    static constexpr int CONV_BYTES = (KVT == DT_E4M3) ? ((KDIRECT || Q8) ? TILE16 : 2 * TILE16) : 0;
+    // e4m3: widened fp16 tiles after the staging ring (K and V; V only with
+    // KDIRECT or Q8; none with VDIRECT)
+    static constexpr int CONV_BYTES = (KVT == DT_E4M3) ? (VDIRECT ? 0 : (KDIRECT || Q8) ? TILE16 : 2 * TILE16) : 0;
     static constexpr int OSTRIDE = D + 4;                // fp32 epilogue row stride (bank spread)
     static constexpr int EPI_BYTES = WN * ROWS * OSTRIDE * 4 + 2 * WN * ROWS * 4;
     static constexpr int MAIN_BYTES = STAGES * STAGE_BYTES + CONV_BYTES;
     static constexpr int SMEM = Q_BYTES + (MAIN_BYTES > EPI_BYTES ? MAIN_BYTES : EPI_BYTES);
     // decode shape with two stages: more CTAs per SM instead of a deeper
-    // ring -- e4m3 cache: 52 KB and at most 128 registers a thread, four CTAs
-    // (three with three stages); 16-bit cache: 68 KB and at most 168
+    // ring -- e4m3 cache: 38 KB (52 KB with a widened V tile) and at most
+    // 128 registers a thread, four CTAs; 16-bit cache: 68 KB and at most 168
     // registers, three CTAs (two with three stages, at 100 KB)
     static constexpr int MIN_BLOCKS = (WARP_LOCAL && STAGES == 2) ? (KVT == DT_E4M3 ? 4 : 3) : 1;
     static_assert(WM * WN == 4, "4 warps");
@@ -368,7 +377,12 @@ __global__ void __launch_bounds__(128, C::MIN_BLOCKS) fwd_mma_kernel(const FwdPa
             cp_async_commit();
         }
         const uint8_t *tK, *tV;
-        if constexpr (C::KVT == DT_E4M3) {
+        if constexpr (C::VDIRECT) {
+            // nothing to widen into shared memory: K and V fragments come
+            // straight from the staged bytes
+            tK = nullptr;
+            tV = sMain + (t % STAGES) * C::STAGE_BYTES + C::TILE_RAW;
+        } else if constexpr (C::KVT == DT_E4M3) {
             convert_tile(t % STAGES);
             tile_sync();
             tK = cK;
@@ -515,14 +529,43 @@ __global__ void __launch_bounds__(128, C::MIN_BLOCKS) fwd_mma_kernel(const FwdPa
             a[1] = pack2<C::MMA_BF16>(s[2 * kk][2], s[2 * kk][3]);
             a[2] = pack2<C::MMA_BF16>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
             a[3] = pack2<C::MMA_BF16>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+            if constexpr (C::VDIRECT) {
+                // keys 2t, 2t + 1, 2t + 8, 2t + 9 of the warp's 16, dims 16g .. 16g + 15
+                const int g = lane >> 2, t4 = lane & 3;
+                const int kb = wn * C::NW + kk * 16 + 2 * t4;
 #pragma unroll
-            for (int j = 0; j < D / 16; ++j) {
-                const int key = wn * C::NW + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int ch = 2 * j + (lane >> 4);
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(b0, b1, b2, b3, smem_u32(tV + swz(key, ch, C::ROW16)));
-                mma16816<C::MMA_BF16>(o[2 * j], a, b0, b1);
-                mma16816<C::MMA_BF16>(o[2 * j + 1], a, b2, b3);
+                for (int h = 0; h < 2; ++h) {
+                    // one half of the 16 bytes at a time (register pressure)
+                    const uint2 r0 = *reinterpret_cast<const uint2 *>(tV + stage8(kb, g) + 8 * h);
+                    const uint2 r1 = *reinterpret_cast<const uint2 *>(tV + stage8(kb + 1, g) + 8 * h);
+                    const uint2 r2 = *reinterpret_cast<const uint2 *>(tV + stage8(kb + 8, g) + 8 * h);
+                    const uint2 r3 = *reinterpret_cast<const uint2 *>(tV + stage8(kb + 9, g) + 8 * h);
+                    const uint32_t w0[2] = {r0.x, r0.y}, w1[2] = {r1.x, r1.y};
+                    const uint32_t w2[2] = {r2.x, r2.y}, w3[2] = {r3.x, r3.y};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        // n8 tile 4w + i (w = 2h + e): dims 16n + 4w + i
+                        const int w = 2 * h + e;
+                        mma16816<false>(o[4 * w + 0], a, e4m3_pair_to_h2_lo8<0>(w0[e], w1[e]),
+                                        e4m3_pair_to_h2_lo8<0>(w2[e], w3[e]));
+                        mma16816<false>(o[4 * w + 1], a, e4m3_pair_to_h2_lo8<1>(w0[e], w1[e]),
+                                        e4m3_pair_to_h2_lo8<1>(w2[e], w3[e]));
+                        mma16816<false>(o[4 * w + 2], a, e4m3_pair_to_h2_lo8<2>(w0[e], w1[e]),
+                                        e4m3_pair_to_h2_lo8<2>(w2[e], w3[e]));
+                        mma16816<false>(o[4 * w + 3], a, e4m3_pair_to_h2_lo8<3>(w0[e], w1[e]),
+                                        e4m3_pair_to_h2_lo8<3>(w2[e], w3[e]));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    const int key = wn * C::NW + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int ch = 2 * j + (lane >> 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(b0, b1, b2, b3, smem_u32(tV + swz(key, ch, C::ROW16)));
+                    mma16816<C::MMA_BF16>(o[2 * j], a, b0, b1);
+                    mma16816<C::MMA_BF16>(o[2 * j + 1], a, b2, b3);
+                }
             }
         }
     }
@@ -543,9 +586,20 @@ __global__ void __launch_bounds__(128, C::MIN_BLOCKS) fwd_mma_kernel(const FwdPa
         const int lr = wm * 16 + (lane >> 2);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) {
-            const int col = i * 8 + 2 * (lane & 3);
-            *reinterpret_cast<float2 *>(&sO[(wn * ROWS + lr) * C::OSTRIDE + col]) = make_float2(o[i][0], o[i][1]);
-            *reinterpret_cast<float2 *>(&sO[(wn * ROWS + lr + 8) * C::OSTRIDE + col]) = make_float2(o[i][2], o[i][3]);
+            if constexpr (C::VDIRECT) {
+                // permuted order: n8 tile i, columns 2t and 2t + 1 are dims
+                // 32t + i and 32t + 16 + i
+                const int c0 = 32 * (lane & 3) + i;
+                sO[(wn * ROWS + lr) * C::OSTRIDE + c0] = o[i][0];
+                sO[(wn * ROWS + lr) * C::OSTRIDE + c0 + 16] = o[i][1];
+                sO[(wn * ROWS + lr + 8) * C::OSTRIDE + c0] = o[i][2];
+                sO[(wn * ROWS + lr + 8) * C::OSTRIDE + c0 + 16] = o[i][3];
+            } else {
+                const int col = i * 8 + 2 * (lane & 3);
+                *reinterpret_cast<float2 *>(&sO[(wn * ROWS + lr) * C::OSTRIDE + col]) = make_float2(o[i][0], o[i][1]);
+                *reinterpret_cast<float2 *>(&sO[(wn * ROWS + lr + 8) * C::OSTRIDE + col]) =
+                    make_float2(o[i][2], o[i][3]);
+            }
         }
         if ((lane & 3) == 0) {
             sM[wn * ROWS + lr] = m[0];

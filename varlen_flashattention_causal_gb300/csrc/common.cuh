@@ -58,6 +58,18 @@ __device__ __forceinline__ void e4m3x4_to_h2x2_lo8(uint32_t w, uint32_t &lo, uin
 // 2^8: the factor e4m3x4_to_h2x2_lo8 leaves out
 constexpr float kE4m3Lo8Scale = 256.f;
 
+// Byte I of x and byte I of y (two e4m3 values) as one fp16x2 register of
+// value * 2^-8 (x's value in the low half): the same field placement as
+// e4m3x4_to_h2x2_lo8, with prmt taking one byte from each register
+template <int I>
+__device__ __forceinline__ uint32_t e4m3_pair_to_h2_lo8(uint32_t x, uint32_t y) {
+    static_assert(I >= 0 && I < 4, "byte index");
+    constexpr uint32_t sel = (uint32_t)I | ((8u | I) << 4) | ((4u + I) << 8) | ((12u + I) << 12);
+    uint32_t a;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(x), "r"(y), "n"(sel));
+    return (a << 7) & 0xBF80BF80u;
+}
+
 // ------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
