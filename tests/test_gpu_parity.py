@@ -349,6 +349,45 @@ def test_fp8_kv_verify_rows():
     assert_no_device_error()
 
 
+@pytest.mark.parametrize("G,q_lens", [(1, [1, 8, 5, 9, 2]), (2, [1, 4, 3, 5, 1]), (4, [1, 2, 2, 3, 1]),
+                                       (8, [1, 1, 2, 1, 1])])
+@pytest.mark.parametrize("q_kind", ["bf16", "fp16", "e4m3"])
+def test_fp8_rows_up_to_eight(G, q_lens, q_kind):
+    """e4m3 cache, head size 128, requests of up to 8 packed rows (the
+    transposed decode kernel: S^T = K Q^T, O^T = V^T P^T, 8-row CTAs) beside
+    requests of 9 to 36 rows (the 16- and 64-row kernels), for G = 1, 2, 4, 8:
+    the causal diagonal inside a tile (q_len > 1), kv_len below one tile,
+    ragged tails, split and unsplit, against the oracle."""
+    Hkv = 4
+    kv_lens = [700, 64, 33, 1000, 9]
+    qdt = torch.float16 if q_kind == "fp16" else torch.bfloat16
+    b = W.make_batch(q_lens, kv_lens, G * Hkv, Hkv, 128, 16, seed=70 + G, kv_dtype="fp8", q_dtype=qdt)
+    kc, vc = gpu_cache(b)
+    ck, cv = cpu_cache(b)
+    q, qs = b.q, 1.0
+    if q_kind == "e4m3":
+        qs = float(b.q.float().abs().max()) / 448.0
+        q = (b.q.float() / qs).to(torch.float8_e4m3fn)
+    ro, rl = oracle.attention(q, ck, cv, b.cu_seqlens_q, b.seqused_k, b.block_table, b.softmax_scale,
+                              k_scale=b.k_scale, v_scale=b.v_scale, q_scale=qs)
+    for ns in (1, 0, 5):
+        out, lse = gpu_attn(b, kc, vc, num_splits=ns, q=q, q_descale=qs)
+        check(out, lse, ro, rl, TOL_FP8)
+    assert_no_device_error()
+
+
+def test_fp8_paged_decode_entry_point():
+    """attn_paged_decode (one token per request, no cu_seqlens) on an e4m3
+    cache with bf16 queries, G = 4, split and unsplit, against the oracle."""
+    b = W.make_batch([1] * 6, [1, 63, 64, 65, 777, 2048], 32, 8, 128, 16, seed=77, kv_dtype="fp8")
+    kc, vc = gpu_cache(b)
+    ro, rl = ref_attn(b, *cpu_cache(b))
+    for ns in (1, 0, 4):
+        out, lse = gpu_decode(b, kc, vc, num_splits=ns)
+        check(out, lse, ro, rl, TOL_FP8)
+    assert_no_device_error()
+
+
 # ------------------------------------------------------------- edge cases
 
 def test_empty_and_degenerate_requests():
@@ -412,6 +451,28 @@ def test_out_of_range_block_id_reads_zeros_and_is_flagged():
     cv[blk] = 0
     ro, rl = ref_attn(b, ck, cv)
     check(out[1:], lse[1:], ro[1:], rl[1:], TOL)
+
+
+def test_out_of_range_block_id_fp8_decode_rows():
+    """The same contract on the e4m3 decode path (rows <= 8, head size 128):
+    the bad block's 16 slots read as zero K and V, the error word records it,
+    the other requests are untouched."""
+    b = W.make_batch([1, 1, 2], [100, 64, 90], 16, 4, 128, 16, seed=14, kv_dtype="fp8")
+    kc, vc = gpu_cache(b)
+    bad = b.block_table.clone()
+    bad[1, 1] = b.num_blocks + 7         # keys 16..31 of request 1
+    out, lse = gpu_attn(b, kc, vc, block_table=bad, num_splits=1)
+    assert va.attn_device_error_flag(reset=True) & va.ERR_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    ck, cv = cpu_cache(b)
+    ro, rl = ref_attn(b, ck, cv)
+    keep = torch.tensor([True, False, True, True])    # tokens of requests 0 and 2
+    check(out[keep], lse[keep], ro[keep], rl[keep], TOL_FP8)
+    blk = int(b.block_table[1, 1])
+    ck[blk] = 0
+    cv[blk] = 0
+    ro, rl = ref_attn(b, ck, cv)
+    check(out[1:2], lse[1:2], ro[1:2], rl[1:2], TOL_FP8)
 
 
 def test_debug_validation_refuses_bad_tables_and_launches_nothing(monkeypatch):

@@ -96,7 +96,9 @@ constexpr size_t kSchedBytes = 256;
 
 // Request classes by packed row count (q_len * G):
 //   0  rows <= 16: decode and short verify rows, mma.sync kernel with 16-row
-//      CTAs (one token x up to 16 heads of a group);
+//      CTAs (one token x up to 16 heads of a group).  On an e4m3 cache with
+//      head size 128 this class ends at 8 rows and runs the transposed
+//      decode kernel (8-row CTAs); class 1 then starts at 9 rows;
 //   1  17 .. 64 rows: longer verify rows and short chunks, mma.sync kernel
 //      with 32- or 64-row CTAs (memory-bound work, where a 128-row
 //      tensor-core tile would mostly be padding);
@@ -126,6 +128,7 @@ struct ClassPlan {
     bool on;       // launched
     int lo, hi;    // packed-row range of the class
     bool tc;       // tcgen05 kernel (else mma.sync with rpc rows per CTA)
+    bool dec;      // transposed decode kernel (class 0 on e4m3 caches)
     int rpc;       // rows per CTA
     int ns;        // segments (automatic choice)
 };
@@ -141,7 +144,9 @@ Plan make_plan(int B, int max_q, int max_k, bool uniform, int Hq, int Hkv, int D
     const int G = Hq / Hkv;
     const int max_rows = std::max(1, max_q) * G;
     const bool heavy_tc = tc_supported(D, q_dtype, kv_dtype, G);
-    const int hi[3] = {kLightRows, heavy_tc ? kMidRows : INT32_MAX, INT32_MAX};
+    const bool dec = dec_supported(D, q_dtype, kv_dtype);
+    const int light = dec ? dec_rows_per_cta() : kLightRows;
+    const int hi[3] = {light, heavy_tc ? kMidRows : INT32_MAX, INT32_MAX};
     for (int k = 0; k < 3; ++k) {
         ClassPlan &c = pl.c[k];
         c.lo = k == 0 ? 0 : hi[k - 1] + 1;
@@ -152,10 +157,11 @@ Plan make_plan(int B, int max_q, int max_k, bool uniform, int Hq, int Hkv, int D
         c.on = uniform ? (max_rows >= c.lo && max_rows <= c.hi) : (max_rows >= c.lo && G <= c.hi);
         if (!c.on) continue;
         c.tc = (k == 2);
+        c.dec = (k == 0 && dec);
         const int rows_cap = std::min(max_rows, c.hi);
         // (class 1 on 16-row CTAs, each row block re-reading K/V from L2,
         // measured slower than one CTA for all of a request's rows)
-        c.rpc = c.tc ? tc_rows_per_cta() : (k == 0 ? kLightRows : mma_rows_per_cta(rows_cap));
+        c.rpc = c.tc ? tc_rows_per_cta() : (k == 0 ? light : mma_rows_per_cta(rows_cap));
         const long long rb = (rows_cap + c.rpc - 1) / c.rpc;
         if (k == 0)        // decode-like rows: also bound the keys per segment (32 tiles)
             c.ns = split_rule((long long)B * Hkv * rb, max_k, 6LL * sms, 2, 32);
@@ -341,6 +347,10 @@ attn_status launch_classes(const FwdArgs &a, const FwdParams &p, const Plan &pl,
             st = check_cuda(launch_fwd_tc2(t, a.q_dtype, a.T, dev->sms, stream));
         else if (c.tc)
             st = check_cuda(launch_fwd_tc(t, a.q_dtype, a.kv_dtype, a.T, dev->sms, stream));
+        else if (c.dec && dec_pool_fits(a.num_blocks, a.bs))
+            st = check_cuda(launch_fwd_dec(t, a.q_dtype, stream));
+        else if (c.dec)   // the 16-row kernel takes any rows <= 8 too
+            st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, mma_rows_per_cta(c.hi), a.max_q <= 1, stream));
         else
             st = check_cuda(launch_fwd_mma(t, a.D, a.q_dtype, a.kv_dtype, c.rpc, a.max_q <= 1, stream));
         if (st != ATTN_OK) return st;

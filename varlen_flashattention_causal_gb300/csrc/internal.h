@@ -118,6 +118,16 @@ __host__ __device__ inline int tile_kind(int q_lo, int q_hi, int k_lo, int k_hi,
 // rows per CTA of the mma kernel for a given largest packed row count
 int mma_rows_per_cta(int max_rows);
 
+// decode-shape kernel on transposed tiles (e4m3 cache, head size 128): whether
+// it takes the shape, its rows per CTA (requests of up to that many packed
+// rows), and its launcher
+bool dec_supported(int D, int q_dtype, int kv_dtype);
+// its TMA maps address cache slots with 32-bit coordinates: the pool's
+// num_blocks * bs slots must stay below 2^31 (else the 16-row kernel runs)
+bool dec_pool_fits(int num_blocks, int bs);
+int dec_rows_per_cta();
+cudaError_t launch_fwd_dec(const FwdParams &p, int q_dtype, cudaStream_t stream);
+
 // tcgen05 kernel: whether it handles this shape, rows per CTA, launcher
 bool tc_supported(int D, int q_dtype, int kv_dtype, int G);
 int tc_rows_per_cta();
