@@ -60,11 +60,11 @@ L2_BYTES = 129 * 1024 * 1024
 # metrics (its summary under profiles/ gives the command).  It is reported only while
 # the kernel's sources hash to the value recorded with the capture.
 DECODE_TRAFFIC = {
-    "bytes": 593427712 + 5385216,        # dram__bytes_read.sum + dram__bytes_write.sum, 4 segments
+    "bytes": 593428480 + 5424640,        # dram__bytes_read.sum + dram__bytes_write.sum, 4 segments
     "sources": ["varlen_flashattention_causal_gb300/csrc/attn_mma.cu",
                 "varlen_flashattention_causal_gb300/csrc/common.cuh",
                 "varlen_flashattention_causal_gb300/csrc/internal.h"],
-    "sha256": "81bfe6479aa56a32ca68e0eb685dc63edee42318a39929c3899e4154f5c9dce7",
+    "sha256": "2c561e466aaf2a6cde3139e63656fdbd1a24f82f66cb9348ffeeb833a01e602e",
 }
 
 
@@ -466,6 +466,7 @@ def wl_fp8decode(va, dev, steps, warmup, pk):
     best = max(lines.values(), key=lambda x: x["gbs"])
     return {"workload": "paged decode, Llama-3-8B shaped, e4m3 cache (per-tensor amax/448 scales)",
             "metric": "fp8-KV decode GB/s", "value": best["gbs"], "unit": "GB/s", "ms": best["ms"],
+            "kernel": "fwd_dec_kernel (S^T = K Q^T, O^T = V^T P^T, 8-row CTAs, TMA tile gather) + combine_light_kernel",
             "bytes": by, "variants": lines,
             "roofline": roofline("hbm", by, best["ms"], hbm, "GB/s"), "clocks": clocks}
 

@@ -62,7 +62,7 @@ struct DecCfg {
     // CTAs per SM the registers are capped for (fp16 queries hold three
     // e4m3 terms of Q: one CTA fewer, no spills)
     static constexpr int MINB = (QT == DT_FP16) ? MINB_ - 1 : MINB_;
-    static constexpr int STAGES = STAGES_;          // K/V tiles in the cp.async ring
+    static constexpr int STAGES = STAGES_;          // K/V tiles in each warp's TMA ring
     static constexpr int D = 128;                   // head size
     static constexpr int ROWS = 8;                  // packed rows per CTA (the N side)
     static constexpr int BN = 64;                   // keys per K/V tile
@@ -84,7 +84,7 @@ struct DecCfg {
     static constexpr int NBARS = STAGES * NWARP;    // one per (stage, warp)
     // + 1 KB: the ring is aligned up to 1024 bytes (the 128-byte swizzle's period)
     static constexpr int SMEM = 1024 + BARS_OFF + NBARS * 8 + 16;
-    static_assert(NW == 16 && CH == 8, "the gather: two lanes a row, four copy rounds");
+    static_assert(NW == 16 && CH == 8, "one 16-slot TMA box of 128-byte rows per warp and tile");
 };
 
 // transpose of an 8 x 8 matrix of 16-bit values held one row pair per lane
