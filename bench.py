@@ -450,7 +450,7 @@ def wl_fp8decode(va, dev, steps, warmup, pk):
     b = W.decode_llama8b(gen_kv=False)
     kc, vc, ks, vs = _device_cache(b, dev, torch.float8_e4m3fn)
     su, bt, cu = b.seqused_k.to(dev), b.block_table.to(dev), b.cu_seqlens_q.to(dev)
-    ns = va.attn_num_splits(b.B, 1, b.max_seqlen_k, b.Hq, b.Hkv, sms)
+    ns = va.attn_num_splits(b.B, 1, b.max_seqlen_k, b.Hq, b.Hkv, sms, b.D, va.ATTN_BF16, va.ATTN_FP8_E4M3)
     wsp = torch.empty(va.attn_workspace_size(b.B, b.Hq, b.D, ns), dtype=torch.uint8, device=dev)
     by = decode_bytes(b, elem=1)
     q8, qs = _q8(b.q)
@@ -506,7 +506,8 @@ def wl_fp8mixed(va, dev, steps, warmup, pk):
     kc, vc, ks, vs = _device_cache(b, dev, torch.float8_e4m3fn)
     q, out = b.q.to(dev), torch.empty(b.q.shape, dtype=torch.bfloat16, device=dev)
     cu, su, bt = b.cu_seqlens_q.to(dev), b.seqused_k.to(dev), b.block_table.to(dev)
-    ns = va.attn_num_splits(b.B, b.max_seqlen_q, b.max_seqlen_k, b.Hq, b.Hkv, sms)
+    ns = va.attn_num_splits(b.B, b.max_seqlen_q, b.max_seqlen_k, b.Hq, b.Hkv, sms, b.D, va.ATTN_BF16,
+                            va.ATTN_FP8_E4M3)
     wsp = torch.empty(va.attn_workspace_size(b.T, b.Hq, b.D, ns), dtype=torch.uint8, device=dev)
     fn = lambda: va.attn_varlen_prefill(q, kc, vc, out, cu, su, bt, b.max_seqlen_q, b.max_seqlen_k,
                                         b.softmax_scale, causal=True, k_descale=ks, v_descale=vs,

@@ -286,11 +286,23 @@ size_t attn_workspace_size(int total_q, int Hq, int D, int num_splits);
 
 /*
  * attn_num_splits -- the split count attn_varlen_prefill(num_splits = 0)
- * would choose for these host scalars on the current device (the decode
+ * would choose for these host scalars with bf16 query and cache at head
+ * size 128 (attn_num_splits_typed: any head size and dtypes) (the decode
  * rule: enough segments to fill every SM a few times over, each segment at
  * least a few K/V tiles long).  Exposed for planning and tests.
  */
 int attn_num_splits(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int num_sms);
+
+/*
+ * attn_num_splits_typed -- the same choice for a given head size and query /
+ * cache dtypes (the request classes and their kernels depend on them: an
+ * e4m3 cache at head size 128 runs decode rows on its own kernel with its
+ * own split target).  attn_num_splits is this call with D = 128 and bf16
+ * query and cache.  Size a workspace with it for num_splits = 0 calls on
+ * other dtypes.  Returns 1 for invalid head counts.
+ */
+int attn_num_splits_typed(int B, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D, attn_dtype q_dtype,
+                          attn_dtype kv_dtype, int num_sms);
 
 /*
  * attn_tile_kind -- [MR] sec. 4 tile classification for a query tile holding

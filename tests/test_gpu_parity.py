@@ -111,8 +111,9 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-def ws_bytes_for(T, Hq, D, B, max_q, max_k, Hkv, num_splits):
-    ns = num_splits if num_splits > 0 else va.attn_num_splits(B, max_q, max_k, Hq, Hkv, _sms())
+def ws_bytes_for(T, Hq, D, B, max_q, max_k, Hkv, num_splits, q_dtype=None, kv_dtype=None):
+    ns = num_splits if num_splits > 0 else va.attn_num_splits(B, max_q, max_k, Hq, Hkv, _sms(), D, q_dtype,
+                                                              kv_dtype)
     return va.attn_workspace_size(T, Hq, D, ns)
 
 
@@ -129,7 +130,8 @@ def gpu_attn(b, kc, vc, num_splits=0, causal=None, q=None, block_table=None, seq
     cu = (b.cu_seqlens_q if cu is None else cu).cuda()
     mq = b.max_seqlen_q if max_q is None else max_q
     mk = b.max_seqlen_k if max_k is None else max_k
-    g = Guarded(T, Hq, D, odt, ws_bytes_for(T, Hq, D, su.numel(), mq, mk, b.Hkv, num_splits))
+    g = Guarded(T, Hq, D, odt, ws_bytes_for(T, Hq, D, su.numel(), mq, mk, b.Hkv, num_splits, va._dt(q),
+                                            va._dt(kc)))
     va.attn_varlen_prefill(q, kc, vc, g.out, cu, su, bt, mq, mk, b.softmax_scale,
                            causal=b.causal if causal is None else causal, lse_out=g.lse,
                            q_descale=q_descale,
@@ -145,7 +147,8 @@ def gpu_decode(b, kc, vc, num_splits=0, q=None):
     rows, NaN-filled workspace); checks the guards after the call."""
     q = (b.q if q is None else q).cuda()
     B, Hq, D = q.shape
-    g = Guarded(B, Hq, D, q.dtype, ws_bytes_for(B, Hq, D, B, 1, b.max_seqlen_k, b.Hkv, num_splits),
+    g = Guarded(B, Hq, D, q.dtype, ws_bytes_for(B, Hq, D, B, 1, b.max_seqlen_k, b.Hkv, num_splits, va._dt(q),
+                                                va._dt(kc)),
                 contiguous=True)
     va.attn_paged_decode(q, kc, vc, g.out, b.seqused_k.cuda(), b.block_table.cuda(), b.max_seqlen_k,
                          b.softmax_scale, lse_out=g.lse, num_splits=num_splits, workspace=g.ws,

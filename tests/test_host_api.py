@@ -205,6 +205,15 @@ def test_workspace_and_split_rules(lib):
     for B, L in ((64, 4096), (4, 32768), (128, 16384), (1, 2048)):
         s = va.attn_num_splits(B, 1, L, 32, 8, 152)
         assert 1 <= s <= 256 and (L // 64) >= s or s == 1
+    # the typed form: bf16 at head size 128 is attn_num_splits itself; an
+    # e4m3 cache runs decode rows on the transposed kernel, whose target is
+    # eight CTAs an SM (5 segments on the decode benchmark shape)
+    E4M3 = va.ATTN_FP8_E4M3
+    assert va.attn_num_splits_typed(64, 1, 4060, 32, 8, 128, va.ATTN_BF16, va.ATTN_BF16, 152) == 4
+    assert va.attn_num_splits_typed(64, 1, 4060, 32, 8, 128, va.ATTN_BF16, E4M3, 152) == 5
+    assert va.attn_num_splits_typed(64, 1, 4060, 32, 8, 128, E4M3, E4M3, 152) == 5
+    assert va.attn_num_splits_typed(64, 1, 4060, 32, 8, 64, va.ATTN_BF16, E4M3, 152) == 4   # 16-row kernel
+    assert va.attn_num_splits_typed(64, 1, 4060, 30, 8, 128, va.ATTN_BF16, E4M3, 152) == 1  # Hq % Hkv
 
 
 def prefill_ext(lib, wl=-1, wr=-1, cap=0.0, sinks=None, **kw):

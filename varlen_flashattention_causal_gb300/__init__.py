@@ -20,7 +20,7 @@ from . import build as _build
 __all__ = [
     "AttnError", "attn_varlen_prefill", "attn_varlen_prefill_ext", "attn_paged_decode",
     "attn_paged_decode_noalloc", "attn_merge_states", "kv_cache_write", "attn_workspace_size",
-    "attn_num_splits", "attn_tile_kind", "attn_status_string", "attn_device_error_flag",
+    "attn_num_splits", "attn_num_splits_typed", "attn_tile_kind", "attn_status_string", "attn_device_error_flag",
     "attn_selftest_wait_timeout", "attn_validate_tables", "attn_validate_slots", "attn_cascade",
     "attn_cascade_splits",
     "attn_debug_validate_enabled", "library_path",
@@ -80,6 +80,8 @@ def _load():
     lib.attn_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.attn_num_splits.restype = i32
     lib.attn_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.attn_num_splits_typed.restype = i32
+    lib.attn_num_splits_typed.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32]
     lib.attn_tile_kind.restype = i32
     lib.attn_tile_kind.argtypes = [i32, i32, i32, i32, i32]
     lib.attn_status_string.restype = c.c_char_p
@@ -178,7 +180,7 @@ def attn_varlen_prefill(q, k_cache, v_cache, out, cu_seqlens_q, seqused_k, block
     # the workspace is sized for the largest split count the library may
     # choose; with num_splits = 0 it picks a count per request class itself
     ns = num_splits if num_splits > 0 else attn_num_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv,
-                                                           _sms(q.device))
+                                                           _sms(q.device), D, _dt(q), _dt(k_cache))
     ws, ws_bytes = _workspace(T, Hq, D, ns, q.device, workspace)
     if sinks is not None and (sinks.dtype != torch.float32 or sinks.numel() != Hq or not sinks.is_contiguous()
                               or not sinks.is_cuda):
@@ -210,7 +212,8 @@ def attn_paged_decode(q, k_cache, v_cache, out, seq_lens, block_table, max_seq_l
     _i32(seq_lens, "seq_lens")
     if block_table.dtype != torch.int32 or block_table.stride(-1) != 1:
         raise TypeError("block_table must be int32 with unit column stride")
-    ns = num_splits if num_splits > 0 else attn_num_splits(B, 1, max_seq_len, Hq, Hkv, _sms(q.device))
+    ns = num_splits if num_splits > 0 else attn_num_splits(B, 1, max_seq_len, Hq, Hkv, _sms(q.device), D,
+                                                           _dt(q), _dt(k_cache))
     ws, ws_bytes = _workspace(B, Hq, D, ns, q.device, workspace)
     st = lib.attn_paged_decode(
         _p(q), _p(k_cache), _p(v_cache), _p(out), _p(lse_out), _p(seq_lens), _p(block_table),
@@ -300,9 +303,20 @@ def attn_workspace_size(total_q, Hq, D, num_splits):
     return int(_load().attn_workspace_size(int(total_q), int(Hq), int(D), int(num_splits)))
 
 
-def attn_num_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, num_sms):
-    return int(_load().attn_num_splits(int(B), int(max_seqlen_q), int(max_seqlen_k), int(Hq), int(Hkv),
-                                       int(num_sms)))
+def attn_num_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, num_sms, D=None, q_dtype=None, kv_dtype=None):
+    """The automatic split count; with D / q_dtype / kv_dtype (ATTN_* codes)
+    given, attn_num_splits_typed for them (defaults 128, bf16, bf16)."""
+    if D is None and q_dtype is None and kv_dtype is None:
+        return int(_load().attn_num_splits(int(B), int(max_seqlen_q), int(max_seqlen_k), int(Hq), int(Hkv),
+                                           int(num_sms)))
+    return int(_load().attn_num_splits_typed(int(B), int(max_seqlen_q), int(max_seqlen_k), int(Hq), int(Hkv),
+                                             128 if D is None else int(D),
+                                             ATTN_BF16 if q_dtype is None else int(q_dtype),
+                                             ATTN_BF16 if kv_dtype is None else int(kv_dtype), int(num_sms)))
+
+
+def attn_num_splits_typed(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, q_dtype, kv_dtype, num_sms):
+    return attn_num_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, num_sms, D, q_dtype, kv_dtype)
 
 
 def attn_tile_kind(q_lo, q_hi, k_lo, k_hi, ctx):
