@@ -8,8 +8,10 @@
 // tile at G = 4 is half padding instead of three quarters.  Against the
 // 16-row kernel that halves the tensor work per key and halves the
 // accumulators: O^T is 8 rows x 128 dims, 32 fp32 values a lane.  The
-// freed registers let more CTAs share an SM, which is what this HBM-bound,
-// latency-bound loop needs to keep enough copies in flight.
+// freed registers let five CTAs share an SM.  The loop is bound by
+// instruction issue and latency, not by HBM (with every read an L2 hit it
+// runs only a few percent faster), so more warps per scheduler and fewer
+// instructions per key are what move it.
 //
 // Work split, gather and masking follow the 16-row kernel.
 //  * One CTA is one request x one KV head x one block of 8 packed rows x one
